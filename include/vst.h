@@ -1,0 +1,176 @@
+/*
+ * vst.h -- C ABI of libvst: incremental sliding-window KV attention on one GB300 (sm_103a).
+ *
+ * The operation. A streaming audio-LLM runs its attention layers incrementally: each new
+ * chunk of frames (encoder) or each new token (decoder) attends, under a windowed-causal
+ * mask keyed on absolute positions, to keys/values cached from earlier calls. The
+ * definition followed here is the offline one: for a query at absolute position i and
+ * query head h,
+ *
+ *     out = sum_j softmax_j( RoPE(q_i, i) . RoPE(k_j, j) / sqrt(D) ) v_j,
+ *     over absolute positions j with 0 <= i - j < W, KV head h / (H / Hk),
+ *
+ * with NEOX (rotate-half) RoPE, theta = 1e6. Sources: "Voxtral Realtime -- incremental
+ * streaming implementation plan", sections "SHIPPED" (Mechanism: encoder cache with
+ * sliding_window=750 under a windowed-causal mask, decoder persistent sliding KV(8192)) and
+ * "Unbounded length (shipped)" (1536-slot encoder ring, compaction that copies the last 750
+ * frames to the front, feeds pushed in <= 512-frame batches, mask on absolute positions);
+ * "Voxtral Realtime" family doc, "Architecture (summary)" (encoder: NEOX RoPE theta=1e6,
+ * head dim 64, sliding window 750; decoder: GQA 32q/8kv, head dim 128, sliding 8192) and
+ * Capability Validation, Streaming row, item (5) (decoder modulo ring: token cur writes
+ * slot cur % n_ctx and the mask reveals [cur-8191, cur]; positions stay absolute).
+ *
+ * The shape of the API follows "Stateless modules and streaming contexts" (bunsen book),
+ * sections "The principle: state is injected" and "The pattern": a config builds an
+ * immutable module (here: the fixed RoPE cos/sin table), and each stream's cache context
+ * is made by the caller and passed in on every call, so one module serves many streams and
+ * a batch of streams can run through one launch.
+ *
+ * Conventions.
+ *   - bf16 tensors are passed as device pointers (void*), row-major, 16-byte aligned.
+ *     q / out: [rows][H][D]; k / v: [rows][Hk][D].
+ *   - `stream` is a cudaStream_t passed as void*. Every call only enqueues work on it and
+ *     returns; no call synchronises the device. Host-side state (positions, ring fill)
+ *     advances when the call returns, so calls on one ctx must stay on one stream (or be
+ *     ordered by the caller).
+ *   - A ctx is used by one host thread at a time. Contexts are independent of each other.
+ *   - Errors: argument and config errors return before anything is enqueued and leave the
+ *     ctx unchanged. A CUDA error while enqueueing marks the ctx failed: later calls on it
+ *     return VST_E_STATE until vst_ctx_reset.
+ *   - Inputs must be finite. Ring slots that are never written are zeroed at create/reset.
+ */
+#ifndef VST_H
+#define VST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VST_API __attribute__((visibility("default")))
+#else
+#define VST_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    VST_OK = 0,
+    VST_E_INVAL = -1,       /* bad argument (null pointer, size, position past the table) */
+    VST_E_UNSUPPORTED = -2, /* configuration this build has no kernel for */
+    VST_E_CUDA = -3,        /* a CUDA runtime call failed */
+    VST_E_STATE = -4,       /* ctx is failed (earlier CUDA error) or of the wrong kind */
+    VST_E_TIMEOUT = -5,     /* a kernel gave up on a bounded wait (reported by vst_ctx_check) */
+    VST_E_NOMEM = -6        /* caller memory too small, or cudaMalloc failed */
+} vst_status;
+
+typedef enum { VST_ENC = 1, VST_DEC = 2 } vst_kind;
+
+/* Configuration of one attention layer's cache. The two shapes the pages give are
+ *   encoder: kind VST_ENC, H = Hk = 20, D = 64, W = 750, ring 1536, max_batch 512
+ *   decoder: kind VST_DEC, H = 32, Hk = 8, D = 128, W = 8192, ring 8192 (or any multiple
+ *            of 128 >= W), max_batch 1
+ * with rope_theta 1e6 and max_position 131072 (the decoder's position cap, family doc,
+ * Streaming row, item (5)). Supported by this build: encoder D = 64 with H = Hk; decoder
+ * D = 128 with H = 4 * Hk. Other values return VST_E_UNSUPPORTED from vst_module_create. */
+typedef struct {
+    int32_t kind;         /* vst_kind */
+    int32_t n_heads;      /* H, query heads */
+    int32_t n_kv_heads;   /* Hk, key/value heads; H % Hk == 0 */
+    int32_t head_dim;     /* D */
+    int32_t window;       /* W: the query at position p sees keys p-W+1 .. p */
+    int32_t ring_slots;   /* R: cache rows per KV head */
+    int32_t max_batch;    /* encoder: frames appended per internal batch (<= 512) */
+    int32_t reserved;     /* must be 0 */
+    int64_t max_position; /* absolute positions must stay below this (RoPE table length) */
+    double rope_theta;    /* RoPE base */
+} vst_config;
+
+/* Fill *cfg with the pages' encoder (kind = VST_ENC) or decoder (VST_DEC) configuration. */
+VST_API vst_status vst_config_default(int32_t kind, vst_config* cfg);
+
+typedef struct vst_module vst_module; /* immutable: config + RoPE table on one device */
+typedef struct vst_ctx vst_ctx;       /* one (stream, layer) cache */
+
+/* Build the module on the current CUDA device: validates cfg, computes the RoPE cos/sin
+ * table on the host in double precision (angle p * theta^(-2i/D)), rounds it to fp32 and
+ * uploads it (device memory owned by the module, max_position * D * 4 bytes). Blocking. */
+VST_API vst_status vst_module_create(const vst_config* cfg, vst_module** out);
+VST_API vst_status vst_module_destroy(vst_module* m); /* all its contexts must be destroyed first */
+VST_API vst_status vst_module_config(const vst_module* m, vst_config* cfg);
+
+/* Device bytes one ctx of this module needs (rings + scratch), a multiple of 256. */
+VST_API size_t vst_ctx_bytes(const vst_module* m);
+
+/* Create a ctx. dev_mem: caller-owned device memory of at least vst_ctx_bytes(m) bytes,
+ * 256-byte aligned, that must outlive the ctx; or NULL, and the library allocates it with
+ * cudaMalloc and frees it in vst_ctx_destroy. The ring is zeroed on `stream`. */
+VST_API vst_status vst_ctx_create(const vst_module* m, void* dev_mem, size_t bytes, void* stream,
+                          vst_ctx** out);
+/* Forget the stream (positions back to 0, ring empty, failure cleared) and zero the ring on
+ * `stream`; memory is kept (streaming plan, "Per-hook behavior": stream_reset). */
+VST_API vst_status vst_ctx_reset(vst_ctx* c, void* stream);
+VST_API vst_status vst_ctx_destroy(vst_ctx* c);
+
+typedef struct {
+    int32_t kind;
+    int32_t failed;         /* 1 after a CUDA error, until reset */
+    int64_t n_kv;           /* encoder: ring rows in use, slots [0, n_kv) */
+    int64_t abs_base;       /* encoder: absolute position held by slot 0 */
+    int64_t abs_next;       /* absolute position of the next frame/token */
+    int64_t n_compactions;  /* encoder compactions enqueued so far */
+    void* k_ring;           /* device [Hk][R][D] bf16, RoPE already applied */
+    void* v_ring;           /* device [Hk][R][D] bf16 */
+} vst_ctx_info;
+VST_API vst_status vst_ctx_info_get(const vst_ctx* c, vst_ctx_info* out);
+
+/* Read the ctx's device error word (blocking: synchronises `stream`). Returns VST_OK, or
+ * VST_E_TIMEOUT when a kernel of this ctx abandoned a bounded wait, and clears the word. */
+VST_API vst_status vst_ctx_check(vst_ctx* c, void* stream);
+
+/* ---- encoder chunk path (streaming plan, "SHIPPED" and "Unbounded length") -------------
+ * Feed n_new >= 0 frames: q [n_new][H][D], k/v [n_new][Hk][D] -> out [n_new][H][D]. Frames
+ * get absolute positions abs_next .. abs_next + n_new - 1. The feed is pushed in batches of
+ * at most max_batch; before a batch that would not fit in the ring, the last W rows are
+ * copied to the front (compaction); each batch's K (rotated) and V are appended at ring
+ * rows [n_kv, n_kv + b), then every new frame attends to the window [p - W + 1, p]. The
+ * output does not depend on how a stream is cut into feeds (bit for bit). */
+VST_API vst_status vst_enc_feed(vst_ctx* c, const void* q, const void* k, const void* v, int32_t n_new,
+                        void* out, void* stream);
+/* The same for n_ctx contexts of one module in lockstep (one launch per kernel): tensors
+ * are stacked per ctx, q [n_ctx][n_new][H][D], k/v [n_ctx][n_new][Hk][D], out like q. The
+ * contexts must be distinct; their positions and ring fills may differ. */
+VST_API vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q, const void* k,
+                              const void* v, int32_t n_new, void* out, void* stream);
+/* Compact now, whatever the fill (keeps the last W rows); no-op when n_kv <= W. */
+VST_API vst_status vst_ctx_compact(vst_ctx* c, void* stream);
+
+/* Host-only: the schedule vst_enc_feed would enqueue for a ctx in state (n_kv, abs_base)
+ * fed n_new frames. Writes up to max_steps entries: batch[i] frames appended in step i,
+ * compact[i] = 1 if a compaction precedes it. Returns the step count in *n_steps and the
+ * final state in *n_kv_out / *abs_base_out. Needs no GPU. */
+VST_API vst_status vst_enc_plan(const vst_config* cfg, int64_t n_kv, int64_t abs_base, int32_t n_new,
+                        int32_t* batch, int32_t* compact, int32_t max_steps, int32_t* n_steps,
+                        int64_t* n_kv_out, int64_t* abs_base_out);
+
+/* ---- decoder step path (family doc, Streaming row, item (5)) ---------------------------
+ * One token per stream: for each of n_streams contexts (one module, distinct), token s is
+ * at absolute position pos_s = abs_next of ctxs[s]; its K (rotated) and V go to ring slot
+ * pos_s % R, then its query attends keys [max(0, pos_s - W + 1), pos_s].
+ * q [n_streams][H][D], k/v [n_streams][Hk][D], out [n_streams][H][D]. */
+VST_API vst_status vst_dec_step(vst_ctx* const* ctxs, int32_t n_streams, const void* q, const void* k,
+                        const void* v, void* out, void* stream);
+/* Append n tokens of K/V (no attention) at positions abs_next .. abs_next + n - 1 of one
+ * decoder ctx: k/v [n][Hk][D]. Used to fill a cache. */
+VST_API vst_status vst_dec_append(vst_ctx* c, const void* k, const void* v, int32_t n, void* stream);
+
+VST_API const char* vst_status_str(vst_status s);
+/* Library version, "major.minor.patch". */
+VST_API const char* vst_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VST_H */

@@ -160,9 +160,8 @@ def attention_row(q_bits, k_bits, v_bits, i: int, window: int, theta: float = TH
         raise ValueError("window slice has %d rows, expected %d" % (n, min(window, i + 1)))
     j0 = i - n + 1
     H, D = q_bits.shape
-    qfull = np.zeros((n, H, D), dtype=np.uint16)
-    qfull[-1] = q_bits
-    qr = rope_rows(qfull, j0, theta)
+    qr = np.zeros((n, H, D), dtype=np.float64)
+    qr[-1] = rope_rows(np.ascontiguousarray(q_bits)[None], i, theta)[0]
     kr = rope_rows(k_bits, j0, theta)
     vv = bf16_to_double(v_bits)
     return attend(qr, kr, vv, n, rows=(n - 1, n))[0]

@@ -1,0 +1,647 @@
+// vst_api.cu -- host side of libvst: configuration checks, the module (RoPE table), the
+// per-stream contexts and their bookkeeping, and the batched launchers (kernel e) that
+// turn one API call over many contexts into one launch per kernel.
+//
+// Bookkeeping follows the streaming plan ("Voxtral Realtime -- incremental streaming
+// implementation plan", "Unbounded length (shipped)"): the encoder ring holds rows
+// [0, n_kv) = absolute frames [abs_base, abs_base + n_kv); a feed is pushed in batches of
+// at most max_batch frames; a batch that would not fit first triggers a compaction that
+// keeps the last W rows. All of it is known on the host, so no call ever waits for the GPU.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "vst_internal.h"
+
+using namespace vst;
+
+struct vst_module {
+    vst_config cfg;
+    int device;
+    float2* rope;  // device [max_position][D/2]
+    int splits;    // decoder: split slots per step (S)
+};
+
+struct vst_ctx {
+    const vst_module* m;
+    uint8_t* mem;
+    bool owns;
+    size_t bytes;
+    __nv_bfloat16* k_ring;
+    __nv_bfloat16* v_ring;
+    float* part_ml;
+    float* part_o;
+    unsigned* counters;
+    int* err;
+    const CUtensorMap* tmap_k;
+    const CUtensorMap* tmap_v;
+    int64_t n_kv, abs_base, abs_next, n_compactions;
+    int failed;
+    CUtensorMap host_maps[2];
+};
+
+namespace {
+
+struct Layout {
+    size_t k_off, v_off, ml_off, o_off, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int dec_splits(const vst_config& c) { return (c.window - 1 + kDecSplit - 1) / kDecSplit + 1; }
+
+Layout layout_of(const vst_config& c)
+{
+    Layout L{};
+    const size_t ring = (size_t)c.n_kv_heads * c.ring_slots * c.head_dim * sizeof(__nv_bfloat16);
+    L.k_off = kCtxHeaderBytes;
+    L.v_off = align256(L.k_off + ring);
+    size_t end = align256(L.v_off + ring);
+    if (c.kind == VST_DEC) {
+        const size_t S = (size_t)dec_splits(c);
+        L.ml_off = end;
+        L.o_off = align256(L.ml_off + (size_t)c.n_heads * S * 2 * sizeof(float));
+        end = align256(L.o_off + (size_t)c.n_heads * S * c.head_dim * sizeof(float));
+    }
+    L.total = end;
+    return L;
+}
+
+vst_status check_config(const vst_config* c)
+{
+    if (!c)
+        return VST_E_INVAL;
+    if (c->reserved != 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+        c->window <= 0 || c->ring_slots <= 0 || c->max_position <= 0 || !(c->rope_theta > 0.0) ||
+        c->n_heads % c->n_kv_heads != 0)
+        return VST_E_INVAL;
+    if (c->kind == VST_ENC) {
+        if (c->max_batch <= 0 || (long long)c->window + c->max_batch > c->ring_slots)
+            return VST_E_INVAL;
+        // kernels (a), (b), (d): head dim 64, one KV head per query head, a compaction plane
+        // of at most 128 KB, batches of at most 512 frames.
+        if (c->head_dim != 64 || c->n_heads != c->n_kv_heads || c->max_batch > 512 ||
+            (long long)c->window * c->head_dim * 2 > 128 * 1024)
+            return VST_E_UNSUPPORTED;
+        return VST_OK;
+    }
+    if (c->kind == VST_DEC) {
+        if (c->ring_slots < c->window)
+            return VST_E_INVAL;
+        // kernel (c): head dim 128, 4 query heads per KV head, ring a multiple of the split.
+        if (c->head_dim != 128 || c->n_heads != 4 * c->n_kv_heads || c->ring_slots % kDecSplit != 0)
+            return VST_E_UNSUPPORTED;
+        return VST_OK;
+    }
+    return VST_E_INVAL;
+}
+
+// Switch to the module's device for the duration of a call, then restore.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess)
+            ok = false;
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev)
+            cudaSetDevice(prev);
+    }
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Tensor map over a ring [Hk][R][D] bf16: box of 64 dims x 128 rows x 1 head, 128-B
+// swizzle, zero fill outside the ring.
+bool make_ring_map(CUtensorMap* map, void* base, const vst_config& c)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.ring_slots, (cuuint64_t)c.n_kv_heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)c.head_dim * 2, (cuuint64_t)c.ring_slots * c.head_dim * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Zero the error word, counters and both rings (not the tensor maps).
+cudaError_t clear_ctx(vst_ctx* c, cudaStream_t s)
+{
+    cudaError_t e = cudaMemsetAsync(c->mem, 0, 256, s);
+    if (e != cudaSuccess)
+        return e;
+    const Layout L = layout_of(c->m->cfg);
+    return cudaMemsetAsync(c->mem + L.k_off, 0, L.ml_off ? (L.ml_off - L.k_off) : (L.total - L.k_off), s);
+}
+
+vst_status fail_all(vst_ctx* const* ctxs, int n)
+{
+    for (int i = 0; i < n; ++i)
+        ctxs[i]->failed = 1;
+    return VST_E_CUDA;
+}
+
+// Common checks for a call over n contexts of one kind.
+vst_status check_ctxs(vst_ctx* const* ctxs, int n, int kind)
+{
+    if (!ctxs || n <= 0)
+        return VST_E_INVAL;
+    const vst_module* m = nullptr;
+    for (int i = 0; i < n; ++i) {
+        if (!ctxs[i])
+            return VST_E_INVAL;
+        if (i == 0)
+            m = ctxs[0]->m;
+        if (ctxs[i]->m != m)
+            return VST_E_INVAL;
+        if (ctxs[i]->m->cfg.kind != kind || ctxs[i]->failed)
+            return VST_E_STATE;
+    }
+    // distinct contexts (small n in practice; quadratic check is cheap next to a launch)
+    for (int i = 0; i < n; ++i)
+        for (int j = i + 1; j < n; ++j)
+            if (ctxs[i] == ctxs[j])
+                return VST_E_INVAL;
+    return VST_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vst_version(void) { return "0.1.0"; }
+
+const char* vst_status_str(vst_status s)
+{
+    switch (s) {
+    case VST_OK: return "ok";
+    case VST_E_INVAL: return "invalid argument";
+    case VST_E_UNSUPPORTED: return "unsupported configuration";
+    case VST_E_CUDA: return "CUDA error";
+    case VST_E_STATE: return "context failed or of the wrong kind";
+    case VST_E_TIMEOUT: return "kernel wait timed out";
+    case VST_E_NOMEM: return "out of memory";
+    }
+    return "unknown status";
+}
+
+vst_status vst_config_default(int32_t kind, vst_config* cfg)
+{
+    if (!cfg)
+        return VST_E_INVAL;
+    std::memset(cfg, 0, sizeof *cfg);
+    cfg->kind = kind;
+    cfg->rope_theta = 1.0e6;
+    cfg->max_position = 131072;
+    if (kind == VST_ENC) {
+        cfg->n_heads = 20;
+        cfg->n_kv_heads = 20;
+        cfg->head_dim = 64;
+        cfg->window = 750;
+        cfg->ring_slots = 1536;
+        cfg->max_batch = 512;
+        return VST_OK;
+    }
+    if (kind == VST_DEC) {
+        cfg->n_heads = 32;
+        cfg->n_kv_heads = 8;
+        cfg->head_dim = 128;
+        cfg->window = 8192;
+        cfg->ring_slots = 8192;
+        cfg->max_batch = 1;
+        return VST_OK;
+    }
+    return VST_E_INVAL;
+}
+
+vst_status vst_module_create(const vst_config* cfg, vst_module** out)
+{
+    if (!out)
+        return VST_E_INVAL;
+    *out = nullptr;
+    vst_status st = check_config(cfg);
+    if (st != VST_OK)
+        return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return VST_E_CUDA;
+    const int half = cfg->head_dim / 2;
+    const size_t n = (size_t)cfg->max_position * half;
+    // RoPE table: (cos, sin) of p * theta^(-2i/D), computed in double, stored as fp32.
+    std::vector<double> freq(half);
+    for (int i = 0; i < half; ++i)
+        freq[i] = std::pow(cfg->rope_theta, -2.0 * i / cfg->head_dim);
+    std::vector<float2> table;
+    try {
+        table.resize(n);
+    } catch (const std::bad_alloc&) {
+        return VST_E_NOMEM;
+    }
+    for (int64_t p = 0; p < cfg->max_position; ++p)
+        for (int i = 0; i < half; ++i) {
+            const double a = (double)p * freq[i];
+            table[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+        }
+    vst_module* m = new (std::nothrow) vst_module();
+    if (!m)
+        return VST_E_NOMEM;
+    m->cfg = *cfg;
+    m->device = dev;
+    m->splits = cfg->kind == VST_DEC ? dec_splits(*cfg) : 0;
+    if (cudaMalloc(&m->rope, n * sizeof(float2)) != cudaSuccess) {
+        delete m;
+        return VST_E_NOMEM;
+    }
+    if (cudaMemcpy(m->rope, table.data(), n * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaFree(m->rope);
+        delete m;
+        return VST_E_CUDA;
+    }
+    *out = m;
+    return VST_OK;
+}
+
+vst_status vst_module_destroy(vst_module* m)
+{
+    if (!m)
+        return VST_E_INVAL;
+    DeviceGuard g(m->device);
+    cudaFree(m->rope);
+    delete m;
+    return VST_OK;
+}
+
+vst_status vst_module_config(const vst_module* m, vst_config* cfg)
+{
+    if (!m || !cfg)
+        return VST_E_INVAL;
+    *cfg = m->cfg;
+    return VST_OK;
+}
+
+size_t vst_ctx_bytes(const vst_module* m)
+{
+    return m ? layout_of(m->cfg).total : 0;
+}
+
+vst_status vst_ctx_create(const vst_module* m, void* dev_mem, size_t bytes, void* stream, vst_ctx** out)
+{
+    if (!m || !out)
+        return VST_E_INVAL;
+    *out = nullptr;
+    const Layout L = layout_of(m->cfg);
+    if (dev_mem && (bytes < L.total || ((uintptr_t)dev_mem & 255u)))
+        return dev_mem && bytes < L.total ? VST_E_NOMEM : VST_E_INVAL;
+    DeviceGuard g(m->device);
+    if (!g.ok)
+        return VST_E_CUDA;
+    vst_ctx* c = new (std::nothrow) vst_ctx();
+    if (!c)
+        return VST_E_NOMEM;
+    c->m = m;
+    c->owns = dev_mem == nullptr;
+    c->bytes = L.total;
+    if (c->owns) {
+        if (cudaMalloc(&dev_mem, L.total) != cudaSuccess) {
+            delete c;
+            return VST_E_NOMEM;
+        }
+    }
+    c->mem = static_cast<uint8_t*>(dev_mem);
+    c->err = reinterpret_cast<int*>(c->mem + kErrOffset);
+    c->counters = reinterpret_cast<unsigned*>(c->mem + kCounterOffset);
+    c->tmap_k = reinterpret_cast<const CUtensorMap*>(c->mem + kTmapOffset);
+    c->tmap_v = reinterpret_cast<const CUtensorMap*>(c->mem + kTmapOffset + sizeof(CUtensorMap));
+    c->k_ring = reinterpret_cast<__nv_bfloat16*>(c->mem + L.k_off);
+    c->v_ring = reinterpret_cast<__nv_bfloat16*>(c->mem + L.v_off);
+    c->part_ml = L.ml_off ? reinterpret_cast<float*>(c->mem + L.ml_off) : nullptr;
+    c->part_o = L.o_off ? reinterpret_cast<float*>(c->mem + L.o_off) : nullptr;
+    bool ok = make_ring_map(&c->host_maps[0], c->k_ring, m->cfg) && make_ring_map(&c->host_maps[1], c->v_ring, m->cfg);
+    cudaStream_t s = as_stream(stream);
+    if (ok)
+        ok = cudaMemcpyAsync(c->mem + kTmapOffset, c->host_maps, sizeof c->host_maps, cudaMemcpyHostToDevice, s) ==
+                 cudaSuccess &&
+             clear_ctx(c, s) == cudaSuccess;
+    if (!ok) {
+        if (c->owns)
+            cudaFree(c->mem);
+        delete c;
+        return VST_E_CUDA;
+    }
+    *out = c;
+    return VST_OK;
+}
+
+vst_status vst_ctx_reset(vst_ctx* c, void* stream)
+{
+    if (!c)
+        return VST_E_INVAL;
+    DeviceGuard g(c->m->device);
+    c->n_kv = c->abs_base = c->abs_next = c->n_compactions = 0;
+    c->failed = 0;
+    if (clear_ctx(c, as_stream(stream)) != cudaSuccess) {
+        c->failed = 1;
+        return VST_E_CUDA;
+    }
+    return VST_OK;
+}
+
+vst_status vst_ctx_destroy(vst_ctx* c)
+{
+    if (!c)
+        return VST_E_INVAL;
+    if (c->owns) {
+        DeviceGuard g(c->m->device);
+        cudaFree(c->mem);
+    }
+    delete c;
+    return VST_OK;
+}
+
+vst_status vst_ctx_info_get(const vst_ctx* c, vst_ctx_info* out)
+{
+    if (!c || !out)
+        return VST_E_INVAL;
+    out->kind = c->m->cfg.kind;
+    out->failed = c->failed;
+    out->n_kv = c->n_kv;
+    out->abs_base = c->abs_base;
+    out->abs_next = c->abs_next;
+    out->n_compactions = c->n_compactions;
+    out->k_ring = c->k_ring;
+    out->v_ring = c->v_ring;
+    return VST_OK;
+}
+
+vst_status vst_ctx_check(vst_ctx* c, void* stream)
+{
+    if (!c)
+        return VST_E_INVAL;
+    DeviceGuard g(c->m->device);
+    int host_err = 0;
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemcpyAsync(&host_err, c->err, sizeof host_err, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return VST_E_CUDA;
+    if (host_err != 0) {
+        cudaMemsetAsync(c->err, 0, sizeof(int), s);
+        return VST_E_TIMEOUT;
+    }
+    return VST_OK;
+}
+
+vst_status vst_enc_plan(const vst_config* cfg, int64_t n_kv, int64_t abs_base, int32_t n_new, int32_t* batch,
+                        int32_t* compact, int32_t max_steps, int32_t* n_steps, int64_t* n_kv_out,
+                        int64_t* abs_base_out)
+{
+    if (!cfg || cfg->kind != VST_ENC || n_new < 0 || n_kv < 0 || n_kv > cfg->ring_slots || !n_steps)
+        return VST_E_INVAL;
+    const vst_status st = check_config(cfg);
+    if (st != VST_OK)
+        return st;
+    int32_t k = 0;
+    for (int32_t off = 0; off < n_new;) {
+        const int32_t b = n_new - off < cfg->max_batch ? n_new - off : cfg->max_batch;
+        int32_t comp = 0;
+        if (n_kv + b > cfg->ring_slots) {
+            const int64_t keep = n_kv < cfg->window ? n_kv : cfg->window;
+            abs_base += n_kv - keep;
+            n_kv = keep;
+            comp = 1;
+        }
+        if (k < max_steps) {
+            if (batch)
+                batch[k] = b;
+            if (compact)
+                compact[k] = comp;
+        }
+        ++k;
+        n_kv += b;
+        off += b;
+    }
+    *n_steps = k;
+    if (n_kv_out)
+        *n_kv_out = n_kv;
+    if (abs_base_out)
+        *abs_base_out = abs_base;
+    return VST_OK;
+}
+
+vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q, const void* k, const void* v,
+                              int32_t n_new, void* out, void* stream)
+{
+    vst_status st = check_ctxs(ctxs, n_ctx, VST_ENC);
+    if (st != VST_OK)
+        return st;
+    if (n_new < 0)
+        return VST_E_INVAL;
+    if (n_new == 0)
+        return VST_OK;
+    if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return VST_E_INVAL;
+    const vst_module* m = ctxs[0]->m;
+    const vst_config& cfg = m->cfg;
+    for (int i = 0; i < n_ctx; ++i)
+        if (ctxs[i]->abs_next + n_new > cfg.max_position)
+            return VST_E_INVAL;
+    DeviceGuard g(m->device);
+    if (!g.ok)
+        return fail_all(ctxs, n_ctx);
+    cudaStream_t s = as_stream(stream);
+    const int H = cfg.n_heads, Hk = cfg.n_kv_heads, D = cfg.head_dim;
+    const auto* qb = static_cast<const __nv_bfloat16*>(q);
+    const auto* kb = static_cast<const __nv_bfloat16*>(k);
+    const auto* vb = static_cast<const __nv_bfloat16*>(v);
+    auto* ob = static_cast<__nv_bfloat16*>(out);
+
+    const CompactCommon cc{Hk, cfg.ring_slots, D, cfg.window};
+    const AppendCommon ac{m->rope, 0, Hk, D, cfg.ring_slots, 0};
+    const EncAttnCommon ec{m->rope, 0, H, cfg.window, (float)(1.4426950408889634 / std::sqrt((double)D))};
+    CompactJob cj[kMaxJobs];
+    AppendJob aj[kMaxJobs];
+    EncAttnJob ej[kMaxJobs];
+
+    for (int32_t off = 0; off < n_new;) {
+        const int32_t b = n_new - off < cfg.max_batch ? n_new - off : cfg.max_batch;
+        for (int c0 = 0; c0 < n_ctx; c0 += kMaxJobs) {
+            const int nj = n_ctx - c0 < kMaxJobs ? n_ctx - c0 : kMaxJobs;
+            int ncj = 0;
+            for (int i = 0; i < nj; ++i) {
+                vst_ctx* c = ctxs[c0 + i];
+                if (c->n_kv + b > cfg.ring_slots) {
+                    const int64_t keep = c->n_kv < cfg.window ? c->n_kv : cfg.window;
+                    cj[ncj++] = CompactJob{c->k_ring, c->v_ring, c->n_kv - keep};
+                    c->abs_base += c->n_kv - keep;
+                    c->n_kv = keep;
+                    c->n_compactions += 1;
+                }
+            }
+            if (launch_compact(cc, cj, ncj, s) != cudaSuccess)
+                return fail_all(ctxs, n_ctx);
+            for (int i = 0; i < nj; ++i) {
+                vst_ctx* c = ctxs[c0 + i];
+                const long long row = (long long)(c0 + i) * n_new + off;
+                aj[i] = AppendJob{kb + row * Hk * D, vb + row * Hk * D, c->k_ring, c->v_ring, c->abs_next, c->n_kv};
+                ej[i] = EncAttnJob{qb + row * H * D, ob + row * H * D, c->tmap_k, c->tmap_v, c->err, c->abs_next,
+                                   c->abs_base};
+            }
+            AppendCommon a2 = ac;
+            a2.n_rows = b;
+            if (launch_rope_append(a2, aj, nj, s) != cudaSuccess)
+                return fail_all(ctxs, n_ctx);
+            EncAttnCommon e2 = ec;
+            e2.n_rows = b;
+            if (launch_enc_attn(e2, ej, nj, s) != cudaSuccess)
+                return fail_all(ctxs, n_ctx);
+            for (int i = 0; i < nj; ++i) {
+                ctxs[c0 + i]->n_kv += b;
+                ctxs[c0 + i]->abs_next += b;
+            }
+        }
+        off += b;
+    }
+    return VST_OK;
+}
+
+vst_status vst_enc_feed(vst_ctx* c, const void* q, const void* k, const void* v, int32_t n_new, void* out,
+                        void* stream)
+{
+    return vst_enc_feed_batch(&c, 1, q, k, v, n_new, out, stream);
+}
+
+vst_status vst_ctx_compact(vst_ctx* c, void* stream)
+{
+    vst_ctx* cs[1] = {c};
+    vst_status st = check_ctxs(cs, 1, VST_ENC);
+    if (st != VST_OK)
+        return st;
+    const vst_config& cfg = c->m->cfg;
+    if (c->n_kv <= cfg.window)
+        return VST_OK;
+    DeviceGuard g(c->m->device);
+    const CompactCommon cc{cfg.n_kv_heads, cfg.ring_slots, cfg.head_dim, cfg.window};
+    const CompactJob cj{c->k_ring, c->v_ring, c->n_kv - cfg.window};
+    if (launch_compact(cc, &cj, 1, as_stream(stream)) != cudaSuccess)
+        return fail_all(cs, 1);
+    c->abs_base += c->n_kv - cfg.window;
+    c->n_kv = cfg.window;
+    c->n_compactions += 1;
+    return VST_OK;
+}
+
+vst_status vst_dec_step(vst_ctx* const* ctxs, int32_t n_streams, const void* q, const void* k, const void* v,
+                        void* out, void* stream)
+{
+    vst_status st = check_ctxs(ctxs, n_streams, VST_DEC);
+    if (st != VST_OK)
+        return st;
+    if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return VST_E_INVAL;
+    const vst_module* m = ctxs[0]->m;
+    const vst_config& cfg = m->cfg;
+    for (int i = 0; i < n_streams; ++i)
+        if (ctxs[i]->abs_next >= cfg.max_position)
+            return VST_E_INVAL;
+    DeviceGuard g(m->device);
+    if (!g.ok)
+        return fail_all(ctxs, n_streams);
+    cudaStream_t s = as_stream(stream);
+    const int H = cfg.n_heads, Hk = cfg.n_kv_heads, D = cfg.head_dim;
+    const auto* qb = static_cast<const __nv_bfloat16*>(q);
+    const auto* kb = static_cast<const __nv_bfloat16*>(k);
+    const auto* vb = static_cast<const __nv_bfloat16*>(v);
+    auto* ob = static_cast<__nv_bfloat16*>(out);
+    const DecCommon dc0{m->rope, 0, Hk, cfg.ring_slots, cfg.window, m->splits,
+                        (float)(1.4426950408889634 / std::sqrt((double)D))};
+    DecJob jobs[kMaxJobs];
+    for (int c0 = 0; c0 < n_streams; c0 += kMaxJobs) {
+        const int nj = n_streams - c0 < kMaxJobs ? n_streams - c0 : kMaxJobs;
+        int work = 0;
+        for (int i = 0; i < nj; ++i) {
+            vst_ctx* c = ctxs[c0 + i];
+            const long long si = c0 + i;
+            const long long pos = c->abs_next;
+            const long long lo = pos - cfg.window + 1 > 0 ? pos - cfg.window + 1 : 0;
+            const int sig0 = (int)(lo / kDecSplit);
+            const int nsp = (int)(pos / kDecSplit) - sig0 + 1;
+            jobs[i] = DecJob{qb + si * H * D, kb + si * Hk * D, vb + si * Hk * D, ob + si * H * D,
+                             c->k_ring, c->v_ring, c->tmap_k, c->tmap_v, c->part_ml, c->part_o,
+                             c->counters, c->err, pos, sig0, nsp, work, 0};
+            work += nsp;
+        }
+        DecCommon dc = dc0;
+        dc.n_jobs = nj;
+        if (launch_dec_step(dc, jobs, nj, work, s) != cudaSuccess)
+            return fail_all(ctxs, n_streams);
+        for (int i = 0; i < nj; ++i)
+            ctxs[c0 + i]->abs_next += 1;
+    }
+    return VST_OK;
+}
+
+vst_status vst_dec_append(vst_ctx* c, const void* k, const void* v, int32_t n, void* stream)
+{
+    vst_ctx* cs[1] = {c};
+    vst_status st = check_ctxs(cs, 1, VST_DEC);
+    if (st != VST_OK)
+        return st;
+    if (n < 0)
+        return VST_E_INVAL;
+    if (n == 0)
+        return VST_OK;
+    if (!k || !v || !aligned16(k) || !aligned16(v))
+        return VST_E_INVAL;
+    const vst_config& cfg = c->m->cfg;
+    if (c->abs_next + n > cfg.max_position)
+        return VST_E_INVAL;
+    DeviceGuard g(c->m->device);
+    const auto* kb = static_cast<const __nv_bfloat16*>(k);
+    const auto* vb = static_cast<const __nv_bfloat16*>(v);
+    const int Hk = cfg.n_kv_heads, D = cfg.head_dim;
+    // At most R rows per launch so that no two rows of one launch share a slot.
+    for (int32_t off = 0; off < n; off += cfg.ring_slots) {
+        const int32_t rows = n - off < cfg.ring_slots ? n - off : cfg.ring_slots;
+        const AppendCommon ac{c->m->rope, rows, Hk, D, cfg.ring_slots, 1};
+        const AppendJob aj{kb + (long long)off * Hk * D, vb + (long long)off * Hk * D, c->k_ring, c->v_ring,
+                           c->abs_next, 0};
+        if (launch_rope_append(ac, &aj, 1, as_stream(stream)) != cudaSuccess)
+            return fail_all(cs, 1);
+        c->abs_next += rows;
+    }
+    return VST_OK;
+}
+
+}  // extern "C"

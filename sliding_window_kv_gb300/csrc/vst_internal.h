@@ -1,0 +1,146 @@
+// vst_internal.h -- structures shared by the host API (vst_api.cu) and the kernels.
+//
+// Device memory of one ctx is one block:
+//   [0, 256)          header: error word (int32 at 0), merge counters (uint32 at 64, one per
+//                     KV head, decoder only)
+//   [256, 512)        two CUtensorMap (128 B each, 64-B aligned): K ring, V ring
+//   [512, ...)        K ring [Hk][R][D] bf16, then V ring [Hk][R][D] bf16
+//   decoder only      partial softmax state per (query head, split): m, l [H][S][2] fp32 and
+//                     o [H][S][D] fp32, S = splits per step
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/vst.h"
+
+namespace vst {
+
+constexpr int kCtxHeaderBytes = 512;
+constexpr int kErrOffset = 0;
+constexpr int kCounterOffset = 64;
+constexpr int kTmapOffset = 256;
+
+// Decoder split: keys are reduced in blocks of kDecSplit absolute positions.
+constexpr int kDecSplit = 128;
+// Encoder attention tiles: 128 queries x 128 keys (absolute-position aligned).
+constexpr int kEncTileM = 128;
+constexpr int kEncTileN = 128;
+
+constexpr int kMaxJobs = 64;  // contexts per launch
+
+// Error codes written into the ctx error word by kernels.
+constexpr int kErrTimeout = 1;
+
+struct AppendJob {
+    const __nv_bfloat16* k;  // [n_rows][Hk][D] input
+    const __nv_bfloat16* v;
+    __nv_bfloat16* k_ring;   // [Hk][R][D]
+    __nv_bfloat16* v_ring;
+    long long pos0;          // absolute position of input row 0
+    long long slot0;         // ring slot of row 0 (contiguous mode)
+};
+
+struct AppendCommon {
+    const float2* rope;      // [max_position][D/2] (cos, sin)
+    int n_rows, Hk, D, R;
+    int modulo;              // 1: slot = position % R (decoder); 0: slot0 + row (encoder)
+};
+
+struct CompactJob {
+    __nv_bfloat16* k_ring;
+    __nv_bfloat16* v_ring;
+    long long src_row;       // rows [src_row, src_row + keep) move to [0, keep)
+};
+
+struct CompactCommon {
+    int Hk, R, D, keep;
+};
+
+struct EncAttnJob {
+    const __nv_bfloat16* q;  // [n_rows][H][D] input rows of this batch
+    __nv_bfloat16* out;      // [n_rows][H][D]
+    const CUtensorMap* tmap_k;  // over the K ring, dims {D, R, Hk}, box {64, 128, 1}, SW128
+    const CUtensorMap* tmap_v;
+    int* err;
+    long long pos0;          // absolute position of row 0
+    long long abs_base;      // absolute position held by ring slot 0
+};
+
+struct EncAttnCommon {
+    const float2* rope;
+    int n_rows, H, W;
+    float scale_log2;        // log2(e) / sqrt(D)
+};
+
+struct DecJob {
+    const __nv_bfloat16* q;  // [H][D] this stream's query
+    const __nv_bfloat16* k;  // [Hk][D] this step's key (not rotated yet)
+    const __nv_bfloat16* v;  // [Hk][D]
+    __nv_bfloat16* out;      // [H][D]
+    __nv_bfloat16* k_ring;
+    __nv_bfloat16* v_ring;
+    const CUtensorMap* tmap_k;  // dims {D, R, Hk}, box {64, 128, 1}, SW128
+    const CUtensorMap* tmap_v;
+    float* part_ml;          // [H][S][2]
+    float* part_o;           // [H][S][D]
+    unsigned* counters;      // [Hk]
+    int* err;
+    long long pos;           // absolute position of this step's token
+    int sigma0;              // first split (absolute block index) of this step
+    int n_splits;
+    int work_begin;          // first work item (blockIdx.x) of this job
+    int pad;
+};
+
+struct DecCommon {
+    const float2* rope;
+    int n_jobs, Hk, R, W, S;
+    float scale_log2;
+};
+
+// Kernel parameters: the common block plus up to J jobs, passed by value. Launchers pick
+// the smallest J that holds the jobs so one-context launches stay small.
+template <class Common, class Job, int J>
+struct KParams {
+    Common c;
+    Job jobs[J];
+};
+
+// Kernel launchers (one per kernel file). They only enqueue; errors are returned as
+// cudaError_t from cudaGetLastError.
+// n_jobs <= kMaxJobs.
+cudaError_t launch_rope_append(const AppendCommon& c, const AppendJob* jobs, int n_jobs,
+                               cudaStream_t s);
+cudaError_t launch_compact(const CompactCommon& c, const CompactJob* jobs, int n_jobs,
+                           cudaStream_t s);
+cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int n_jobs,
+                            cudaStream_t s);
+cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, int total_work,
+                            cudaStream_t s);
+
+// Copy jobs into a KParams<J> with the smallest J in {1, 8, 64} that fits and call
+// f(params) with it.
+template <class Common, class Job, class F>
+cudaError_t with_params(const Common& c, const Job* jobs, int n_jobs, F&& f)
+{
+    if (n_jobs <= 1) {
+        KParams<Common, Job, 1> p;
+        p.c = c;
+        p.jobs[0] = jobs[0];
+        return f(p);
+    }
+    if (n_jobs <= 8) {
+        KParams<Common, Job, 8> p;
+        p.c = c;
+        for (int i = 0; i < n_jobs; ++i) p.jobs[i] = jobs[i];
+        return f(p);
+    }
+    KParams<Common, Job, kMaxJobs> p;
+    p.c = c;
+    for (int i = 0; i < n_jobs; ++i) p.jobs[i] = jobs[i];
+    return f(p);
+}
+
+}  // namespace vst

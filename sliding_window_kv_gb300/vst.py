@@ -1,0 +1,250 @@
+"""Thin ctypes binding of libvst (include/vst.h), same names without the ``vst_`` prefix.
+
+Argument marshalling only: every step of the attention path runs in the CUDA kernels of
+libvst.so. Tensors are torch bf16 CUDA tensors (contiguous); their data pointers and the
+current CUDA stream are passed through. There is no fallback: if libvst.so is missing or
+fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libvst.so")
+
+OK, E_INVAL, E_UNSUPPORTED, E_CUDA, E_STATE, E_TIMEOUT, E_NOMEM = 0, -1, -2, -3, -4, -5, -6
+ENC, DEC = 1, 2
+
+
+class VstError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s: %s (%d)" % (what, status_str(status), status))
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("n_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("window", ctypes.c_int32), ("ring_slots", ctypes.c_int32),
+                ("max_batch", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("max_position", ctypes.c_int64), ("rope_theta", ctypes.c_double)]
+
+
+class CtxInfo(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("failed", ctypes.c_int32), ("n_kv", ctypes.c_int64),
+                ("abs_base", ctypes.c_int64), ("abs_next", ctypes.c_int64),
+                ("n_compactions", ctypes.c_int64), ("k_ring", ctypes.c_void_p), ("v_ring", ctypes.c_void_p)]
+
+
+EXPORTS = ["vst_config_default", "vst_module_create", "vst_module_destroy", "vst_module_config",
+           "vst_ctx_bytes", "vst_ctx_create", "vst_ctx_reset", "vst_ctx_destroy", "vst_ctx_info_get",
+           "vst_ctx_check", "vst_enc_feed", "vst_enc_feed_batch", "vst_ctx_compact", "vst_enc_plan",
+           "vst_dec_step", "vst_dec_append", "vst_status_str", "vst_version"]
+
+_lib = None
+
+
+def lib():
+    """Load libvst.so (raises if it is missing: there is no other implementation)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libvst.so is not built (run __graft_entry__.build()): %s" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        PP = ctypes.POINTER(ctypes.c_void_p)
+        sig = {
+            "vst_config_default": ([I32, ctypes.POINTER(Config)], I32),
+            "vst_module_create": ([ctypes.POINTER(Config), PP], I32),
+            "vst_module_destroy": ([P], I32),
+            "vst_module_config": ([P, ctypes.POINTER(Config)], I32),
+            "vst_ctx_bytes": ([P], SZ),
+            "vst_ctx_create": ([P, P, SZ, P, PP], I32),
+            "vst_ctx_reset": ([P, P], I32),
+            "vst_ctx_destroy": ([P], I32),
+            "vst_ctx_info_get": ([P, ctypes.POINTER(CtxInfo)], I32),
+            "vst_ctx_check": ([P, P], I32),
+            "vst_enc_feed": ([P, P, P, P, I32, P, P], I32),
+            "vst_enc_feed_batch": ([PP, I32, P, P, P, I32, P, P], I32),
+            "vst_ctx_compact": ([P, P], I32),
+            "vst_enc_plan": ([ctypes.POINTER(Config), I64, I64, I32, ctypes.POINTER(I32), ctypes.POINTER(I32), I32,
+                              ctypes.POINTER(I32), ctypes.POINTER(I64), ctypes.POINTER(I64)], I32),
+            "vst_dec_step": ([PP, I32, P, P, P, P, P], I32),
+            "vst_dec_append": ([P, P, P, I32, P], I32),
+            "vst_status_str": ([I32], ctypes.c_char_p),
+            "vst_version": ([], ctypes.c_char_p),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def status_str(s: int) -> str:
+    return lib().vst_status_str(s).decode()
+
+
+def version() -> str:
+    return lib().vst_version().decode()
+
+
+def _check(s: int, what: str):
+    if s != OK:
+        raise VstError(s, what)
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+        # raw device pointer
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous bf16 CUDA tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def config_default(kind: int) -> Config:
+    c = Config()
+    _check(lib().vst_config_default(kind, ctypes.byref(c)), "vst_config_default")
+    return c
+
+
+def module_create(cfg: Config) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().vst_module_create(ctypes.byref(cfg), ctypes.byref(h)), "vst_module_create")
+    return h.value
+
+
+def module_destroy(m: int):
+    _check(lib().vst_module_destroy(m), "vst_module_destroy")
+
+
+def module_config(m: int) -> Config:
+    c = Config()
+    _check(lib().vst_module_config(m, ctypes.byref(c)), "vst_module_config")
+    return c
+
+
+def ctx_bytes(m: int) -> int:
+    return lib().vst_ctx_bytes(m)
+
+
+def ctx_create(m: int, dev_mem: int = 0, nbytes: int = 0, stream=None) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().vst_ctx_create(m, dev_mem or None, nbytes, _stream(stream), ctypes.byref(h)), "vst_ctx_create")
+    return h.value
+
+
+def ctx_reset(c: int, stream=None):
+    _check(lib().vst_ctx_reset(c, _stream(stream)), "vst_ctx_reset")
+
+
+def ctx_destroy(c: int):
+    _check(lib().vst_ctx_destroy(c), "vst_ctx_destroy")
+
+
+def ctx_info_get(c: int) -> CtxInfo:
+    i = CtxInfo()
+    _check(lib().vst_ctx_info_get(c, ctypes.byref(i)), "vst_ctx_info_get")
+    return i
+
+
+def ctx_check(c: int, stream=None) -> int:
+    return lib().vst_ctx_check(c, _stream(stream))
+
+
+def enc_feed(c: int, q, k, v, out, stream=None, n_new: int | None = None):
+    n = q.shape[0] if n_new is None else n_new
+    _check(lib().vst_enc_feed(c, _ptr(q), _ptr(k), _ptr(v), n, _ptr(out), _stream(stream)), "vst_enc_feed")
+
+
+def _handles(ctxs):
+    arr = (ctypes.c_void_p * len(ctxs))(*ctxs)
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), arr
+
+
+def enc_feed_batch(ctxs, q, k, v, out, n_new: int, stream=None):
+    h, keep = _handles(ctxs)
+    _check(lib().vst_enc_feed_batch(h, len(ctxs), _ptr(q), _ptr(k), _ptr(v), n_new, _ptr(out), _stream(stream)),
+           "vst_enc_feed_batch")
+
+
+def ctx_compact(c: int, stream=None):
+    _check(lib().vst_ctx_compact(c, _stream(stream)), "vst_ctx_compact")
+
+
+def enc_plan(cfg: Config, n_kv: int, abs_base: int, n_new: int, max_steps: int = 4096):
+    batch = (ctypes.c_int32 * max_steps)()
+    comp = (ctypes.c_int32 * max_steps)()
+    n = ctypes.c_int32()
+    nk = ctypes.c_int64()
+    ab = ctypes.c_int64()
+    _check(lib().vst_enc_plan(ctypes.byref(cfg), n_kv, abs_base, n_new, batch, comp, max_steps, ctypes.byref(n),
+                              ctypes.byref(nk), ctypes.byref(ab)), "vst_enc_plan")
+    k = min(n.value, max_steps)
+    return [(batch[i], comp[i]) for i in range(k)], nk.value, ab.value
+
+
+def dec_step(ctxs, q, k, v, out, stream=None):
+    h, keep = _handles(ctxs)
+    _check(lib().vst_dec_step(h, len(ctxs), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream)),
+           "vst_dec_step")
+
+
+def dec_append(c: int, k, v, n: int | None = None, stream=None):
+    n = k.shape[0] if n is None else n
+    _check(lib().vst_dec_append(c, _ptr(k), _ptr(v), n, _stream(stream)), "vst_dec_append")
+
+
+class Module:
+    """Owning wrapper: vst_module_create / vst_module_destroy."""
+
+    def __init__(self, cfg_or_kind):
+        self.cfg = config_default(cfg_or_kind) if isinstance(cfg_or_kind, int) else cfg_or_kind
+        self.handle = module_create(self.cfg)
+
+    def close(self):
+        if self.handle:
+            module_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Ctx:
+    """Owning wrapper: vst_ctx_create (library-allocated memory) / vst_ctx_destroy."""
+
+    def __init__(self, module: Module, stream=None):
+        self.module = module
+        self.handle = ctx_create(module.handle, 0, 0, stream)
+
+    def info(self) -> CtxInfo:
+        return ctx_info_get(self.handle)
+
+    def close(self):
+        if self.handle:
+            ctx_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

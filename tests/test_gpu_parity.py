@@ -1,0 +1,342 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by element,
+plus the bit-exact self-consistency the method promises (chunking and compaction schedules
+are not observable; batched decode equals single-stream decode; ring size is not
+observable). Tolerances: max|d| <= 2e-2 and mean|d| <= 2e-3 against the oracle on bf16
+inputs with fp32 accumulation; bit-exact for ring bytes and for self-consistency.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sliding_window_kv_gb300 import synth, vst
+
+pytestmark = pytest.mark.gpu
+
+MAX_TOL = 2e-2
+MEAN_TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.init()
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def enc_module(dev):
+    m = vst.Module(vst.ENC)
+    yield m
+    m.close()
+
+
+@pytest.fixture(scope="module")
+def dec_module(dev):
+    m = vst.Module(vst.DEC)
+    yield m
+    m.close()
+
+
+def _enc_inputs(seed, layer, T, H=20, D=64, device="cpu", first=0):
+    q = synth.frames(synth.tensor_key(seed, layer, 0), first, T, H, D, device)
+    k = synth.frames(synth.tensor_key(seed, layer, 1), first, T, H, D, device)
+    v = synth.frames(synth.tensor_key(seed, layer, 2), first, T, H, D, device)
+    return q, k, v
+
+
+def _compare(gpu_out, want, tag=""):
+    got = gpu_out.float().cpu().double().numpy().reshape(want.shape)
+    d = np.abs(got - want)
+    assert np.isfinite(got).all(), tag
+    assert d.max() <= MAX_TOL, "%s max|d| %.3e" % (tag, d.max())
+    assert d.mean() <= MEAN_TOL, "%s mean|d| %.3e" % (tag, d.mean())
+    return d.max(), d.mean()
+
+
+def _feed(module, q, k, v, chunks, compact_before=(), dev="cuda"):
+    """Stream q/k/v through one fresh ctx in the given chunk sizes; returns out [T][H][D]."""
+    ctx = vst.Ctx(module)
+    T = q.shape[0]
+    out = torch.empty_like(q, device=dev)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    t = 0
+    for ci, n in enumerate(chunks):
+        if ci in compact_before:
+            vst.ctx_compact(ctx.handle)
+        vst.enc_feed(ctx.handle, qd[t:t + n], kd[t:t + n], vd[t:t + n], out[t:t + n], n_new=n)
+        t += n
+    assert t == T
+    torch.cuda.synchronize()
+    assert vst.ctx_check(ctx.handle) == vst.OK
+    info = ctx.info()
+    ctx.close()
+    return out, info
+
+
+# ---------------------------------------------------------------- encoder
+
+def test_enc_small_single_tile(dev, enc_module):
+    q, k, v = _enc_inputs(101, 0, 60)
+    out, _ = _feed(enc_module, q, k, v, [60])
+    want = oracle.attention(synth.bits(q), synth.bits(k), synth.bits(v), window=750)
+    _compare(out, want, "T=60")
+
+
+def test_enc_config0_parity_and_bit_exact(dev, enc_module):
+    """1 layer, 20 heads x 64, 1000 frames fed as 10 chunks of 100 with a compaction forced
+    before chunk 9 (n_kv 800 -> 750): matches the oracle, and matches bit for bit a single
+    1000-frame feed and the same chunking without the forced compaction."""
+    q, k, v = _enc_inputs(1, 0, 1000)
+    want = oracle.attention(synth.bits(q), synth.bits(k), synth.bits(v), window=750, threads=8)
+    out_c, info = _feed(enc_module, q, k, v, [100] * 10, compact_before=(8,))
+    assert (info.n_compactions, info.abs_base, info.n_kv) == (1, 50, 950)
+    _compare(out_c, want, "chunks of 100 + compaction")
+    out_1, info1 = _feed(enc_module, q, k, v, [1000])
+    assert info1.n_compactions == 0
+    out_n, _ = _feed(enc_module, q, k, v, [100] * 10)
+    assert torch.equal(out_c, out_1)
+    assert torch.equal(out_c, out_n)
+
+
+@pytest.mark.parametrize("sched", ["ones_then_big", "ragged", "max_batch_edges"])
+def test_enc_chunking_not_observable(dev, enc_module, sched):
+    T = 1700
+    q, k, v = _enc_inputs(7, 3, T)
+    ref, _ = _feed(enc_module, q, k, v, [T])
+    if sched == "ones_then_big":
+        chunks = [1] * 37 + [T - 37]
+    elif sched == "ragged":
+        rng = np.random.default_rng(3)
+        chunks = []
+        while sum(chunks) < T:
+            chunks.append(int(min(T - sum(chunks), rng.choice([1, 3, 49, 50, 127, 128, 129, 300, 511]))))
+    else:
+        chunks = [511, 512, 513, T - 1536]
+    out, info = _feed(enc_module, q, k, v, chunks)
+    assert info.abs_next == T
+    assert torch.equal(out, ref), sched
+
+
+def test_enc_long_stream_parity_sampled(dev, enc_module):
+    """5000 frames in 50-frame feeds (lazy compactions): sampled rows against the oracle
+    computed from each row's own window."""
+    T = 5000
+    q, k, v = _enc_inputs(2, 5, T)
+    out, info = _feed(enc_module, q, k, v, [50] * 100)
+    st = oracle.RingState()
+    for _ in range(100):
+        st.feed(50)
+    assert (info.n_kv, info.abs_base, info.n_compactions) == (st.n_kv, st.abs_base, st.n_compactions)
+    qb, kb, vb = synth.bits(q), synth.bits(k), synth.bits(v)
+    rows = [0, 1, 749, 750, 1499, 1500, 1536, 2287, 3333, 4999]
+    got = out.float().cpu().double().numpy()
+    for i in rows:
+        j0 = max(0, i - 749)
+        want = oracle.attention_row(qb[i], kb[j0:i + 1], vb[j0:i + 1], i, 750)
+        d = np.abs(got[i] - want)
+        assert d.max() <= MAX_TOL, (i, d.max())
+
+
+class TorchCtx:
+    """A ctx on caller-provided memory (a torch uint8 buffer), so the rings can be viewed."""
+
+    def __init__(self, module, dev):
+        cfg = module.cfg
+        self.mem = torch.zeros(vst.ctx_bytes(module.handle), dtype=torch.uint8, device=dev)
+        self.handle = vst.ctx_create(module.handle, self.mem.data_ptr(), self.mem.numel())
+        info = vst.ctx_info_get(self.handle)
+        n = cfg.n_kv_heads * cfg.ring_slots * cfg.head_dim * 2
+        shape = (cfg.n_kv_heads, cfg.ring_slots, cfg.head_dim)
+        ko = info.k_ring - self.mem.data_ptr()
+        vo = info.v_ring - self.mem.data_ptr()
+        self.k_ring = self.mem[ko:ko + n].view(torch.bfloat16).view(shape)
+        self.v_ring = self.mem[vo:vo + n].view(torch.bfloat16).view(shape)
+
+    def info(self):
+        return vst.ctx_info_get(self.handle)
+
+    def close(self):
+        vst.ctx_destroy(self.handle)
+
+
+def test_enc_ring_after_compaction_bit_exact(dev, enc_module):
+    """After compaction slot s holds what slot n_kv - 750 + s held before (bit for bit), and
+    the appended keys are the oracle's rotated keys rounded to bf16."""
+    T = 1000
+    q, k, v = _enc_inputs(11, 0, T)
+    ctx = TorchCtx(enc_module, dev)
+    out = torch.empty_like(q, device=dev)
+    vst.enc_feed(ctx.handle, q.to(dev), k.to(dev), v.to(dev), out)
+    torch.cuda.synchronize()
+    before_k = ctx.k_ring.clone()
+    before_v = ctx.v_ring.clone()
+    vst.ctx_compact(ctx.handle)
+    torch.cuda.synchronize()
+    info = ctx.info()
+    assert (info.n_kv, info.abs_base, info.n_compactions) == (750, 250, 1)
+    assert torch.equal(ctx.k_ring[:, :750], before_k[:, 250:1000])
+    assert torch.equal(ctx.v_ring[:, :750], before_v[:, 250:1000])
+    # slot s now holds absolute frame 250 + s: rotated K (bf16) and V as fed
+    krot = oracle.rope_rows(synth.bits(k), 0)
+    got = ctx.k_ring[:, :750].float().cpu().double().numpy().transpose(1, 0, 2)
+    want = krot[250:1000]
+    assert np.abs(got - want).max() <= np.abs(want).max() * 2 ** -8 + 1e-6
+    assert torch.equal(ctx.v_ring[:, :750].cpu(), v[250:1000].transpose(0, 1).contiguous())
+    # the ring keeps serving: next frames attend across the compacted rows
+    q2, k2, v2 = _enc_inputs(11, 0, 200, first=1000)
+    out2 = torch.empty_like(q2, device=dev)
+    vst.enc_feed(ctx.handle, q2.to(dev), k2.to(dev), v2.to(dev), out2)
+    torch.cuda.synchronize()
+    qa, ka, va = (torch.cat([a, b]) for a, b in ((q, q2), (k, k2), (v, v2)))
+    want2 = oracle.attention(synth.bits(qa), synth.bits(ka), synth.bits(va), window=750, rows=(1000, 1200),
+                             threads=8)
+    _compare(out2, want2, "after compaction")
+    ctx.close()
+
+
+def test_enc_batch_equals_single(dev, enc_module):
+    """Streams with staggered starts fed together through vst_enc_feed_batch give the same
+    bits as each stream fed alone."""
+    n_ctx, T, step = 4, 900, 300
+    offsets = [0, 96, 192, 700]
+    ins = [_enc_inputs(5, s, T) for s in range(n_ctx)]
+    pres = [_enc_inputs(55, s, offsets[s]) if offsets[s] else None for s in range(n_ctx)]
+
+    def prefeed(ctx, s):
+        if pres[s] is not None:
+            o = torch.empty_like(pres[s][0], device=dev)
+            vst.enc_feed(ctx.handle, *(t.to(dev) for t in pres[s]), o)
+
+    singles = []
+    for s in range(n_ctx):
+        ctx = vst.Ctx(enc_module)
+        prefeed(ctx, s)
+        out = torch.empty_like(ins[s][0], device=dev)
+        for t0 in range(0, T, step):
+            vst.enc_feed(ctx.handle, *(t[t0:t0 + step].to(dev) for t in ins[s]), out[t0:t0 + step])
+        singles.append(out)
+        ctx.close()
+    ctxs = [vst.Ctx(enc_module) for _ in range(n_ctx)]
+    for s in range(n_ctx):
+        prefeed(ctxs[s], s)
+    Q, K, V = (torch.stack([ins[s][i] for s in range(n_ctx)]).to(dev) for i in range(3))
+    OUT = torch.empty_like(Q)
+    for t0 in range(0, T, step):
+        o = torch.empty_like(Q[:, t0:t0 + step].contiguous())
+        vst.enc_feed_batch([c.handle for c in ctxs], Q[:, t0:t0 + step].contiguous(),
+                           K[:, t0:t0 + step].contiguous(), V[:, t0:t0 + step].contiguous(), o, step)
+        OUT[:, t0:t0 + step] = o
+    torch.cuda.synchronize()
+    for s in range(n_ctx):
+        assert torch.equal(OUT[s], singles[s]), s
+        assert ctxs[s].info().abs_next == offsets[s] + T
+    for c in ctxs:
+        c.close()
+
+
+# ---------------------------------------------------------------- decoder
+
+def _dec_seq(seed, stream, layer, n_tok, device="cpu", first=0):
+    q = synth.frames(synth.tensor_key(seed, stream, layer, 0), first, n_tok, 32, 128, device)
+    k = synth.frames(synth.tensor_key(seed, stream, layer, 1), first, n_tok, 8, 128, device)
+    v = synth.frames(synth.tensor_key(seed, stream, layer, 2), first, n_tok, 8, 128, device)
+    return q, k, v
+
+
+def _run_dec(module, q, k, v, fill, steps, dev="cuda", ring_cfg=None):
+    """Append `fill` tokens, then run `steps` decoder steps; returns out [steps][32][128]."""
+    m = module
+    ctx = vst.Ctx(m)
+    if fill:
+        vst.dec_append(ctx.handle, k[:fill].to(dev), v[:fill].to(dev))
+    outs = torch.empty((steps, 32, 128), dtype=torch.bfloat16, device=dev)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    for s in range(steps):
+        t = fill + s
+        vst.dec_step([ctx.handle], qd[t:t + 1], kd[t:t + 1], vd[t:t + 1], outs[s:s + 1])
+    torch.cuda.synchronize()
+    assert vst.ctx_check(ctx.handle) == vst.OK
+    ctx.close()
+    return outs
+
+
+def test_dec_short_parity(dev, dec_module):
+    n = 300
+    q, k, v = _dec_seq(3, 0, 0, n)
+    outs = _run_dec(dec_module, q, k, v, fill=0, steps=n)
+    want = oracle.attention(synth.bits(q), synth.bits(k), synth.bits(v), window=8192, threads=8)
+    _compare(outs, want, "decoder from empty")
+
+
+def test_dec_wrap_parity_and_ring_ab(dev, dec_module):
+    """Fill past the 8192 window so the modulo ring wraps, then step across more wraps;
+    compare sampled steps with the oracle and the whole run with a 16384-slot ring."""
+    fill, steps = 8190, 40
+    n = fill + steps
+    q, k, v = _dec_seq(3, 1, 0, n)
+    outs = _run_dec(dec_module, q, k, v, fill=fill, steps=steps)
+    cfg = vst.config_default(vst.DEC)
+    cfg.ring_slots = 16384
+    big = vst.Module(cfg)
+    outs_big = _run_dec(big, q, k, v, fill=fill, steps=steps)
+    big.close()
+    assert torch.equal(outs, outs_big)
+    qb, kb, vb = synth.bits(q), synth.bits(k), synth.bits(v)
+    got = outs.float().cpu().double().numpy()
+    for s in (0, 1, 2, 17, 39):
+        i = fill + s
+        j0 = max(0, i - 8191)
+        want = oracle.attention_row(qb[i], kb[j0:i + 1], vb[j0:i + 1], i, 8192)
+        d = np.abs(got[s] - want)
+        assert d.max() <= MAX_TOL and d.mean() <= MEAN_TOL, (s, d.max(), d.mean())
+
+
+def test_dec_batched_equals_single(dev, dec_module):
+    """One vst_dec_step over 6 contexts with different fills = 6 single-stream steps."""
+    fills = [0, 1, 127, 128, 4000, 9000]
+    steps = 3
+    seqs = [_dec_seq(4, s, 0, f + steps) for s, f in enumerate(fills)]
+    singles = [_run_dec(dec_module, *seqs[s], fill=f, steps=steps) for s, f in enumerate(fills)]
+    ctxs = [vst.Ctx(dec_module) for _ in fills]
+    for c, (q, k, v), f in zip(ctxs, seqs, fills):
+        if f:
+            vst.dec_append(c.handle, k[:f].to(dev), v[:f].to(dev))
+    for s in range(steps):
+        Q = torch.stack([q[f + s] for (q, k, v), f in zip(seqs, fills)]).to(dev)
+        K = torch.stack([k[f + s] for (q, k, v), f in zip(seqs, fills)]).to(dev)
+        V = torch.stack([v[f + s] for (q, k, v), f in zip(seqs, fills)]).to(dev)
+        O = torch.empty_like(Q)
+        vst.dec_step([c.handle for c in ctxs], Q, K, V, O)
+        for i in range(len(fills)):
+            assert torch.equal(O[i], singles[i][s]), (i, s)
+    for c in ctxs:
+        c.close()
+
+
+def test_dec_append_ring_contents(dev, dec_module):
+    """Token p lands in slot p % 8192 as bf16(RoPE(k, p)) (within bf16 rounding of the fp64
+    oracle) and V bit for bit; the step path writes the same bytes as the append path."""
+    n = 8192 + 300
+    _, k, v = _dec_seq(9, 0, 0, n)
+    ctx = TorchCtx(dec_module, dev)
+    vst.dec_append(ctx.handle, k.to(dev), v.to(dev))
+    torch.cuda.synchronize()
+    pos = np.arange(n - 8192, n)
+    slots = torch.from_numpy(pos % 8192).to(dev)
+    krot = oracle.rope_rows(synth.bits(k[n - 8192:]), n - 8192)
+    got = ctx.k_ring[:, slots].float().cpu().double().numpy().transpose(1, 0, 2)
+    assert np.abs(got - krot).max() <= np.abs(krot).max() * 2 ** -8 + 1e-6
+    assert torch.equal(ctx.v_ring[:, slots].cpu(), v[n - 8192:].transpose(0, 1).contiguous())
+    # one more token through the step path: same bytes as appending it
+    q1, k1, v1 = _dec_seq(9, 0, 0, 1, first=n)
+    ctx2 = TorchCtx(dec_module, dev)
+    vst.dec_append(ctx2.handle, torch.cat([k, k1]).to(dev), torch.cat([v, v1]).to(dev))
+    o = torch.empty((1, 32, 128), dtype=torch.bfloat16, device=dev)
+    vst.dec_step([ctx.handle], q1.to(dev), k1.to(dev), v1.to(dev), o)
+    torch.cuda.synchronize()
+    assert torch.equal(ctx.k_ring, ctx2.k_ring)
+    assert torch.equal(ctx.v_ring, ctx2.v_ring)
+    ctx.close()
+    ctx2.close()

@@ -1,0 +1,112 @@
+"""CPU-only checks of the C ABI: the library loads without a GPU, exports exactly what
+include/vst.h declares, the binding declares the same names, and the host logic (config
+validation, the encoder feed schedule) behaves as the pages' rules say. No compute call."""
+import ctypes
+import os
+import random
+import re
+
+import pytest
+
+import oracle
+from sliding_window_kv_gb300 import vst
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "vst.h")).read()
+    return sorted(set(re.findall(r"^VST_API\s+[\w\s\*]+?\b(vst_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_loads_and_exports_header(page_constants):
+    L = vst.lib()
+    names = header_functions()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(vst.EXPORTS) == names
+
+
+def test_version_and_status_strings():
+    assert re.match(r"^\d+\.\d+\.\d+$", vst.version())
+    for s in (0, -1, -2, -3, -4, -5, -6):
+        assert vst.status_str(s)
+
+
+def test_default_configs_match_pages(page_constants):
+    c = page_constants
+    e = vst.config_default(vst.ENC)
+    assert (e.n_heads, e.n_kv_heads, e.head_dim, e.window, e.ring_slots, e.max_batch) == (
+        c["enc_heads"], c["enc_heads"], c["enc_head_dim"], c["enc_window"], c["enc_ring_slots"], c["enc_max_batch"])
+    d = vst.config_default(vst.DEC)
+    assert (d.n_heads, d.n_kv_heads, d.head_dim, d.window) == (
+        c["dec_q_heads"], c["dec_kv_heads"], c["dec_head_dim"], c["dec_window"])
+    assert e.rope_theta == d.rope_theta == c["rope_theta"]
+    assert d.max_position == c["max_position"]
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 32, vst.E_UNSUPPORTED), ("window", 0, vst.E_INVAL), ("ring_slots", 1000, vst.E_INVAL),
+    ("n_kv_heads", 3, vst.E_INVAL), ("reserved", 1, vst.E_INVAL), ("max_batch", 1024, vst.E_INVAL),
+    ("rope_theta", -1.0, vst.E_INVAL), ("kind", 7, vst.E_INVAL)])
+def test_bad_encoder_configs_rejected_before_cuda(field, value, status):
+    c = vst.config_default(vst.ENC)
+    setattr(c, field, value)
+    h = ctypes.c_void_p()
+    assert vst.lib().vst_module_create(ctypes.byref(c), ctypes.byref(h)) == status
+    assert not h.value
+
+
+def test_batch_over_512_unsupported():
+    c = vst.config_default(vst.ENC)
+    c.ring_slots, c.max_batch = 4096, 1024
+    h = ctypes.c_void_p()
+    assert vst.lib().vst_module_create(ctypes.byref(c), ctypes.byref(h)) == vst.E_UNSUPPORTED
+
+
+def test_bad_decoder_configs_rejected_before_cuda():
+    for field, value, status in [("n_heads", 16, vst.E_UNSUPPORTED), ("ring_slots", 8000, vst.E_INVAL),
+                                 ("ring_slots", 8192 + 64, vst.E_UNSUPPORTED), ("head_dim", 64, vst.E_UNSUPPORTED)]:
+        c = vst.config_default(vst.DEC)
+        setattr(c, field, value)
+        h = ctypes.c_void_p()
+        assert vst.lib().vst_module_create(ctypes.byref(c), ctypes.byref(h)) == status, (field, value)
+
+
+def test_null_arguments_rejected():
+    L = vst.lib()
+    assert L.vst_enc_feed(None, None, None, None, 1, None, None) == vst.E_INVAL
+    assert L.vst_dec_step(None, 1, None, None, None, None, None) == vst.E_INVAL
+    assert L.vst_ctx_reset(None, None) == vst.E_INVAL
+    assert L.vst_ctx_compact(None, None) == vst.E_INVAL
+    assert L.vst_ctx_bytes(None) == 0
+
+
+def test_enc_plan_matches_oracle_ring():
+    """The schedule vst_enc_feed enqueues equals the oracle's ring bookkeeping (bit-exact
+    integer work), for random feed sizes including 0, 1 and more than a batch."""
+    cfg = vst.config_default(vst.ENC)
+    rng = random.Random(11)
+    for trial in range(20):
+        st = oracle.RingState()
+        n_kv, base = 0, 0
+        for _ in range(200):
+            n = rng.choice([0, 1, 3, 24, 48, 50, 100, 511, 512, 513, 1024, 2000])
+            steps, n_kv, base = vst.enc_plan(cfg, n_kv, base, n)
+            before = st.n_compactions
+            st.feed(n)
+            assert (n_kv, base) == (st.n_kv, st.abs_base)
+            assert sum(b for b, _ in steps) == n
+            assert all(0 < b <= 512 for b, _ in steps)
+            assert sum(c for _, c in steps) == st.n_compactions - before
+
+
+def test_enc_plan_hand_cases():
+    cfg = vst.config_default(vst.ENC)
+    steps, n_kv, base = vst.enc_plan(cfg, 0, 0, 2000)
+    assert steps == [(512, 0), (512, 0), (512, 0), (464, 1)] and (n_kv, base) == (1214, 786)
+    steps, n_kv, base = vst.enc_plan(cfg, 1500, 0, 50)
+    assert steps == [(50, 1)] and (n_kv, base) == (800, 750)
+    steps, n_kv, base = vst.enc_plan(cfg, 1486, 0, 50)
+    assert steps == [(50, 0)] and (n_kv, base) == (1536, 0)
