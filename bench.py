@@ -1,0 +1,700 @@
+#!/usr/bin/env python
+"""Benchmark of the sliding-window KV attention path on one GB300.
+
+Default line (the configuration the metric is quoted on): the encoder streaming workload
+-- 32 layers x 20 heads x 64, window 750, ring 1536, one stream of 4416 frames fed in
+50-frame chunks (88 x 50 + 16, four lazy compactions per layer). One step streams the whole
+clip through all 32 layers (contexts reset at the start of the step), so every step covers
+feed bookkeeping, compaction, RoPE + append and chunk attention. `value` is encoder frames
+per second with inputs resident in HBM, measured on CUDA-graph replays of the step.
+
+The same line carries `dec`: the decoder step workload (26 layers, GQA 32q/8kv x 128, KV
+filled to 8192, batch 1, 256 steps across the ring wrap) in decoder steps per second, so
+both halves of the metric are reported. `--workload` selects the other configurations for
+exploration (they print the same kind of line).
+
+Inputs are synthetic (seeded counter-based bf16 ~N(0,1), sliding_window_kv_gb300.synth);
+the per-step inputs and caches exceed the 129 MB L2, so no flush is needed between steps.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "streamed enc frames/s + dec steps/s (1 GPU); % of HBM / BF16 tensor roofline"
+
+ENC_H, ENC_D, ENC_W = 20, 64, 750
+DEC_H, DEC_HK, DEC_D, DEC_W = 32, 8, 128, 8192
+
+WORKLOADS = {
+    # configs[1]: the metric's configuration
+    "enc_stream": dict(kind="enc", layers=32, frames=4416, feed=50, streams=1, seed=2, stagger=0),
+    # configs[0]: small correctness case
+    "enc_small": dict(kind="enc", layers=1, frames=1000, feed=100, streams=1, seed=1, stagger=0),
+    # configs[4]: 16 concurrent streams, staggered starts (96*s frames), 512-frame batches
+    "enc_long16": dict(kind="enc", layers=32, frames=15300, feed=512, streams=16, seed=5, stagger=96),
+    # configs[2]: decoder batch 1
+    "dec_b1": dict(kind="dec", layers=26, streams=1, fill="full", steps=256, seed=3),
+    # configs[3]: decoder, 64 streams with fills uniform in [1, 8192]
+    "dec_b64": dict(kind="dec", layers=26, streams=64, fill="uniform", steps=256, seed=4),
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="vst", choices=["vst", "reference"])
+    ap.add_argument("--workload", default="enc_stream", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-dec", action="store_true", help="skip the decoder object of the default line")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dec-steps", type=int, default=256, help="decoder steps (decoder workloads and dec object)")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+class Dist:
+    def __init__(self, n_gpus: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if _cuda_ok() else "gloo"
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if _cuda_ok() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def _cuda_ok():
+    import torch
+    return torch.cuda.is_available()
+
+
+# ---------------------------------------------------------------- clocks during timing
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int = 0):
+        self.proc = None
+        self.lines = []
+        self.sel = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if uuid:
+                self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "100"] + self.sel, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+
+def enc_feed_schedule(frames: int, feed: int):
+    out, t = [], 0
+    while t < frames:
+        n = min(feed, frames - t)
+        out.append((t, n))
+        t += n
+    return out
+
+
+class EncWorkload:
+    """Streams `frames` frames per stream through `layers` encoder layers in `feed`-frame
+    chunks; stream s first gets an extra 96*s-frame feed (staggered start) when stagger.
+
+    Inputs of one layer live in one contiguous buffer per tensor, laid out feed after feed
+    as [S][n][H][D] blocks (what vst_enc_feed_batch takes), so a host copy of a layer's
+    inputs is one copy per tensor."""
+
+    def __init__(self, spec, dev, rank=0):
+        import torch
+        from sliding_window_kv_gb300 import synth, vst
+        self.vst = vst
+        self.spec = spec
+        self.L, self.S = spec["layers"], spec["streams"]
+        self.frames, self.feed = spec["frames"], spec["feed"]
+        self.pre = [spec["stagger"] * s for s in range(self.S)]
+        self.module = vst.Module(vst.ENC)
+        self.ctxs = [[vst.Ctx(self.module) for _ in range(self.S)] for _ in range(self.L)]
+        self.sched = enc_feed_schedule(self.frames, self.feed)
+        seed = spec["seed"] + 1000 * rank
+        HD = ENC_H * ENC_D
+        self.buf = []      # [layer][role] flat bf16 buffers (q, k, v, out)
+        self.views = []    # [layer][role][feed] -> [S][n][H][D] views
+        self.pbuf = []     # [layer][role] flat pre-feed buffers (all streams back to back)
+        self.pviews = []   # [layer][role][stream] -> [pre_s][H][D]
+        npre = sum(self.pre)
+        for l in range(self.L):
+            bl = [torch.empty(self.S * self.frames * HD, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+            pl = [torch.empty(max(1, npre) * HD, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+            vl = [[None] * len(self.sched) for _ in range(4)]
+            pv = [[None] * self.S for _ in range(4)]
+            for f, (t, n) in enumerate(self.sched):
+                for i in range(4):
+                    vl[i][f] = bl[i][self.S * t * HD:self.S * (t + n) * HD].view(self.S, n, ENC_H, ENC_D)
+            off = 0
+            for s in range(self.S):
+                for i in range(4):
+                    pv[i][s] = pl[i][off * HD:(off + self.pre[s]) * HD].view(self.pre[s], ENC_H, ENC_D)
+                off += self.pre[s]
+            for i in range(3):
+                for s in range(self.S):
+                    x = synth.frames(synth.tensor_key(seed, s, l, i), 0, self.pre[s] + self.frames, ENC_H, ENC_D, dev)
+                    if self.pre[s]:
+                        pv[i][s].copy_(x[:self.pre[s]])
+                    for f, (t, n) in enumerate(self.sched):
+                        vl[i][f][s].copy_(x[self.pre[s] + t:self.pre[s] + t + n])
+                    del x
+            self.buf.append(bl)
+            self.pbuf.append(pl)
+            self.views.append(vl)
+            self.pviews.append(pv)
+        self.frames_per_step = npre + self.S * self.frames
+        self.in_bytes = self.L * 3 * (self.S * self.frames + npre) * HD * 2
+        self.out_bytes = self.L * (self.S * self.frames + npre) * HD * 2
+
+    def run_step(self, stream):
+        vst = self.vst
+        for l in range(self.L):
+            for c in self.ctxs[l]:
+                vst.ctx_reset(c.handle, stream)
+        for l in range(self.L):
+            pv = self.pviews[l]
+            for s in range(self.S):
+                if self.pre[s]:
+                    vst.enc_feed(self.ctxs[l][s].handle, pv[0][s], pv[1][s], pv[2][s], pv[3][s], stream)
+        for f, (t, n) in enumerate(self.sched):
+            for l in range(self.L):
+                q, k, v, o = (self.views[l][i][f] for i in range(4))
+                if self.S == 1:
+                    vst.enc_feed(self.ctxs[l][0].handle, q[0], k[0], v[0], o[0], stream, n_new=n)
+                else:
+                    vst.enc_feed_batch([c.handle for c in self.ctxs[l]], q, k, v, o, n, stream)
+
+    def host_buffers(self):
+        """Pinned host copies of the step's inputs and room for its outputs (for e2e)."""
+        import torch
+        npre = sum(self.pre)
+        hin = [[self.buf[l][i].cpu().pin_memory() for i in range(3)] for l in range(self.L)]
+        hin_pre = [[self.pbuf[l][i].cpu().pin_memory() for i in range(3)] for l in range(self.L)] if npre else None
+        hout = [torch.empty(self.buf[l][3].shape, dtype=torch.bfloat16, pin_memory=True) for l in range(self.L)]
+        hout_pre = [torch.empty(self.pbuf[l][3].shape, dtype=torch.bfloat16, pin_memory=True)
+                    for l in range(self.L)] if npre else None
+        return hin, hin_pre, hout, hout_pre
+
+    def e2e_step(self, bufs, stream):
+        hin, hin_pre, hout, hout_pre = bufs
+        for l in range(self.L):
+            for i in range(3):
+                self.buf[l][i].copy_(hin[l][i], non_blocking=True)
+                if hin_pre:
+                    self.pbuf[l][i].copy_(hin_pre[l][i], non_blocking=True)
+        self.run_step(stream)
+        for l in range(self.L):
+            hout[l].copy_(self.buf[l][3], non_blocking=True)
+            if hout_pre:
+                hout_pre[l].copy_(self.pbuf[l][3], non_blocking=True)
+
+    def attn_flops(self):
+        """Algorithmic FLOPs of kernel (b) per step: 4*D per visible (query, key) pair, per
+        head and layer: sum over rows at absolute position p of min(W, p+1)."""
+        pairs = 0
+        for s in range(self.S):
+            n = self.pre[s] + self.frames
+            pairs += ENC_W * (ENC_W + 1) // 2 if n >= ENC_W else n * (n + 1) // 2
+            pairs += max(0, n - ENC_W) * ENC_W
+        return 4.0 * ENC_D * ENC_H * self.L * pairs
+
+    def compact_bytes(self):
+        """Algorithmic bytes of kernel (d) per step: each compaction reads and writes 750
+        rows of K and V for every head (ring rule: compact before a batch that would not
+        fit in 1536 rows; feeds pushed in batches of at most 512)."""
+        n = 0
+        for s in range(self.S):
+            n_kv = 0
+            for chunk in ([self.pre[s]] if self.pre[s] else []) + [c for (_, c) in self.sched]:
+                t = chunk
+                while t > 0:
+                    b = min(512, t)
+                    if n_kv + b > 1536:
+                        n_kv = 750
+                        n += 1
+                    n_kv += b
+                    t -= b
+        return n * self.L * 2 * 2 * ENC_H * ENC_W * ENC_D * 2
+
+    def close(self):
+        for row in self.ctxs:
+            for c in row:
+                c.close()
+        self.module.close()
+
+
+class DecWorkload:
+    """26 decoder layers; each stream's cache filled (untimed) then `steps` decoder steps.
+    Inputs of step t, layer l are [S][H][D] / [S][Hk][D] slices of per-layer buffers."""
+
+    def __init__(self, spec, dev, n_steps, rank=0):
+        import torch
+        from sliding_window_kv_gb300 import synth, vst
+        self.vst = vst
+        self.L, self.S, self.steps = spec["layers"], spec["streams"], n_steps
+        seed = spec["seed"] + 1000 * rank
+        if spec["fill"] == "full":
+            self.fills = [DEC_W] * self.S
+        else:
+            self.fills = synth.uniform_int(synth.tensor_key(seed, 99), self.S, 1, DEC_W)
+        self.module = vst.Module(vst.DEC)
+        self.ctxs = [[vst.Ctx(self.module) for _ in range(self.S)] for _ in range(self.L)]
+        self.Q, self.K, self.V, self.O = [], [], [], []
+        for l in range(self.L):
+            qs, ks, vs = [], [], []
+            for s in range(self.S):
+                f = self.fills[s]
+                k = synth.frames(synth.tensor_key(seed, s, l, 1), 0, f + self.steps, DEC_HK, DEC_D, dev)
+                v = synth.frames(synth.tensor_key(seed, s, l, 2), 0, f + self.steps, DEC_HK, DEC_D, dev)
+                vst.dec_append(self.ctxs[l][s].handle, k[:f], v[:f])
+                qs.append(synth.frames(synth.tensor_key(seed, s, l, 0), f, self.steps, DEC_H, DEC_D, dev))
+                ks.append(k[f:])
+                vs.append(v[f:])
+            # [steps][S][...] so that step t is one contiguous [S][...] block
+            self.Q.append(torch.stack(qs, 1).contiguous())
+            self.K.append(torch.stack(ks, 1).contiguous())
+            self.V.append(torch.stack(vs, 1).contiguous())
+            self.O.append(torch.empty_like(self.Q[-1]))
+            torch.cuda.synchronize()
+
+    def positions(self):
+        return [self.vst.ctx_info_get(self.ctxs[0][s].handle).abs_next for s in range(self.S)]
+
+    def run_steps(self, stream):
+        vst = self.vst
+        for t in range(self.steps):
+            for l in range(self.L):
+                vst.dec_step([c.handle for c in self.ctxs[l]], self.Q[l][t], self.K[l][t], self.V[l][t],
+                             self.O[l][t], stream)
+
+    def kv_bytes(self, start_positions):
+        """Algorithmic bytes of kernel (c) for one run of the steps starting at the given
+        positions: K and V of every visible key (min(pos+1, W) keys x Hk x D x 2 B x 2)
+        plus the step's q, k, v and out."""
+        per_key = DEC_HK * DEC_D * 2 * 2
+        io = (DEC_H * DEC_D * 2) * 2 + DEC_HK * DEC_D * 2 * 2
+        tot = 0
+        for p0 in start_positions:
+            for t in range(self.steps):
+                tot += min(p0 + t + 1, DEC_W) * per_key + io
+        return tot * self.L
+
+    def close(self):
+        for row in self.ctxs:
+            for c in row:
+                c.close()
+        self.module.close()
+
+
+# ---------------------------------------------------------------- timing helpers
+
+def capture(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        fn(torch.cuda.current_stream())
+    return g
+
+
+def time_graph(g, stream, n, dist=None):
+    import torch
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(n):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    return a.elapsed_time(b)
+
+
+def profiled_kernels(step_fn, stream):
+    """Capture one step with per-kernel events on, replay it twice, return the second
+    replay's {kernel: (launches, total_ms)}."""
+    import torch
+    from sliding_window_kv_gb300 import vst
+    vst.prof_read()
+    vst.prof_enable(True)
+    try:
+        g = capture(step_fn, stream)
+    finally:
+        vst.prof_enable(False)
+    g.replay()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    return vst.prof_read()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def dram_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it is current."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        return d.get(kernel)
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- CPU baseline (oracle)
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_enc(spec, layers_sample: int, threads: int):
+    """Time the fp64 oracle on `layers_sample` layers of stream 0 of the workload (whole
+    clip per layer) and scale to encoder frames/s of the full workload."""
+    import oracle
+    from sliding_window_kv_gb300 import synth
+    n = spec["frames"]
+    seed = spec["seed"]
+    ins = []
+    for l in range(layers_sample):
+        ins.append([synth.bits(synth.frames(synth.tensor_key(seed, 0, l, i), 0, n, ENC_H, ENC_D)) for i in range(3)])
+    t0 = time.perf_counter()
+    for q, k, v in ins:
+        oracle.attention(q, k, v, ENC_W, threads=threads)
+    dt = time.perf_counter() - t0
+    per_layer = dt / layers_sample
+    fps = n / (per_layer * spec["layers"])
+    return fps, dt, "oracle on %d of %d layers, whole %d-frame clip of stream 0, %d threads" % (
+        layers_sample, spec["layers"], n, threads)
+
+
+def cpu_baseline_dec(spec, steps_sample: int, threads: int):
+    """Time the oracle for `steps_sample` decoder steps of one layer at a full 8192 window
+    and scale to decoder steps/s of the 26-layer step."""
+    import numpy as np
+
+    import oracle
+    from sliding_window_kv_gb300 import synth
+    seed = spec["seed"]
+    fill = DEC_W
+    n = fill + steps_sample
+    q = synth.bits(synth.frames(synth.tensor_key(seed, 0, 0, 0), 0, n, DEC_H, DEC_D))
+    k = synth.bits(synth.frames(synth.tensor_key(seed, 0, 0, 1), 0, n, DEC_HK, DEC_D))
+    v = synth.bits(synth.frames(synth.tensor_key(seed, 0, 0, 2), 0, n, DEC_HK, DEC_D))
+    t0 = time.perf_counter()
+    qr = np.zeros((n, DEC_H, DEC_D))
+    qr[fill:] = oracle.rope_rows(q[fill:], fill)
+    kr = oracle.rope_rows(k, 0)
+    vv = oracle.bf16_to_double(v)
+    oracle.attend(qr, kr, vv, DEC_W, rows=(fill, n), threads=threads)
+    dt = time.perf_counter() - t0
+    sps = steps_sample / (dt * spec["layers"])
+    return sps, dt, "oracle on 1 of %d layers, %d steps at window 8192 (incl. RoPE of the window), %d threads" % (
+        spec["layers"], steps_sample, threads)
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, dist):
+    """The oracle as it stands, on this host's cores, over a bounded sample per step."""
+    if dist.rank != 0:
+        return
+    spec = WORKLOADS[args.workload]
+    threads = cpu_threads()
+    vals = []
+    for i in range(args.warmup + args.steps):
+        if spec["kind"] == "enc":
+            v, dt, sample = cpu_baseline_enc(spec, 1, threads)
+        else:
+            v, dt, sample = cpu_baseline_dec(spec, 8, threads)
+        if i >= args.warmup:
+            vals.append((v, dt))
+    total = sum(dt for _, dt in vals)
+    value = statistics.mean(v for v, _ in vals)
+    unit = "enc frames/s" if spec["kind"] == "enc" else "dec steps/s"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / max(1, len(vals)),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(args.workload, spec),
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def workload_config(name, spec):
+    if spec["kind"] == "enc":
+        return {"workload": "enc_%dL_%dx%d_W%d_ring1536_%dstream_%dframes_chunk%d%s" % (
+            spec["layers"], ENC_H, ENC_D, ENC_W, spec["streams"], spec["frames"], spec["feed"],
+            "_stagger%d" % spec["stagger"] if spec["stagger"] else ""),
+            "layers": spec["layers"], "streams": spec["streams"], "frames_per_stream": spec["frames"],
+            "chunk": spec["feed"], "seed": spec["seed"],
+            "l2": "inputs larger than L2 (no flush)"}
+    return {"workload": "dec_%dL_gqa%d-%dx%d_W%d_%dstreams_fill_%s_steps%d" % (
+        spec["layers"], DEC_H, DEC_HK, DEC_D, DEC_W, spec["streams"], spec["fill"], spec["steps"]),
+        "layers": spec["layers"], "streams": spec["streams"], "steps": spec["steps"], "seed": spec["seed"],
+        "l2": "KV cache read per step larger than L2 (no flush)"}
+
+
+def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu):
+    import torch
+    from sliding_window_kv_gb300 import vst
+    w = DecWorkload(spec, dev, n_steps, dist.rank)
+    w.run_steps(stream)  # eager warm-up (also configures kernels)
+    torch.cuda.synchronize()
+    n0 = vst.launch_count()
+    g = capture(w.run_steps, stream)
+    launches = vst.launch_count() - n0
+    for _ in range(max(1, warmup)):
+        g.replay()
+    ms = time_graph(g, stream, 1, dist)
+    ms = dist.max(ms)
+    steps_per_s = dist.world * w.steps / (ms / 1e3)
+    start_pos = w.positions()
+    prof = profiled_kernels(w.run_steps, stream)
+    nl, kms = prof["dec_step_kernel"]
+    bytes_per_launch = w.kv_bytes(start_pos) / max(1, nl)
+    achieved = bytes_per_launch / (kms / nl / 1e3) / 1e9
+    hbm, _, _, src = peaks
+    out = {"value": steps_per_s, "unit": "dec steps/s", "config": workload_config("", spec),
+           "ms_per_step": ms / w.steps, "gpu_launches": launches,
+           "roofline": {"kernel": "dec_step_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm,
+                        "unit": "GB/s", "frac": achieved / hbm, "traffic": dram_traffic("dec_step_kernel"),
+                        "peak_source": src, "launches": nl, "avg_launch_us": 1e3 * kms / nl,
+                        "algorithmic_bytes_per_launch": bytes_per_launch}}
+    if want_cpu:
+        v, dt, sample = cpu_baseline_dec(spec, 16, cpu_threads())
+        out["cpu_baseline"] = {"value": v, "unit": "dec steps/s", "cores": cpu_threads(), "kind": "oracle",
+                               "sample": sample}
+    w.close()
+    return out
+
+
+def run_vst(args, dist):
+    import torch
+    from sliding_window_kv_gb300 import vst
+    if not torch.cuda.is_available():
+        raise RuntimeError("no CUDA device: the benchmark needs the GPU (there is no CPU path)")
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    vst.lib()
+    stream = torch.cuda.Stream(dev)
+    peaks = load_peaks()
+    spec = dict(WORKLOADS[args.workload])
+    if args.layers:
+        spec["layers"] = args.layers
+    if spec["kind"] == "dec":
+        spec["steps"] = args.dec_steps
+    sampler = ClockSampler(dist.local_rank)
+    line = {"metric": METRIC, "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded counter-hash bf16 ~N(0,1))", "impl": "vst"}
+
+    if spec["kind"] == "dec":
+        with torch.cuda.stream(stream):
+            sampler.start()
+            d = bench_dec(spec, dev, stream, dist, spec["steps"], args.warmup, peaks, not args.no_cpu and dist.rank == 0)
+            clocks = sampler.stop()
+        line.update({"value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"], "config": d["config"],
+                     "roofline": d["roofline"], "gpu_launches": d["gpu_launches"], "clocks": clocks})
+        if "cpu_baseline" in d:
+            line["cpu_baseline"] = d["cpu_baseline"]
+        if dist.rank == 0:
+            print(json.dumps(line))
+        return
+
+    w = EncWorkload(spec, dev, dist.rank)
+    with torch.cuda.stream(stream):
+        w.run_step(stream)  # eager warm-up
+        torch.cuda.synchronize()
+        n0 = vst.launch_count()
+        g = capture(w.run_step, stream)
+        launches_per_step = vst.launch_count() - n0
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        sampler.start()
+        ms = time_graph(g, stream, args.steps, dist)
+        ms = dist.max(ms)
+        value = dist.world * w.frames_per_step * args.steps / (ms / 1e3)
+        prof = profiled_kernels(w.run_step, stream)
+        clocks = sampler.stop()
+        del g
+
+        # dominant kernel: chunk attention (kernel b), tensor-bound
+        nl, kms = prof["enc_attn_kernel"]
+        flops_per_launch = w.attn_flops() / max(1, nl)
+        achieved = flops_per_launch / (kms / nl / 1e3) / 1e12
+        hbm, tf, tfs, src = peaks
+        line.update({"value": value, "unit": "enc frames/s", "ms_per_step": ms / args.steps,
+                     "config": workload_config(args.workload, spec),
+                     "roofline": {"kernel": "enc_attn_kernel", "bound": "tensor", "achieved": achieved, "peak": tf,
+                                  "unit": "TFLOP/s", "frac": achieved / tf, "traffic": dram_traffic("enc_attn_kernel"),
+                                  "peak_source": src + " bf16 burst", "launches": nl,
+                                  "avg_launch_us": 1e3 * kms / nl, "algorithmic_flops_per_launch": flops_per_launch},
+                     "kernels": {k: {"launches": v[0], "total_ms": v[1]} for k, v in prof.items() if v[0]},
+                     "gpu_launches": launches_per_step * args.steps, "clocks": clocks})
+        ncmp, cms = prof["compact_kernel"]
+        if ncmp:
+            cb = w.compact_bytes() / ncmp
+            line["compaction"] = {"kernel": "compact_kernel", "bound": "hbm", "launches": ncmp,
+                                  "avg_launch_us": 1e3 * cms / ncmp, "algorithmic_bytes_per_launch": cb,
+                                  "achieved_gbs": cb / (cms / ncmp / 1e3) / 1e9,
+                                  "frac": cb / (cms / ncmp / 1e3) / 1e9 / hbm}
+
+        if not args.no_e2e:
+            bufs = w.host_buffers()
+            w.e2e_step(bufs, stream)
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            e2e_steps = max(1, min(args.steps, 5))
+            dist.barrier()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            a.record(stream)
+            for _ in range(e2e_steps):
+                w.e2e_step(bufs, stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - t0
+            dist.barrier()
+            ems = dist.max(a.elapsed_time(b))
+            line["e2e"] = {"value": dist.world * w.frames_per_step * e2e_steps / (ems / 1e3), "unit": "enc frames/s",
+                           "h2d_bytes_per_step": w.in_bytes, "d2h_bytes_per_step": w.out_bytes,
+                           "steps": e2e_steps, "host_wall_s": wall,
+                           "path": "vst_enc_feed per layer and feed (no graph), pinned host copies in the region"}
+            del bufs
+        w.close()
+
+        if not args.no_dec and args.workload == "enc_stream":
+            sampler2 = ClockSampler(dist.local_rank)
+            sampler2.start()
+            dspec = dict(WORKLOADS["dec_b1"])
+            dspec["steps"] = args.dec_steps
+            d = bench_dec(dspec, dev, stream, dist, args.dec_steps, args.warmup, peaks,
+                          not args.no_cpu and dist.rank == 0)
+            d["clocks"] = sampler2.stop()
+            line["dec"] = d
+
+    if not args.no_cpu and dist.rank == 0:
+        v, dt, sample = cpu_baseline_enc(spec, 4 if spec["layers"] >= 4 else spec["layers"], cpu_threads())
+        line["cpu_baseline"] = {"value": v, "unit": "enc frames/s", "cores": cpu_threads(), "kind": "oracle",
+                                "sample": sample, "seconds": dt}
+    if dist.rank == 0:
+        print(json.dumps(line))
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if world > 1 and rank != 0:
+            return
+        class _D:
+            rank = 0
+        run_reference(args, _D())
+        return
+    dist = Dist(args.gpus)
+    try:
+        run_vst(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

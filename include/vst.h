@@ -165,6 +165,27 @@ VST_API vst_status vst_dec_step(vst_ctx* const* ctxs, int32_t n_streams, const v
  * decoder ctx: k/v [n][Hk][D]. Used to fill a cache. */
 VST_API vst_status vst_dec_append(vst_ctx* c, const void* k, const void* v, int32_t n, void* stream);
 
+/* ---- kernel timing (tracing) -------------------------------------------------------------
+ * When enabled, every kernel launch of this library is bracketed by two CUDA events
+ * recorded on the launching stream (the kernel-level analogue of the pages' per-component
+ * stream timer, family doc, Streaming row, item (7)). Off by default; costs two event
+ * records per launch when on. One device per process while enabled. */
+typedef enum { VST_K_ROPE_APPEND = 0, VST_K_COMPACT = 1, VST_K_ENC_ATTN = 2, VST_K_DEC_STEP = 3,
+               VST_K_COUNT = 4 } vst_kernel_id;
+typedef struct {
+    int32_t kernel;    /* vst_kernel_id */
+    int32_t reserved;
+    int64_t launches;  /* launches timed since the last read */
+    double total_ms;   /* sum of their event-to-event durations */
+} vst_prof_stat;
+VST_API vst_status vst_prof_enable(int32_t on);
+/* Wait for the recorded events, fill out[0 .. VST_K_COUNT-1] (one entry per kernel id) and
+ * forget them. Blocking. */
+VST_API vst_status vst_prof_read(vst_prof_stat* out, int32_t max);
+/* Kernels launched by this library since it was loaded (always counted). */
+VST_API int64_t vst_launch_count(void);
+VST_API const char* vst_kernel_name(int32_t kernel);
+
 VST_API const char* vst_status_str(vst_status s);
 /* Library version, "major.minor.patch". */
 VST_API const char* vst_version(void);

@@ -6,22 +6,23 @@
 // token cur writes slot cur % n_ctx (evicting cur-8192), the step mask reveals
 // [cur-8191, cur], positions stay absolute.
 //
-// Work item: one CTA per (stream, KV head, split), a split being the 128 absolute positions
-// [128*sigma, 128*sigma + 128); the splits of a step are those that meet
-// [max(0, pos-W+1), pos]. Each CTA
-//   1. TMA-loads the split's K and V rows (slots 128*sigma mod R, 2 x 64-dim boxes each,
-//      128-B swizzle) -- 64 KB per CTA, all in flight at once;
-//   2. meanwhile rotates the 4 query heads of its group (fp32, scaled to log2 units) and,
-//      if the split holds pos, rotates the new key: that row of the smem tile is replaced
-//      by K'/V of this step and the same bytes are stored to ring slot pos % R;
-//   3. scores: one thread per key, 4 heads; masked keys get -inf;
-//   4. split-local softmax (max and sum by warp shuffles, then across the 4 warps in fixed
-//      order) and P.V (two key halves, combined in fixed order);
-//   5. writes its partial (m, l, o) and bumps a per-(stream, KV head) counter; the CTA that
-//      finishes last folds all partials of its group in ascending split order and writes
-//      the output, then re-arms the counter.
-// The fold order depends only on absolute positions, so a stream's output is the same bits
-// whether it runs alone or in a batch, and whatever the ring size.
+// Work item: one CTA per (stream, KV head g, split), a split being the 512 absolute
+// positions [512*sigma, 512*sigma + 512) -- four key tiles of 128 -- cut to the step's
+// window [max(0, pos-W+1), pos]. The CTA streams its tiles through a two-stage TMA ring
+// (K and V of a tile, 64 KB per stage, 128-B swizzle, slots 128*tau mod R) and for each tile:
+//   S^T = K Q'^T     tcgen05.mma M=128 keys, N=16 (the 4 query heads of the group, zero
+//                    padded), K=128 dims; A = K tile (K-major), B = Q' (K-major); in TMEM
+//   softmax          one key per thread (TMEM lane); per head: tile max and sum by warp
+//                    shuffles then across the 4 warps in fixed order; P^T -> smem (bf16)
+//   O^T = V^T P^T    tcgen05.mma M=128 dims, N=16, K=128 keys; A = V tile read as
+//                    MN-major (dims contiguous), B = P^T (K-major); in TMEM
+//   fold             thread d folds (m_t, l_t, O_t[d]) of the 4 heads into registers.
+// The query heads are rotated in the prologue; if the split holds pos, the new key is
+// rotated too, patched into its tile row in shared memory, and stored (K', V) to ring slot
+// pos % R by this CTA. Each CTA writes its split's (m, l, o) per head; the last CTA of
+// (stream, g) folds the splits in ascending order and writes the output. Tiles and splits
+// are fixed by absolute position, so a stream's output is the same bits alone or in a
+// batch, and whatever the ring size.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "vst_internal.h"
@@ -32,19 +33,21 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kD = 128;
-constexpr int kG = 4;                      // query heads per KV head
-constexpr uint32_t kBox = 128u * 128u;     // 128 keys x 64 dims x 2 B
-constexpr uint32_t kOffK0 = 0;
-constexpr uint32_t kOffK1 = kBox;
-constexpr uint32_t kOffV0 = 2 * kBox;
-constexpr uint32_t kOffV1 = 3 * kBox;
-constexpr uint32_t kOffQ = 4 * kBox;               // float [4][128]
-constexpr uint32_t kOffP = kOffQ + kG * kD * 4;    // float [4][128]
-constexpr uint32_t kOffRed = kOffP + kG * kD * 4;  // float [64][8]
-constexpr uint32_t kOffNew = kOffRed + 64 * 8 * 4; // bf16 K'[128], V[128]
-constexpr uint32_t kOffWarp = kOffNew + 512;       // float [4 warps][4 heads] x 2
-constexpr uint32_t kOffBar = kOffWarp + 2 * 16 * 4;
+constexpr int kG = 4;                       // query heads per KV head
+constexpr int kTile = kDecTile;             // keys per tile
+constexpr int kTilesPerSplit = kDecSplit / kTile;
+constexpr uint32_t kBox = 128u * 128u;      // 128 keys x 64 dims x 2 B
+constexpr uint32_t kStage = 4 * kBox;       // K lo, K hi, V lo, V hi
+constexpr uint32_t kOffQ = 2 * kStage;      // Q' [16 rows][128 dims]: 2 blocks of 2 KB
+constexpr uint32_t kOffP = kOffQ + 4096;    // P^T [16 rows][128 keys]: 2 blocks of 2 KB
+constexpr uint32_t kOffNew = kOffP + 4096;  // new K' row, new V row (bf16 x 128 each)
+constexpr uint32_t kOffRed = kOffNew + 512; // float [2][4 warps][4 heads]
+constexpr uint32_t kOffBar = kOffRed + 128;
 constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;
+constexpr uint32_t kTmemCols = 32;          // S^T in [0,16), O^T in [16,32)
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 16, false, false);
+constexpr uint32_t kIdescO = idesc_bf16_f32(128, 16, true, false);
 
 __device__ __forceinline__ float warp_max(float x)
 {
@@ -62,23 +65,43 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
+// Fold a tile-local (or split-local) softmax state into a running one (one value of o).
+__device__ __forceinline__ void fold1(float& m, float& l, float& o, float mt, float lt, float ot)
+{
+    const float mn = fmaxf(m, mt);
+    const float a = ex2(__fsub_rn(m, mn));
+    const float b = ex2(__fsub_rn(mt, mn));
+    l = __fmaf_rn(l, a, __fmul_rn(lt, b));
+    o = __fmaf_rn(o, a, __fmul_rn(ot, b));
+    m = mn;
+}
+
+__device__ __forceinline__ uint32_t sw16(int row, int col)
+{
+    // byte offset of element col (0..127) of row `row` in a [16][128] bf16 K-major operand
+    // stored as two 64-column blocks of 2 KB
+    return (uint32_t)((col >> 6) * 2048) + sw128_offset(row, (col & 63) >> 3) + (uint32_t)((col & 7) * 2);
+}
+
 }  // namespace
 
 template <int J>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
     dec_step_kernel(const __grid_constant__ KParams<DecCommon, DecJob, J> p)
 {
     extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t s_tmem;
     __shared__ int s_last;
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    float* sq = reinterpret_cast<float*>(smem + kOffQ);
-    float* sp = reinterpret_cast<float*>(smem + kOffP);
-    float* sred = reinterpret_cast<float*>(smem + kOffRed);
+    uint8_t* sQ = smem + kOffQ;
+    uint8_t* sP = smem + kOffP;
     __nv_bfloat16* snew = reinterpret_cast<__nv_bfloat16*>(smem + kOffNew);
-    float* swarp = reinterpret_cast<float*>(smem + kOffWarp);
+    float* sred = reinterpret_cast<float*>(smem + kOffRed);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    const uint32_t bar = smem_u32(&bars[0]);
+    const uint32_t bar_full0 = smem_u32(&bars[0]);
+    const uint32_t bar_full1 = smem_u32(&bars[1]);
+    const uint32_t bar_m = smem_u32(&bars[2]);
 
     const DecCommon& c = p.c;
     const int item = blockIdx.x;
@@ -89,28 +112,52 @@ __global__ void __launch_bounds__(kThreads)
     const int g = blockIdx.y;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int sl = item - job.work_begin;          // split index within this step
-    const long long key0 = (long long)(job.sigma0 + sl) * kDecSplit;
+    const int sl = item - job.work_begin;  // split index within this step
     const long long pos = job.pos;
     const long long lo = max(0LL, pos - c.W + 1);
-    const int slot0 = (int)(key0 % c.R);
-    const bool newest = pos >= key0 && pos < key0 + kDecSplit;
+    const long long sig = job.sigma0 + sl;
+    const long long tau_lo = max(sig * kTilesPerSplit, lo / kTile);
+    const long long tau_hi = min(sig * kTilesPerSplit + kTilesPerSplit - 1, pos / kTile);
+    const int n_tiles = (int)(tau_hi - tau_lo + 1);
+    const long long tau_new = pos / kTile;  // tile holding this step's key
+
+    auto issue_tile = [&](int i) {
+        const int st = i & 1;
+        const uint32_t base = smem_u32(smem) + st * kStage;
+        const uint32_t bar = st ? bar_full1 : bar_full0;
+        const int slot = (int)(((tau_lo + i) * kTile) % c.R);
+        mbar_arrive_expect_tx(bar, kStage);
+        tma_load_3d(base, job.tmap_k, bar, 0, slot, g);
+        tma_load_3d(base + kBox, job.tmap_k, bar, 64, slot, g);
+        tma_load_3d(base + 2 * kBox, job.tmap_v, bar, 0, slot, g);
+        tma_load_3d(base + 3 * kBox, job.tmap_v, bar, 64, slot, g);
+    };
 
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(bar_full0, 1);
+        mbar_init(bar_full1, 1);
+        mbar_init(bar_m, 1);
         fence_mbar_init();
         tmap_acquire(job.tmap_k);
         tmap_acquire(job.tmap_v);
-        mbar_arrive_expect_tx(bar, 4 * kBox);
-        tma_load_3d(smem_u32(smem + kOffK0), job.tmap_k, bar, 0, slot0, g);
-        tma_load_3d(smem_u32(smem + kOffK1), job.tmap_k, bar, 64, slot0, g);
-        tma_load_3d(smem_u32(smem + kOffV0), job.tmap_v, bar, 0, slot0, g);
-        tma_load_3d(smem_u32(smem + kOffV1), job.tmap_v, bar, 64, slot0, g);
+        issue_tile(0);
+        if (n_tiles > 1)
+            issue_tile(1);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&s_tmem), kTmemCols);
+        tmem_relinquish();
     }
 
-    // ---- rotate the 4 query heads of group g (fp32, then scaled to log2 units)
+    // ---- Q' (4 rotated heads, bf16) and zero padding rows 4..15 of Q' and P^T
+    for (int e = tid; e < 12 * 16; e += kThreads) {  // 12 rows x 16 chunks of zeros, both tiles
+        const int row = 4 + e / 16, ch = e % 16;
+        const uint32_t off = (uint32_t)((ch >> 3) * 2048) + sw128_offset(row, ch & 7);
+        *reinterpret_cast<uint4*>(sQ + off) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sP + off) = make_uint4(0, 0, 0, 0);
+    }
     {
-        const int hh = warp;  // one warp per query head
+        const int hh = warp;  // one warp per query head, lane owns pairs (2l, 2l+1)
         const __nv_bfloat16* q = job.q + (long long)(g * kG + hh) * kD;
         const float2* cs = c.rope + pos * (kD / 2);
         const uint32_t a = *reinterpret_cast<const uint32_t*>(q + 2 * lane);
@@ -118,13 +165,11 @@ __global__ void __launch_bounds__(kThreads)
         float y1, y2, y3, y4;
         rope_pair(bf16lo(a), bf16lo(b), cs[2 * lane], y1, y2);
         rope_pair(bf16hi(a), bf16hi(b), cs[2 * lane + 1], y3, y4);
-        sq[hh * kD + 2 * lane] = __fmul_rn(y1, c.scale_log2);
-        sq[hh * kD + 2 * lane + 1] = __fmul_rn(y3, c.scale_log2);
-        sq[hh * kD + 64 + 2 * lane] = __fmul_rn(y2, c.scale_log2);
-        sq[hh * kD + 64 + 2 * lane + 1] = __fmul_rn(y4, c.scale_log2);
+        *reinterpret_cast<uint32_t*>(sQ + sw16(hh, 2 * lane)) = pack_bf16(y1, y3);
+        *reinterpret_cast<uint32_t*>(sQ + sw16(hh, 64 + 2 * lane)) = pack_bf16(y2, y4);
     }
-    // ---- the new key (rotated) and value of this step, if this split holds pos
-    if (newest && warp == 0) {
+    const bool has_new = tau_new >= tau_lo && tau_new <= tau_hi;
+    if (has_new && warp == 0) {
         const __nv_bfloat16* k = job.k + (long long)g * kD;
         const __nv_bfloat16* v = job.v + (long long)g * kD;
         const float2* cs = c.rope + pos * (kD / 2);
@@ -138,166 +183,206 @@ __global__ void __launch_bounds__(kThreads)
         reinterpret_cast<uint32_t*>(snew + kD)[lane] = *reinterpret_cast<const uint32_t*>(v + 2 * lane);
         reinterpret_cast<uint32_t*>(snew + kD)[32 + lane] = *reinterpret_cast<const uint32_t*>(v + 64 + 2 * lane);
     }
+    fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
-    const bool loaded = mbar_wait(bar, 0);
-    if (newest && tid < 16) {
-        // chunk tid of the 256-byte row: dims [8*tid, 8*tid+8)
-        const int rr = (int)(pos - key0);
-        const int half = tid >> 3, ch = tid & 7;
-        const uint4 kw = reinterpret_cast<const uint4*>(snew)[tid];
-        const uint4 vw = reinterpret_cast<const uint4*>(snew + kD)[tid];
-        *reinterpret_cast<uint4*>(smem + (half ? kOffK1 : kOffK0) + sw128_offset(rr, ch)) = kw;
-        *reinterpret_cast<uint4*>(smem + (half ? kOffV1 : kOffV0) + sw128_offset(rr, ch)) = vw;
-        const long long gofs = ((long long)g * c.R + pos % c.R) * kD + 8 * tid;
-        *reinterpret_cast<uint4*>(job.k_ring + gofs) = kw;
-        *reinterpret_cast<uint4*>(job.v_ring + gofs) = vw;
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+    // running state: thread tid owns dimension d = tid of the 4 heads
+    float m[kG], l[kG], o[kG];
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+        o[h] = 0.f;
     }
-    if (__syncthreads_or(!loaded)) {
-        if (tid == 0)
+    int fail = 0, aborted = 0;
+    uint32_t ph_m = 0;
+    int issued = n_tiles < 2 ? n_tiles : 2;  // tiles whose loads thread 0 has issued
+    int consumed = 0;                       // tiles whose loads have landed
+
+    for (int i = 0; i < n_tiles; ++i) {
+        const long long tau = tau_lo + i;
+        const int st = i & 1;
+        uint8_t* sK = smem + st * kStage;
+        uint8_t* sV = sK + 2 * kBox;
+        if (!mbar_wait(st ? bar_full1 : bar_full0, (uint32_t)((i >> 1) & 1)))
+            fail = 1;
+        else
+            consumed = i + 1;
+        if (!fail && has_new && tau == tau_new && tid < 16) {
+            // chunk tid of the new 256-byte row: dims [8*tid, 8*tid+8)
+            const int rr = (int)(pos - tau * kTile);
+            const int half = tid >> 3, ch = tid & 7;
+            const uint4 kw = reinterpret_cast<const uint4*>(snew)[tid];
+            const uint4 vw = reinterpret_cast<const uint4*>(snew + kD)[tid];
+            *reinterpret_cast<uint4*>(sK + half * kBox + sw128_offset(rr, ch)) = kw;
+            *reinterpret_cast<uint4*>(sV + half * kBox + sw128_offset(rr, ch)) = vw;
+            const long long gofs = ((long long)g * c.R + pos % c.R) * kD + 8 * tid;
+            *reinterpret_cast<uint4*>(job.k_ring + gofs) = kw;
+            *reinterpret_cast<uint4*>(job.v_ring + gofs) = vw;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(fail)) {
+            aborted = 1;
+            break;
+        }
+        tc_fence_after();
+
+        // ---- S^T = K Q'^T
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t ad = smem_desc_sw128(smem_u32(sK) + (kk >> 2) * kBox + 32 * (kk & 3), 16, 1024);
+                const uint64_t bd = smem_desc_sw128(smem_u32(sQ) + (kk >> 2) * 2048 + 32 * (kk & 3), 16, 1024);
+                mma_bf16_ss(tmem + 0, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar_m);
+        }
+        if (!mbar_wait(bar_m, ph_m))
+            fail = 1;
+        ph_m ^= 1;
+        tc_fence_after();
+
+        // ---- tile softmax: thread tid owns key 128*tau + tid
+        uint32_t sv[32];
+        tmem_ld_32x32b_x32(tmem + lane_base, sv);
+        tmem_ld_wait();
+        const long long kp = tau * kTile + tid;
+        const bool valid = kp >= lo && kp <= pos;
+        float sc[kG];
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+            sc[h] = valid ? __fmul_rn(__uint_as_float(sv[h]), c.scale_log2) : -INFINITY;
+            const float wm = warp_max(sc[h]);
+            if (lane == 0)
+                sred[warp * kG + h] = wm;
+        }
+        __syncthreads();
+        float mt[kG], pv[kG];
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+            mt[h] = fmaxf(fmaxf(sred[h], sred[kG + h]), fmaxf(sred[2 * kG + h], sred[3 * kG + h]));
+            pv[h] = valid ? ex2(__fsub_rn(sc[h], mt[h])) : 0.f;
+            const float ws = warp_sum(pv[h]);
+            if (lane == 0)
+                sred[16 + warp * kG + h] = ws;
+        }
+#pragma unroll
+        for (int h = 0; h < kG; ++h)
+            *reinterpret_cast<__nv_bfloat16*>(sP + sw16(h, tid)) = __float2bfloat16_rn(pv[h]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        float lt[kG];
+#pragma unroll
+        for (int h = 0; h < kG; ++h)
+            lt[h] = __fadd_rn(__fadd_rn(sred[16 + h], sred[16 + kG + h]),
+                              __fadd_rn(sred[16 + 2 * kG + h], sred[16 + 3 * kG + h]));
+
+        // ---- O^T = V^T P^T
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t ad = smem_desc_sw128(smem_u32(sV) + 2048 * kk, kBox, 1024);
+                const uint64_t bd = smem_desc_sw128(smem_u32(sP) + (kk >> 2) * 2048 + 32 * (kk & 3), 16, 1024);
+                mma_bf16_ss(tmem + 16, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar_m);
+        }
+        if (!mbar_wait(bar_m, ph_m))
+            fail = 1;
+        ph_m ^= 1;
+        tc_fence_after();
+        if (tid == 0 && !fail && i + 2 < n_tiles) {  // this stage is free: fetch tile i + 2
+            issue_tile(i + 2);
+            issued = i + 3;
+        }
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(tmem + lane_base, ov);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < kG; ++h)
+            fold1(m[h], l[h], o[h], mt[h], lt[h], __uint_as_float(ov[16 + h]));
+        tc_fence_before();
+        if (__syncthreads_or(fail)) {
+            aborted = 1;
+            break;
+        }
+        tc_fence_after();
+    }
+
+    if (aborted) {
+        if (tid == 0) {
+            // A bounded wait gave up: record it, let copies still in flight land, release TMEM.
             atomicExch(job.err, kErrTimeout);
-    }
-
-    // ---- scores: thread tid owns key key0 + tid
-    const long long kp = key0 + tid;
-    const bool valid = kp >= lo && kp <= pos && loaded;
-    float s[kG] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int cidx = 0; cidx < 16; ++cidx) {
-        const uint8_t* kt = smem + ((cidx >> 3) ? kOffK1 : kOffK0);
-        const uint4 kw = *reinterpret_cast<const uint4*>(kt + sw128_offset(tid, cidx & 7));
-        const float kf[8] = {bf16lo(kw.x), bf16hi(kw.x), bf16lo(kw.y), bf16hi(kw.y),
-                             bf16lo(kw.z), bf16hi(kw.z), bf16lo(kw.w), bf16hi(kw.w)};
-#pragma unroll
-        for (int hh = 0; hh < kG; ++hh) {
-            const float4 qa = reinterpret_cast<const float4*>(sq + hh * kD + 8 * cidx)[0];
-            const float4 qb = reinterpret_cast<const float4*>(sq + hh * kD + 8 * cidx)[1];
-            float acc = s[hh];
-            acc = __fmaf_rn(qa.x, kf[0], acc);
-            acc = __fmaf_rn(qa.y, kf[1], acc);
-            acc = __fmaf_rn(qa.z, kf[2], acc);
-            acc = __fmaf_rn(qa.w, kf[3], acc);
-            acc = __fmaf_rn(qb.x, kf[4], acc);
-            acc = __fmaf_rn(qb.y, kf[5], acc);
-            acc = __fmaf_rn(qb.z, kf[6], acc);
-            acc = __fmaf_rn(qb.w, kf[7], acc);
-            s[hh] = acc;
+            for (int k = consumed; k < issued; ++k)
+                mbar_wait((k & 1) ? bar_full1 : bar_full0, (uint32_t)((k >> 1) & 1));
         }
-    }
+    } else {
+        // ---- this split's partial; the last CTA of (stream, g) folds all splits in order
 #pragma unroll
-    for (int hh = 0; hh < kG; ++hh)
-        if (!valid)
-            s[hh] = -INFINITY;
-
-    // ---- split-local softmax per head
-#pragma unroll
-    for (int hh = 0; hh < kG; ++hh) {
-        const float wm = warp_max(s[hh]);
-        if (lane == 0)
-            swarp[warp * kG + hh] = wm;
-    }
-    __syncthreads();
-    float mh[kG], lh[kG];
-#pragma unroll
-    for (int hh = 0; hh < kG; ++hh) {
-        float m = swarp[hh];
-        for (int w = 1; w < 4; ++w)
-            m = fmaxf(m, swarp[w * kG + hh]);
-        mh[hh] = m;
-        const float pv = valid ? ex2(__fsub_rn(s[hh], m)) : 0.f;
-        sp[hh * kD + tid] = pv;
-        const float ws = warp_sum(pv);
-        if (lane == 0)
-            swarp[16 + warp * kG + hh] = ws;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int hh = 0; hh < kG; ++hh) {
-        float l = swarp[16 + hh];
-        for (int w = 1; w < 4; ++w)
-            l = __fadd_rn(l, swarp[16 + w * kG + hh]);
-        lh[hh] = l;
-    }
-
-    // ---- P.V: thread -> dims (2dp, 2dp+1), keys [64kh, 64kh+64)
-    const int dp = tid & 63, kh = tid >> 6;
-    const int d = 2 * dp;
-    const uint8_t* vt = smem + ((d >> 6) ? kOffV1 : kOffV0);
-    const int ch = (d & 63) >> 3;
-    const int within = (d & 7) * 2;
-    float acc[kG][2];
-#pragma unroll
-    for (int hh = 0; hh < kG; ++hh)
-        acc[hh][0] = acc[hh][1] = 0.f;
-#pragma unroll 8
-    for (int kk = 0; kk < 64; ++kk) {
-        const int key = 64 * kh + kk;
-        const uint32_t vw = *reinterpret_cast<const uint32_t*>(vt + sw128_offset(key, ch) + within);
-        const float v0 = bf16lo(vw), v1 = bf16hi(vw);
-#pragma unroll
-        for (int hh = 0; hh < kG; ++hh) {
-            const float pp = sp[hh * kD + key];
-            acc[hh][0] = __fmaf_rn(pp, v0, acc[hh][0]);
-            acc[hh][1] = __fmaf_rn(pp, v1, acc[hh][1]);
+        for (int h = 0; h < kG; ++h)
+            job.part_o[((long long)(g * kG + h) * c.S + sl) * kD + tid] = o[h];
+        if (tid < kG)
+            *reinterpret_cast<float2*>(job.part_ml + ((long long)(g * kG + tid) * c.S + sl) * 2) =
+                make_float2(m[tid], l[tid]);
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned prev = atomicAdd(job.counters + g, 1u);
+            s_last = prev == (unsigned)(job.n_splits - 1);
         }
-    }
-    if (kh == 1) {
-#pragma unroll
-        for (int hh = 0; hh < kG; ++hh) {
-            sred[dp * 8 + 2 * hh] = acc[hh][0];
-            sred[dp * 8 + 2 * hh + 1] = acc[hh][1];
-        }
-    }
-    __syncthreads();
-    if (kh == 0) {
-#pragma unroll
-        for (int hh = 0; hh < kG; ++hh) {
-            const float o0 = __fadd_rn(acc[hh][0], sred[dp * 8 + 2 * hh]);
-            const float o1 = __fadd_rn(acc[hh][1], sred[dp * 8 + 2 * hh + 1]);
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            const int hh = warp;
             const int hq = g * kG + hh;
-            *reinterpret_cast<float2*>(job.part_o + ((long long)hq * c.S + sl) * kD + d) = make_float2(o0, o1);
+            const int d4 = lane * 4;
+            float mm = -INFINITY, ll = 0.f;
+            float oo[4] = {0.f, 0.f, 0.f, 0.f};
+            const float* pml = job.part_ml + (long long)hq * c.S * 2;
+            const float* po = job.part_o + (long long)hq * c.S * kD + d4;
+            for (int s0 = 0; s0 < job.n_splits; s0 += 8) {
+                float2 ml[8];
+                float4 ov4[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (s0 + u < job.n_splits) {
+                        ml[u] = __ldcg(reinterpret_cast<const float2*>(pml + (s0 + u) * 2));
+                        ov4[u] = __ldcg(reinterpret_cast<const float4*>(po + (long long)(s0 + u) * kD));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (s0 + u < job.n_splits) {
+                        float m0 = mm, l0 = ll;
+                        fold1(m0, l0, oo[0], ml[u].x, ml[u].y, ov4[u].x);
+                        float m1 = mm, l1 = ll;
+                        fold1(m1, l1, oo[1], ml[u].x, ml[u].y, ov4[u].y);
+                        float m2 = mm, l2 = ll;
+                        fold1(m2, l2, oo[2], ml[u].x, ml[u].y, ov4[u].z);
+                        fold1(mm, ll, oo[3], ml[u].x, ml[u].y, ov4[u].w);
+                    }
+                }
+            }
+            const uint32_t w0 = pack_bf16(__fdiv_rn(oo[0], ll), __fdiv_rn(oo[1], ll));
+            const uint32_t w1 = pack_bf16(__fdiv_rn(oo[2], ll), __fdiv_rn(oo[3], ll));
+            *reinterpret_cast<uint2*>(job.out + (long long)hq * kD + d4) = make_uint2(w0, w1);
+            if (tid == 0)
+                job.counters[g] = 0u;
         }
     }
-    if (tid < kG) {
-        const int hq = g * kG + tid;
-        *reinterpret_cast<float2*>(job.part_ml + ((long long)hq * c.S + sl) * 2) = make_float2(mh[tid], lh[tid]);
-    }
-    __threadfence();
+    tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
-        const unsigned prev = atomicAdd(job.counters + g, 1u);
-        s_last = (prev == (unsigned)(job.n_splits - 1));
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
     }
-    __syncthreads();
-    if (!s_last)
-        return;
-    __threadfence();
-
-    // ---- last CTA of (stream, g): fold the splits in ascending order
-    {
-        const int hh = warp;
-        const int hq = g * kG + hh;
-        const int d4 = lane * 4;
-        float m = -INFINITY, l = 0.f;
-        float o[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int sj = 0; sj < job.n_splits; ++sj) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(job.part_ml + ((long long)hq * c.S + sj) * 2));
-            const float4 oj = __ldcg(reinterpret_cast<const float4*>(job.part_o + ((long long)hq * c.S + sj) * kD + d4));
-            const float mn = fmaxf(m, ml.x);
-            const float a = ex2(__fsub_rn(m, mn));
-            const float b = ex2(__fsub_rn(ml.x, mn));
-            l = __fmaf_rn(l, a, __fmul_rn(ml.y, b));
-            o[0] = __fmaf_rn(o[0], a, __fmul_rn(oj.x, b));
-            o[1] = __fmaf_rn(o[1], a, __fmul_rn(oj.y, b));
-            o[2] = __fmaf_rn(o[2], a, __fmul_rn(oj.z, b));
-            o[3] = __fmaf_rn(o[3], a, __fmul_rn(oj.w, b));
-            m = mn;
-        }
-        const uint32_t w0 = pack_bf16(__fdiv_rn(o[0], l), __fdiv_rn(o[1], l));
-        const uint32_t w1 = pack_bf16(__fdiv_rn(o[2], l), __fdiv_rn(o[3], l));
-        *reinterpret_cast<uint2*>(job.out + (long long)hq * kD + d4) = make_uint2(w0, w1);
-    }
-    if (tid == 0)
-        job.counters[g] = 0u;
 }
 
 template <int J>

@@ -1,26 +1,40 @@
-// enc_attn.cu -- kernel (b): windowed-causal chunk attention against the encoder ring.
+// enc_attn.cu -- kernel (b) with the encoder half of kernel (a) fused in: windowed-causal
+// chunk attention against the encoder ring, for one batch of new frames per context.
 //
 // Streaming plan ("Voxtral Realtime -- incremental streaming implementation plan"):
-// SHIPPED/Mechanism -- mha_cached reads cache rows [0, n_kv_total) under a windowed-causal
-// mask; "Unbounded length" -- the mask uses absolute positions (slot 0 holds frame
-// abs_base); "Risk / notes" -- the chunk attention is a multi-query prefill against <= 750
-// cached keys. Frame i attends to [i-749, i] ("RECOMMENDED implementation").
+// SHIPPED/Mechanism -- mha_cached writes the chunk's K/V at cache rows
+// [n_kv_before, n_kv_total) and reads [0, n_kv_total) under a windowed-causal mask;
+// "Unbounded length" -- the mask uses absolute positions (slot 0 holds frame abs_base);
+// "Chunk alignment" -- RoPE at absolute positions; "Risk / notes" -- the chunk attention is a
+// multi-query prefill against <= 750 cached keys. Frame i attends to [i-749, i]
+// ("RECOMMENDED implementation").
 //
-// Work item: one CTA per (context, head, 128-query tile of the batch). Keys are visited in
-// tiles of 128 ABSOLUTE positions [128t, 128t+128), loaded by TMA from ring slots
-// 128t - abs_base (rows outside the ring read as zero). Per tile:
-//   S  = Q' K'^T       tcgen05.mma, M=128 N=128 K=64, A/B K-major bf16 in smem, D in TMEM
-//   softmax            each thread owns one query row (TMEM lane); tile-local max m_t,
-//                      p = 2^(s*log2e/sqrt(D) - m_t), l_t = sum p; P -> smem as bf16
-//   O_t = P V          tcgen05.mma, M=128 N=64 K=128, A = P (K-major), B = V (MN-major)
-//   fold               (m, l, o) <- merge((m, l, o), (m_t, l_t, O_t)) in registers
-// A tile with no visible key for a row is skipped for that row (an exact no-op). Because
-// tiles are fixed by absolute position and are folded in ascending order, a row's result
-// depends only on its own window, never on how the stream was cut into feeds or when the
-// ring was compacted.
+// Keys are visited in tiles of 128 ABSOLUTE positions [128t, 128t+128), loaded by TMA from
+// ring slots 128t - abs_base (rows outside the ring read as zero). Rows of a tile that
+// belong to this batch (positions >= pos0) are not in the ring yet: every CTA that loads
+// such a tile rotates those keys itself from the input and patches them into shared
+// memory; the CTA whose query tile holds a new row also stores it (K rotated, V) to ring
+// slot n_kv_before + row. Per tile:
+//   S   = Q' K'^T      tcgen05.mma M=128 N=128 K=64, A/B K-major bf16 in smem, D in TMEM
+//   softmax            tile-local max m_t, p = 2^(s*log2e/sqrt(D) - m_t), l_t = sum p;
+//                      P -> smem as bf16
+//   O_t = P V          tcgen05.mma M=128 N=64 K=128, A = P (K-major), B = V (MN-major)
+//   fold               (m, l, o) <- fold((m, l, o), (m_t, l_t, O_t)), ascending t
+// A tile where a row sees no key is skipped for that row (exact no-op).
 //
-// The query is rotated here, in the prologue (fp32 math, rounded to bf16 as the MMA
-// operand); keys arrive already rotated in the ring (kernel a).
+// Threads: 512 per CTA. Query row r (TMEM lane r) is shared by the four threads
+// (r, q), q = 0..3, one in each group of four warps: thread (r, q) owns score columns
+// [32q, 32q+32), output dims [16q, 16q+16) and RoPE pairs [8q, 8q+8). Row max and row sum
+// are combined from the four quarters through shared memory in fixed order q = 0..3.
+//
+// Two launch shapes, chosen by the host from the amount of work, give the same bits:
+//   loop mode  -- one CTA per (context, head, 128-query tile) folds its tiles in registers;
+//   split mode -- one CTA per (context, head, key tile) of a single query tile writes its
+//                 tile's (m_t, l_t, O_t) to scratch, and the last CTA of the (context,
+//                 head) folds the tiles in ascending order with the same fold function.
+// Tiles are fixed by absolute position and folded in ascending order, so a row's result
+// depends only on its own window -- never on how the stream was cut into feeds, on when
+// the ring was compacted, or on the launch shape.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "vst_internal.h"
@@ -29,14 +43,16 @@ namespace vst {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 512;
 constexpr int kD = 64;
+constexpr int kDq = kD / 4;                   // output dims per thread
 constexpr uint32_t kTileBytes = 128u * 128u;  // 128 rows x 128 B
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;
 constexpr uint32_t kOffV = kOffK + kTileBytes;
 constexpr uint32_t kOffP = kOffV + kTileBytes;       // two 64-key blocks
-constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
+constexpr uint32_t kOffRed = kOffP + 2 * kTileBytes; // float [2][4][128]: row max / row sum quarters
+constexpr uint32_t kOffBar = kOffRed + 2 * 4 * 128 * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmS = 0;    // S tile: columns [0, 128)
@@ -44,6 +60,112 @@ constexpr uint32_t kTmO = 128;  // O tile: columns [128, 192)
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64, false, true);
+
+// The one fold used by both launch shapes (and so the reason they agree bit for bit):
+// merge the tile-local softmax state (mt, lt, ot) into the running state (m, l, o).
+__device__ __forceinline__ void fold_tile(float& m, float& l, float* o, float mt, float lt, const float* ot)
+{
+    const float mn = fmaxf(m, mt);
+    const float a = ex2(__fsub_rn(m, mn));
+    const float b = ex2(__fsub_rn(mt, mn));
+    l = __fmaf_rn(l, a, __fmul_rn(lt, b));
+#pragma unroll
+    for (int d = 0; d < kDq; ++d)
+        o[d] = __fmaf_rn(o[d], a, __fmul_rn(ot[d], b));
+    m = mn;
+}
+
+// Rotate pairs [8q, 8q+8) of a 64-value head row (NEOX: element i pairs with i + 32) at the
+// angle table row cs, and write them as chunks q and 4 + q of a swizzled 128-byte row.
+__device__ __forceinline__ void rotate_quarter(const __nv_bfloat16* src, const float2* cs, uint8_t* tile, int row,
+                                               int q)
+{
+    const uint4 a = *reinterpret_cast<const uint4*>(src + 8 * q);
+    const uint4 b = *reinterpret_cast<const uint4*>(src + 32 + 8 * q);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+    uint32_t ya[4], yb[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float y1a, y2a, y1b, y2b;
+        rope_pair(bf16lo(aw[w]), bf16lo(bw[w]), cs[8 * q + 2 * w], y1a, y2a);
+        rope_pair(bf16hi(aw[w]), bf16hi(bw[w]), cs[8 * q + 2 * w + 1], y1b, y2b);
+        ya[w] = pack_bf16(y1a, y1b);
+        yb[w] = pack_bf16(y2a, y2b);
+    }
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, q)) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, 4 + q)) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+}
+
+struct Cta {
+    uint8_t *sQ, *sK, *sV, *sP;
+    float *red_m, *red_l;  // [4][128]
+    uint32_t bar_k, bar_v, bar_m;
+    uint32_t tmem, lane_base;
+    int tid, warp, r, q;
+};
+
+// New rows of key tile t (positions >= pos0) are not in the ring yet: thread (r, q) replaces
+// its quarter of row r of the smem tile with K' = RoPE(k) (is_k) or V from the input; the
+// CTA whose query tile owns the row also stores that quarter to ring slot slot0 + row.
+__device__ __forceinline__ void patch_new_row(const Cta& s, const EncAttnCommon& c, const EncAttnJob& job, int h,
+                                              long long t, int own_lo, int own_hi, bool is_k)
+{
+    const long long p = t * 128 + s.r;
+    const long long i = p - job.pos0;  // batch row
+    if (i < 0 || i >= c.n_rows)
+        return;
+    uint8_t* tile = is_k ? s.sK : s.sV;
+    int ch0, ch1;
+    if (is_k) {
+        rotate_quarter(job.k + (i * c.H + h) * kD, c.rope + p * (kD / 2), tile, s.r, s.q);
+        ch0 = s.q;
+        ch1 = 4 + s.q;
+    } else {
+        const __nv_bfloat16* vrow = job.v + (i * c.H + h) * kD;
+        ch0 = 2 * s.q;
+        ch1 = 2 * s.q + 1;
+        *reinterpret_cast<uint4*>(tile + sw128_offset(s.r, ch0)) = *reinterpret_cast<const uint4*>(vrow + 8 * ch0);
+        *reinterpret_cast<uint4*>(tile + sw128_offset(s.r, ch1)) = *reinterpret_cast<const uint4*>(vrow + 8 * ch1);
+    }
+    if (i >= own_lo && i < own_hi) {
+        __nv_bfloat16* ring = (is_k ? job.k_ring : job.v_ring) + ((long long)h * c.R + (job.slot0 + i)) * kD;
+        *reinterpret_cast<uint4*>(ring + 8 * ch0) = *reinterpret_cast<const uint4*>(tile + sw128_offset(s.r, ch0));
+        *reinterpret_cast<uint4*>(ring + 8 * ch1) = *reinterpret_cast<const uint4*>(tile + sw128_offset(s.r, ch1));
+    }
+}
+
+__device__ __forceinline__ void issue_s_mma(const Cta& s)
+{
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ad = smem_desc_sw128(smem_u32(s.sQ) + 32 * kk, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(smem_u32(s.sK) + 32 * kk, 16, 1024);
+        mma_bf16_ss(s.tmem + kTmS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+    }
+    mma_commit(s.bar_m);
+}
+
+__device__ __forceinline__ void issue_o_mma(const Cta& s)
+{
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t ad = smem_desc_sw128(smem_u32(s.sP) + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024);
+        const uint64_t bd = smem_desc_sw128(smem_u32(s.sV) + 2048 * kk, kTileBytes, 1024);
+        mma_bf16_ss(s.tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
+    }
+    mma_commit(s.bar_m);
+}
+
+__device__ __forceinline__ void store_out_quarter(__nv_bfloat16* orow, const float* o, float l, int q)
+{
+    uint32_t w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        w[e] = pack_bf16(__fdiv_rn(o[2 * e], l), __fdiv_rn(o[2 * e + 1], l));
+    *reinterpret_cast<uint4*>(orow + kDq * q) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(orow + kDq * q + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+}
 
 }  // namespace
 
@@ -53,257 +175,273 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t* sQ = smem + kOffQ;
-    uint8_t* sK = smem + kOffK;
-    uint8_t* sV = smem + kOffV;
-    uint8_t* sP = smem + kOffP;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    const uint32_t bar_k = smem_u32(&bars[0]);
-    const uint32_t bar_v = smem_u32(&bars[1]);
-    const uint32_t bar_m = smem_u32(&bars[2]);
-
+    __shared__ int s_last;
     const EncAttnCommon& c = p.c;
     const EncAttnJob& job = p.jobs[blockIdx.z];
     const int h = blockIdx.y;
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int row0 = blockIdx.x * 128;
+    const bool split = c.split != 0;
+    const int qt = split ? 0 : blockIdx.x;
+    const int row0 = qt * 128;
     const int nrows = min(128, c.n_rows - row0);
     const long long p_first = job.pos0 + row0;
     const long long p_last = p_first + nrows - 1;
-    const long long key_lo = max(0LL, p_first - c.W + 1);
-    const long long t_begin = key_lo / 128;
-    const long long t_end = p_last / 128;
+    const long long t_lo = max(0LL, p_first - c.W + 1) / 128;
+    const long long t_hi = p_last / 128;
+    const long long t_begin = split ? t_lo + blockIdx.x : t_lo;
+    const long long t_end = split ? t_begin : t_hi;
+    if (t_begin > t_hi)
+        return;  // split mode: this job has fewer tiles than the grid
 
-    if (tid == 0) {
-        mbar_init(bar_k, 1);
-        mbar_init(bar_v, 1);
-        mbar_init(bar_m, 1);
+    Cta s;
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    s.sQ = smem + kOffQ;
+    s.sK = smem + kOffK;
+    s.sV = smem + kOffV;
+    s.sP = smem + kOffP;
+    s.red_m = reinterpret_cast<float*>(smem + kOffRed);
+    s.red_l = s.red_m + 4 * 128;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    s.bar_k = smem_u32(&bars[0]);
+    s.bar_v = smem_u32(&bars[1]);
+    s.bar_m = smem_u32(&bars[2]);
+    s.tid = threadIdx.x;
+    s.warp = s.tid >> 5;
+    s.r = 32 * (s.warp & 3) + (s.tid & 31);  // TMEM lane = query row of this thread
+    s.q = s.warp >> 2;                       // quarter of the row
+
+    if (s.tid == 0) {
+        mbar_init(s.bar_k, 1);
+        mbar_init(s.bar_v, 1);
+        mbar_init(s.bar_m, 1);
         fence_mbar_init();
         tmap_acquire(job.tmap_k);
         tmap_acquire(job.tmap_v);
+        const int slot = (int)(t_begin * 128 - job.abs_base);
+        mbar_arrive_expect_tx(s.bar_k, kTileBytes);
+        tma_load_3d(smem_u32(s.sK), job.tmap_k, s.bar_k, 0, slot, h);
+        mbar_arrive_expect_tx(s.bar_v, kTileBytes);
+        tma_load_3d(smem_u32(s.sV), job.tmap_v, s.bar_v, 0, slot, h);
     }
-    if (warp == 0) {
+    if (s.warp == 0) {
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
         tmem_relinquish();
     }
 
-    // ---- rotate this thread's query row into sQ (bf16, K-major, 128-B swizzle)
-    const int r = tid;
+    // ---- this thread's quarter of query row r, rotated, into sQ
+    const int r = s.r;
     const long long pq = p_first + r;
     if (r < nrows) {
-        const __nv_bfloat16* qrow = job.q + ((long long)(row0 + r) * c.H + h) * kD;
-        const float2* cs = c.rope + pq * (kD / 2);
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-            const uint4 a = *reinterpret_cast<const uint4*>(qrow + 8 * ch);
-            const uint4 b = *reinterpret_cast<const uint4*>(qrow + 32 + 8 * ch);
-            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-            uint32_t ya[4], yb[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                float y1a, y2a, y1b, y2b;
-                rope_pair(bf16lo(aw[w]), bf16lo(bw[w]), cs[8 * ch + 2 * w], y1a, y2a);
-                rope_pair(bf16hi(aw[w]), bf16hi(bw[w]), cs[8 * ch + 2 * w + 1], y1b, y2b);
-                ya[w] = pack_bf16(y1a, y1b);
-                yb[w] = pack_bf16(y2a, y2b);
-            }
-            *reinterpret_cast<uint4*>(sQ + sw128_offset(r, ch)) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-            *reinterpret_cast<uint4*>(sQ + sw128_offset(r, 4 + ch)) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
-        }
+        rotate_quarter(job.q + ((long long)(row0 + r) * c.H + h) * kD, c.rope + pq * (kD / 2), s.sQ, r, s.q);
     } else {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4*>(sQ + sw128_offset(r, ch)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(s.sQ + sw128_offset(r, s.q)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(s.sQ + sw128_offset(r, 4 + s.q)) = make_uint4(0, 0, 0, 0);
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = s_tmem;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    s.tmem = s_tmem;
+    s.lane_base = (uint32_t)((s.warp & 3) * 32) << 16;
 
-    bool pend_k = false, pend_v = false;
-    if (tid == 0) {
-        const int slot = (int)(t_begin * 128 - job.abs_base);
-        mbar_arrive_expect_tx(bar_k, kTileBytes);
-        tma_load_3d(smem_u32(sK), job.tmap_k, bar_k, 0, slot, h);
-        mbar_arrive_expect_tx(bar_v, kTileBytes);
-        tma_load_3d(smem_u32(sV), job.tmap_v, bar_v, 0, slot, h);
-        pend_k = pend_v = true;
-    }
-
-    float o[kD];
+    float o[kDq];
 #pragma unroll
-    for (int d = 0; d < kD; ++d)
+    for (int d = 0; d < kDq; ++d)
         o[d] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
     uint32_t ph_k = 0, ph_v = 0, ph_m = 0;
-    bool aborted = false;
+    bool pend_k = s.tid == 0, pend_v = s.tid == 0;
+    int fail = 0, aborted = 0;
 
     for (long long t = t_begin; t <= t_end; ++t) {
-        int fail = 0;
-        // ---- S = Q K^T
-        if (tid == 0) {
-            if (mbar_wait(bar_k, ph_k)) {
-                pend_k = false;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sQ) + 32 * kk, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(smem_u32(sK) + 32 * kk, 16, 1024);
-                    mma_bf16_ss(tmem + kTmS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(bar_m);
-            } else {
-                fail = 1;
-            }
-        }
-        ph_k ^= 1;
-        if (!fail && !mbar_wait(bar_m, ph_m))
+        const bool has_new = (t + 1) * 128 > job.pos0;
+        // ---- K of tile t in smem (new rows patched in), then S = Q K^T
+        if (!mbar_wait(s.bar_k, ph_k))
             fail = 1;
-        ph_m ^= 1;
-        tc_fence_after();
-        if (tid == 0 && !fail && t < t_end) {
-            const int slot = (int)((t + 1) * 128 - job.abs_base);
-            mbar_arrive_expect_tx(bar_k, kTileBytes);
-            tma_load_3d(smem_u32(sK), job.tmap_k, bar_k, 0, slot, h);
-            pend_k = true;
-        }
-
-        // ---- tile-local softmax of row r (scores in log2 units)
-        const long long kbase = t * 128;
-        const long long lo_c = (r < nrows) ? (pq - c.W + 1 - kbase) : 1000;
-        const long long hi_c = (r < nrows) ? (pq - kbase) : -1;
-        float mt = -INFINITY;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + kTmS + cc * 32, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int col = cc * 32 + j;
-                if (col >= lo_c && col <= hi_c)
-                    mt = fmaxf(mt, __fmul_rn(__uint_as_float(v[j]), c.scale_log2));
-            }
-        }
-        float lt = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + kTmS + cc * 32, v);
-            tmem_ld_wait();
-            float pv[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int col = cc * 32 + j;
-                const bool ok = col >= lo_c && col <= hi_c;
-                pv[j] = ok ? ex2(__fsub_rn(__fmul_rn(__uint_as_float(v[j]), c.scale_log2), mt)) : 0.f;
-                lt = __fadd_rn(lt, pv[j]);
-            }
-#pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
-                const uint4 w = make_uint4(pack_bf16(pv[8 * qd + 0], pv[8 * qd + 1]),
-                                           pack_bf16(pv[8 * qd + 2], pv[8 * qd + 3]),
-                                           pack_bf16(pv[8 * qd + 4], pv[8 * qd + 5]),
-                                           pack_bf16(pv[8 * qd + 6], pv[8 * qd + 7]));
-                *reinterpret_cast<uint4*>(sP + (cc >> 1) * kTileBytes + sw128_offset(r, (cc & 1) * 4 + qd)) = w;
-            }
-        }
+        ph_k ^= 1;
+        if (s.tid == 0)
+            pend_k = false;
+        if (!fail && has_new)
+            patch_new_row(s, c, job, h, t, row0, row0 + nrows, true);
         fence_proxy_async_smem();
         tc_fence_before();
         if (__syncthreads_or(fail)) {
-            aborted = true;
+            aborted = 1;
             break;
         }
         tc_fence_after();
-
-        // ---- O_t = P V
-        if (tid == 0) {
-            if (mbar_wait(bar_v, ph_v)) {
-                pend_v = false;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sP) + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(smem_u32(sV) + 2048 * kk, kTileBytes, 1024);
-                    mma_bf16_ss(tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(bar_m);
-            } else {
-                fail = 1;
-            }
-        }
-        ph_v ^= 1;
-        if (!fail && !mbar_wait(bar_m, ph_m))
+        if (s.tid == 0)
+            issue_s_mma(s);
+        if (!mbar_wait(s.bar_m, ph_m))
             fail = 1;
         ph_m ^= 1;
         tc_fence_after();
-        if (tid == 0 && !fail && t < t_end) {
-            const int slot = (int)((t + 1) * 128 - job.abs_base);
-            mbar_arrive_expect_tx(bar_v, kTileBytes);
-            tma_load_3d(smem_u32(sV), job.tmap_v, bar_v, 0, slot, h);
+        if (s.tid == 0 && !fail && t < t_end) {  // K buffer is free: fetch the next tile's K
+            mbar_arrive_expect_tx(s.bar_k, kTileBytes);
+            tma_load_3d(smem_u32(s.sK), job.tmap_k, s.bar_k, 0, (int)((t + 1) * 128 - job.abs_base), h);
+            pend_k = true;
+        }
+
+        // ---- tile-local softmax: this thread's 32 columns of row r
+        const long long kbase = t * 128;
+        int lo = 1, hi = 0;  // visible columns of row r in this tile; empty unless r is real
+        if (r < nrows) {
+            lo = (int)max(-1LL, min(128LL, pq - c.W + 1 - kbase));
+            hi = (int)max(-1LL, min(128LL, pq - kbase));
+        }
+        const int c0 = 32 * s.q;
+        const bool full = lo <= c0 && hi >= c0 + 31;
+        uint32_t sv[32];
+        tmem_ld_32x32b_x32(s.tmem + s.lane_base + kTmS + c0, sv);
+        tmem_ld_wait();
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (full || (c0 + j >= lo && c0 + j <= hi))
+                m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(sv[j]));
+        s.red_m[s.q * 128 + r] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        __syncthreads();
+        const float mraw = fmaxf(fmaxf(s.red_m[r], s.red_m[128 + r]), fmaxf(s.red_m[256 + r], s.red_m[384 + r]));
+        const float mt = __fmul_rn(mraw, c.scale_log2);  // -inf when the row sees nothing here
+        const float neg = -mt;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        float pv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const bool ok = full || (c0 + j >= lo && c0 + j <= hi);
+            pv[j] = ok ? ex2(__fmaf_rn(__uint_as_float(sv[j]), c.scale_log2, neg)) : 0.f;
+            l4[j & 3] = __fadd_rn(l4[j & 3], pv[j]);
+        }
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+            const uint4 w = make_uint4(pack_bf16(pv[8 * qd + 0], pv[8 * qd + 1]), pack_bf16(pv[8 * qd + 2], pv[8 * qd + 3]),
+                                       pack_bf16(pv[8 * qd + 4], pv[8 * qd + 5]), pack_bf16(pv[8 * qd + 6], pv[8 * qd + 7]));
+            *reinterpret_cast<uint4*>(s.sP + (s.q >> 1) * kTileBytes + sw128_offset(r, (s.q & 1) * 4 + qd)) = w;
+        }
+        s.red_l[s.q * 128 + r] = __fadd_rn(__fadd_rn(l4[0], l4[1]), __fadd_rn(l4[2], l4[3]));
+
+        // ---- V of tile t in smem (new rows patched in), then O_t = P V
+        if (!mbar_wait(s.bar_v, ph_v))
+            fail = 1;
+        ph_v ^= 1;
+        if (s.tid == 0)
+            pend_v = false;
+        if (!fail && has_new)
+            patch_new_row(s, c, job, h, t, row0, row0 + nrows, false);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (__syncthreads_or(fail)) {
+            aborted = 1;
+            break;
+        }
+        tc_fence_after();
+        if (s.tid == 0)
+            issue_o_mma(s);
+        const float lt = __fadd_rn(__fadd_rn(s.red_l[r], s.red_l[128 + r]), __fadd_rn(s.red_l[256 + r], s.red_l[384 + r]));
+        if (!mbar_wait(s.bar_m, ph_m))
+            fail = 1;
+        ph_m ^= 1;
+        tc_fence_after();
+        if (s.tid == 0 && !fail && t < t_end) {  // V buffer is free: fetch the next tile's V
+            mbar_arrive_expect_tx(s.bar_v, kTileBytes);
+            tma_load_3d(smem_u32(s.sV), job.tmap_v, s.bar_v, 0, (int)((t + 1) * 128 - job.abs_base), h);
             pend_v = true;
         }
 
-        // ---- fold the tile into the running state (skipped when the row saw no key)
-        uint32_t ov[64];
-        tmem_ld_32x32b_x32(tmem + lane_base + kTmO, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
-        tmem_ld_32x32b_x32(tmem + lane_base + kTmO + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
-        tmem_ld_wait();
-        if (mt != -INFINITY) {
-            const float mn = fmaxf(m_run, mt);
-            const float a = ex2(__fsub_rn(m_run, mn));
-            const float b = ex2(__fsub_rn(mt, mn));
-            l_run = __fmaf_rn(l_run, a, __fmul_rn(lt, b));
+        float ot[kDq];
+        {
+            uint32_t ov[16];
+            tmem_ld_32x32b_x16(s.tmem + s.lane_base + kTmO + kDq * s.q, ov);
+            tmem_ld_wait();
 #pragma unroll
-            for (int d = 0; d < kD; ++d)
-                o[d] = __fmaf_rn(o[d], a, __fmul_rn(__uint_as_float(ov[d]), b));
-            m_run = mn;
+            for (int j = 0; j < kDq; ++j)
+                ot[j] = __uint_as_float(ov[j]);
+        }
+        if (split) {
+            // tile partial of (row r, quarter q) -> scratch [h][tile][row]
+            const long long slot_t = (long long)h * c.split_tiles + (t - t_lo);
+            float* po = job.part_o + (slot_t * 128 + r) * kD + kDq * s.q;
+#pragma unroll
+            for (int d = 0; d < kDq; d += 4)
+                *reinterpret_cast<float4*>(po + d) = make_float4(ot[d], ot[d + 1], ot[d + 2], ot[d + 3]);
+            if (s.q == 0)
+                *reinterpret_cast<float2*>(job.part_ml + (slot_t * 128 + r) * 2) = make_float2(mt, lt);
+        } else if (mt != -INFINITY) {
+            fold_tile(m_run, l_run, o, mt, lt, ot);
         }
         tc_fence_before();
         if (__syncthreads_or(fail)) {
-            aborted = true;
+            aborted = 1;
             break;
         }
         tc_fence_after();
     }
 
-    if (!aborted) {
-        if (r < nrows) {
-            __nv_bfloat16* orow = job.out + ((long long)(row0 + r) * c.H + h) * kD;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    w[e] = pack_bf16(__fdiv_rn(o[8 * ch + 2 * e], l_run), __fdiv_rn(o[8 * ch + 2 * e + 1], l_run));
-                *reinterpret_cast<uint4*>(orow + 8 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
+    if (aborted) {
+        if (s.tid == 0) {
+            // A bounded wait gave up: record it, let copies still in flight land, then release
+            // TMEM and leave.
+            atomicExch(job.err, kErrTimeout);
+            if (pend_k)
+                mbar_wait(s.bar_k, ph_k);
+            if (pend_v)
+                mbar_wait(s.bar_v, ph_v);
         }
-    } else if (tid == 0) {
-        // A bounded wait gave up: record it, let copies still in flight land, then release
-        // TMEM and leave.
-        atomicExch(job.err, kErrTimeout);
-        if (pend_k)
-            mbar_wait(bar_k, ph_k);
-        if (pend_v)
-            mbar_wait(bar_v, ph_v);
+    } else if (!split) {
+        if (r < nrows)
+            store_out_quarter(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, s.q);
+    } else {
+        // split mode: the last CTA of (job, head) folds all tiles in ascending order
+        __threadfence();
+        __syncthreads();
+        if (s.tid == 0) {
+            const unsigned prev = atomicAdd(job.counters + h, 1u);
+            s_last = prev == (unsigned)(t_hi - t_lo);
+        }
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            if (r < nrows) {
+                const int nt = (int)(t_hi - t_lo + 1);
+                const long long base = (long long)h * c.split_tiles;
+                for (int u0 = 0; u0 < nt; u0 += 8) {
+                    float2 ml[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (u0 + u < nt)
+                            ml[u] = __ldcg(reinterpret_cast<const float2*>(job.part_ml + ((base + u0 + u) * 128 + r) * 2));
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (u0 + u < nt && ml[u].x != -INFINITY) {
+                            const float* po = job.part_o + ((base + u0 + u) * 128 + r) * kD + kDq * s.q;
+                            float ot[kDq];
+#pragma unroll
+                            for (int d = 0; d < kDq; d += 4) {
+                                const float4 x = __ldcg(reinterpret_cast<const float4*>(po + d));
+                                ot[d] = x.x;
+                                ot[d + 1] = x.y;
+                                ot[d + 2] = x.z;
+                                ot[d + 3] = x.w;
+                            }
+                            fold_tile(m_run, l_run, o, ml[u].x, ml[u].y, ot);
+                        }
+                    }
+                }
+                store_out_quarter(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, s.q);
+            }
+            if (s.tid == 0)
+                job.counters[h] = 0u;
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (s.warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(s.tmem, kTmemCols);
     }
 }
 
 template <int J>
-static cudaError_t launch_enc_attn_j(const KParams<EncAttnCommon, EncAttnJob, J>& p, int n_jobs,
+static cudaError_t launch_enc_attn_j(const KParams<EncAttnCommon, EncAttnJob, J>& p, int n_jobs, int grid_x,
                                      cudaStream_t s)
 {
     static int configured[64] = {0};
@@ -316,17 +454,17 @@ static cudaError_t launch_enc_attn_j(const KParams<EncAttnCommon, EncAttnJob, J>
             return e;
         configured[dev] = 1;
     }
-    const dim3 grid((unsigned)((p.c.n_rows + 127) / 128), (unsigned)p.c.H, (unsigned)n_jobs);
+    const dim3 grid((unsigned)grid_x, (unsigned)p.c.H, (unsigned)n_jobs);
     enc_attn_kernel<J><<<grid, kThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int n_jobs, cudaStream_t s)
+cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int n_jobs, int grid_x, cudaStream_t s)
 {
     if (n_jobs == 0 || c.n_rows == 0)
         return cudaSuccess;
     return with_params(c, jobs, n_jobs, [&](const auto& p) {
-        return launch_enc_attn_j<sizeof(p.jobs) / sizeof(p.jobs[0])>(p, n_jobs, s);
+        return launch_enc_attn_j<sizeof(p.jobs) / sizeof(p.jobs[0])>(p, n_jobs, grid_x, s);
     });
 }
 

@@ -12,6 +12,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -23,8 +24,9 @@ using namespace vst;
 struct vst_module {
     vst_config cfg;
     int device;
+    int n_sms;     // SMs of the device (launch-shape choice)
     float2* rope;  // device [max_position][D/2]
-    int splits;    // decoder: split slots per step (S)
+    int splits;    // scratch slots per head: decoder splits per step / encoder key tiles
 };
 
 struct vst_ctx {
@@ -55,6 +57,12 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 int dec_splits(const vst_config& c) { return (c.window - 1 + kDecSplit - 1) / kDecSplit + 1; }
 
+// Key tiles (128 absolute positions each) met by a query tile of up to 128 rows: the keys
+// span at most 127 + W positions, which cross at most ceil((127 + W) / 128) + 1 tiles.
+int enc_split_tiles(const vst_config& c) { return (c.window + 127 + 127) / kEncTileN + 1; }
+
+int scratch_slots(const vst_config& c) { return c.kind == VST_DEC ? dec_splits(c) : enc_split_tiles(c); }
+
 Layout layout_of(const vst_config& c)
 {
     Layout L{};
@@ -62,12 +70,13 @@ Layout layout_of(const vst_config& c)
     L.k_off = kCtxHeaderBytes;
     L.v_off = align256(L.k_off + ring);
     size_t end = align256(L.v_off + ring);
-    if (c.kind == VST_DEC) {
-        const size_t S = (size_t)dec_splits(c);
-        L.ml_off = end;
-        L.o_off = align256(L.ml_off + (size_t)c.n_heads * S * 2 * sizeof(float));
-        end = align256(L.o_off + (size_t)c.n_heads * S * c.head_dim * sizeof(float));
-    }
+    // partial softmax scratch: decoder one row per (head, split); encoder 128 rows per
+    // (head, key tile)
+    const size_t rows = c.kind == VST_DEC ? 1 : kEncTileM;
+    const size_t S = (size_t)scratch_slots(c);
+    L.ml_off = end;
+    L.o_off = align256(L.ml_off + (size_t)c.n_heads * S * rows * 2 * sizeof(float));
+    end = align256(L.o_off + (size_t)c.n_heads * S * rows * c.head_dim * sizeof(float));
     L.total = end;
     return L;
 }
@@ -94,7 +103,7 @@ vst_status check_config(const vst_config* c)
         if (c->ring_slots < c->window)
             return VST_E_INVAL;
         // kernel (c): head dim 128, 4 query heads per KV head, ring a multiple of the split.
-        if (c->head_dim != 128 || c->n_heads != 4 * c->n_kv_heads || c->ring_slots % kDecSplit != 0)
+        if (c->head_dim != 128 || c->n_heads != 4 * c->n_kv_heads || c->ring_slots % kDecTile != 0)
             return VST_E_UNSUPPORTED;
         return VST_OK;
     }
@@ -155,6 +164,56 @@ bool make_ring_map(CUtensorMap* map, void* base, const vst_config& c)
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// ---- launch accounting and optional per-kernel event timing
+std::atomic<long long> g_launches{0};
+std::atomic<int> g_prof_on{0};
+std::mutex g_prof_mu;
+struct ProfRec {
+    int kid;
+    cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pooled_event()
+{
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Launch one kernel through f(); count it, and time it when timing is on.
+template <class F>
+cudaError_t tracked(int kid, cudaStream_t s, F&& f)
+{
+    if (!g_prof_on.load(std::memory_order_relaxed)) {
+        const cudaError_t e = f();
+        if (e == cudaSuccess)
+            g_launches.fetch_add(1, std::memory_order_relaxed);
+        return e;
+    }
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    ProfRec r{kid, pooled_event(), pooled_event()};
+    // Under stream capture an event record becomes a graph node only with the external
+    // flag; then every replay of the graph re-records it.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &cap);
+    const unsigned flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u;
+    cudaEventRecordWithFlags(r.a, s, flags);
+    const cudaError_t e = f();
+    cudaEventRecordWithFlags(r.b, s, flags);
+    if (e == cudaSuccess) {
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        g_prof_recs.push_back(r);
+    }
+    return e;
+}
+
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // Zero the error word, counters and both rings (not the tensor maps).
@@ -164,7 +223,7 @@ cudaError_t clear_ctx(vst_ctx* c, cudaStream_t s)
     if (e != cudaSuccess)
         return e;
     const Layout L = layout_of(c->m->cfg);
-    return cudaMemsetAsync(c->mem + L.k_off, 0, L.ml_off ? (L.ml_off - L.k_off) : (L.total - L.k_off), s);
+    return cudaMemsetAsync(c->mem + L.k_off, 0, L.ml_off - L.k_off, s);
 }
 
 vst_status fail_all(vst_ctx* const* ctxs, int n)
@@ -203,6 +262,46 @@ vst_status check_ctxs(vst_ctx* const* ctxs, int n, int kind)
 extern "C" {
 
 const char* vst_version(void) { return "0.1.0"; }
+
+vst_status vst_prof_enable(int32_t on)
+{
+    g_prof_on.store(on ? 1 : 0);
+    return VST_OK;
+}
+
+vst_status vst_prof_read(vst_prof_stat* out, int32_t max)
+{
+    if (!out || max < VST_K_COUNT)
+        return VST_E_INVAL;
+    for (int k = 0; k < VST_K_COUNT; ++k)
+        out[k] = vst_prof_stat{k, 0, 0, 0.0};
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    vst_status st = VST_OK;
+    for (const ProfRec& r : g_prof_recs) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+            st = VST_E_CUDA;
+        out[r.kid].launches += 1;
+        out[r.kid].total_ms += ms;
+        g_event_pool.push_back(r.a);
+        g_event_pool.push_back(r.b);
+    }
+    g_prof_recs.clear();
+    return st;
+}
+
+int64_t vst_launch_count(void) { return g_launches.load(); }
+
+const char* vst_kernel_name(int32_t kernel)
+{
+    switch (kernel) {
+    case VST_K_ROPE_APPEND: return "rope_append_kernel";
+    case VST_K_COMPACT: return "compact_kernel";
+    case VST_K_ENC_ATTN: return "enc_attn_kernel";
+    case VST_K_DEC_STEP: return "dec_step_kernel";
+    }
+    return "unknown";
+}
 
 const char* vst_status_str(vst_status s)
 {
@@ -280,7 +379,9 @@ vst_status vst_module_create(const vst_config* cfg, vst_module** out)
         return VST_E_NOMEM;
     m->cfg = *cfg;
     m->device = dev;
-    m->splits = cfg->kind == VST_DEC ? dec_splits(*cfg) : 0;
+    m->splits = scratch_slots(*cfg);
+    if (cudaDeviceGetAttribute(&m->n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || m->n_sms <= 0)
+        m->n_sms = 148;
     if (cudaMalloc(&m->rope, n * sizeof(float2)) != cudaSuccess) {
         delete m;
         return VST_E_NOMEM;
@@ -347,8 +448,8 @@ vst_status vst_ctx_create(const vst_module* m, void* dev_mem, size_t bytes, void
     c->tmap_v = reinterpret_cast<const CUtensorMap*>(c->mem + kTmapOffset + sizeof(CUtensorMap));
     c->k_ring = reinterpret_cast<__nv_bfloat16*>(c->mem + L.k_off);
     c->v_ring = reinterpret_cast<__nv_bfloat16*>(c->mem + L.v_off);
-    c->part_ml = L.ml_off ? reinterpret_cast<float*>(c->mem + L.ml_off) : nullptr;
-    c->part_o = L.o_off ? reinterpret_cast<float*>(c->mem + L.o_off) : nullptr;
+    c->part_ml = reinterpret_cast<float*>(c->mem + L.ml_off);
+    c->part_o = reinterpret_cast<float*>(c->mem + L.o_off);
     bool ok = make_ring_map(&c->host_maps[0], c->k_ring, m->cfg) && make_ring_map(&c->host_maps[1], c->v_ring, m->cfg);
     cudaStream_t s = as_stream(stream);
     if (ok)
@@ -488,14 +589,14 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
     auto* ob = static_cast<__nv_bfloat16*>(out);
 
     const CompactCommon cc{Hk, cfg.ring_slots, D, cfg.window};
-    const AppendCommon ac{m->rope, 0, Hk, D, cfg.ring_slots, 0};
-    const EncAttnCommon ec{m->rope, 0, H, cfg.window, (float)(1.4426950408889634 / std::sqrt((double)D))};
+    const EncAttnCommon ec{m->rope, 0, H, cfg.window, cfg.ring_slots, 0, m->splits,
+                           (float)(1.4426950408889634 / std::sqrt((double)D))};
     CompactJob cj[kMaxJobs];
-    AppendJob aj[kMaxJobs];
     EncAttnJob ej[kMaxJobs];
 
     for (int32_t off = 0; off < n_new;) {
         const int32_t b = n_new - off < cfg.max_batch ? n_new - off : cfg.max_batch;
+        const int q_tiles = (b + kEncTileM - 1) / kEncTileM;
         for (int c0 = 0; c0 < n_ctx; c0 += kMaxJobs) {
             const int nj = n_ctx - c0 < kMaxJobs ? n_ctx - c0 : kMaxJobs;
             int ncj = 0;
@@ -509,22 +610,28 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
                     c->n_compactions += 1;
                 }
             }
-            if (launch_compact(cc, cj, ncj, s) != cudaSuccess)
+            if (ncj > 0 && tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc, cj, ncj, s); }) != cudaSuccess)
                 return fail_all(ctxs, n_ctx);
+            // Launch shape: one CTA per (ctx, head, query tile) when that fills the GPU;
+            // otherwise (a single query tile) one CTA per (ctx, head, key tile). Same bits.
+            const bool split = q_tiles == 1 && (long long)nj * H < m->n_sms;
+            int grid_x = q_tiles;
             for (int i = 0; i < nj; ++i) {
                 vst_ctx* c = ctxs[c0 + i];
                 const long long row = (long long)(c0 + i) * n_new + off;
-                aj[i] = AppendJob{kb + row * Hk * D, vb + row * Hk * D, c->k_ring, c->v_ring, c->abs_next, c->n_kv};
-                ej[i] = EncAttnJob{qb + row * H * D, ob + row * H * D, c->tmap_k, c->tmap_v, c->err, c->abs_next,
-                                   c->abs_base};
+                ej[i] = EncAttnJob{qb + row * H * D, kb + row * Hk * D, vb + row * Hk * D, ob + row * H * D,
+                                   c->k_ring, c->v_ring, c->tmap_k, c->tmap_v, c->part_ml, c->part_o,
+                                   c->counters, c->err, c->abs_next, c->abs_base, c->n_kv};
+                if (split) {
+                    const long long lo = c->abs_next - cfg.window + 1 > 0 ? c->abs_next - cfg.window + 1 : 0;
+                    const int tiles = (int)((c->abs_next + b - 1) / kEncTileN - lo / kEncTileN + 1);
+                    grid_x = tiles > grid_x ? tiles : grid_x;
+                }
             }
-            AppendCommon a2 = ac;
-            a2.n_rows = b;
-            if (launch_rope_append(a2, aj, nj, s) != cudaSuccess)
-                return fail_all(ctxs, n_ctx);
             EncAttnCommon e2 = ec;
             e2.n_rows = b;
-            if (launch_enc_attn(e2, ej, nj, s) != cudaSuccess)
+            e2.split = split ? 1 : 0;
+            if (tracked(VST_K_ENC_ATTN, s, [&] { return launch_enc_attn(e2, ej, nj, grid_x, s); }) != cudaSuccess)
                 return fail_all(ctxs, n_ctx);
             for (int i = 0; i < nj; ++i) {
                 ctxs[c0 + i]->n_kv += b;
@@ -554,7 +661,8 @@ vst_status vst_ctx_compact(vst_ctx* c, void* stream)
     DeviceGuard g(c->m->device);
     const CompactCommon cc{cfg.n_kv_heads, cfg.ring_slots, cfg.head_dim, cfg.window};
     const CompactJob cj{c->k_ring, c->v_ring, c->n_kv - cfg.window};
-    if (launch_compact(cc, &cj, 1, as_stream(stream)) != cudaSuccess)
+    cudaStream_t s = as_stream(stream);
+    if (tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc, &cj, 1, s); }) != cudaSuccess)
         return fail_all(cs, 1);
     c->abs_base += c->n_kv - cfg.window;
     c->n_kv = cfg.window;
@@ -604,7 +712,7 @@ vst_status vst_dec_step(vst_ctx* const* ctxs, int32_t n_streams, const void* q, 
         }
         DecCommon dc = dc0;
         dc.n_jobs = nj;
-        if (launch_dec_step(dc, jobs, nj, work, s) != cudaSuccess)
+        if (tracked(VST_K_DEC_STEP, s, [&] { return launch_dec_step(dc, jobs, nj, work, s); }) != cudaSuccess)
             return fail_all(ctxs, n_streams);
         for (int i = 0; i < nj; ++i)
             ctxs[c0 + i]->abs_next += 1;
@@ -637,7 +745,8 @@ vst_status vst_dec_append(vst_ctx* c, const void* k, const void* v, int32_t n, v
         const AppendCommon ac{c->m->rope, rows, Hk, D, cfg.ring_slots, 1};
         const AppendJob aj{kb + (long long)off * Hk * D, vb + (long long)off * Hk * D, c->k_ring, c->v_ring,
                            c->abs_next, 0};
-        if (launch_rope_append(ac, &aj, 1, as_stream(stream)) != cudaSuccess)
+        cudaStream_t s = as_stream(stream);
+        if (tracked(VST_K_ROPE_APPEND, s, [&] { return launch_rope_append(ac, &aj, 1, s); }) != cudaSuccess)
             return fail_all(cs, 1);
         c->abs_next += rows;
     }

@@ -5,8 +5,10 @@
 //                     KV head, decoder only)
 //   [256, 512)        two CUtensorMap (128 B each, 64-B aligned): K ring, V ring
 //   [512, ...)        K ring [Hk][R][D] bf16, then V ring [Hk][R][D] bf16
-//   decoder only      partial softmax state per (query head, split): m, l [H][S][2] fp32 and
-//                     o [H][S][D] fp32, S = splits per step
+//   then              partial softmax state per (query head, split or key tile): m, l
+//                     [H][S][(128)][2] fp32 and o [H][S][(128)][D] fp32; decoder: S splits
+//                     per step, one query row each; encoder: S key tiles of 128 rows (split
+//                     launch shape of the chunk attention)
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -22,9 +24,12 @@ constexpr int kErrOffset = 0;
 constexpr int kCounterOffset = 64;
 constexpr int kTmapOffset = 256;
 
-// Decoder split: keys are reduced in blocks of kDecSplit absolute positions.
-constexpr int kDecSplit = 128;
-// Encoder attention tiles: 128 queries x 128 keys (absolute-position aligned).
+// Decoder: keys are processed in tiles of kDecTile absolute positions and reduced into one
+// partial per split of kDecSplit absolute positions (the ring must be a multiple of a tile).
+constexpr int kDecTile = 128;
+constexpr int kDecSplit = 512;
+// Encoder attention tiles: 128 queries x 128 keys (absolute-position aligned). A query tile
+// of up to 128 rows meets at most enc_split_tiles(W) key tiles.
 constexpr int kEncTileM = 128;
 constexpr int kEncTileN = 128;
 
@@ -60,17 +65,27 @@ struct CompactCommon {
 
 struct EncAttnJob {
     const __nv_bfloat16* q;  // [n_rows][H][D] input rows of this batch
+    const __nv_bfloat16* k;  // [n_rows][H][D] (encoder: Hk = H), not rotated yet
+    const __nv_bfloat16* v;
     __nv_bfloat16* out;      // [n_rows][H][D]
+    __nv_bfloat16* k_ring;   // [H][R][D]: the batch's rows go to slots slot0 + row
+    __nv_bfloat16* v_ring;
     const CUtensorMap* tmap_k;  // over the K ring, dims {D, R, Hk}, box {64, 128, 1}, SW128
     const CUtensorMap* tmap_v;
+    float* part_ml;          // split mode scratch: [H][split_tiles][128][2] (m_t, l_t)
+    float* part_o;           // split mode scratch: [H][split_tiles][128][D]
+    unsigned* counters;      // split mode: [H] tiles finished per head
     int* err;
     long long pos0;          // absolute position of row 0
     long long abs_base;      // absolute position held by ring slot 0
+    long long slot0;         // ring slot of row 0 (n_kv before the batch)
 };
 
 struct EncAttnCommon {
     const float2* rope;
-    int n_rows, H, W;
+    int n_rows, H, W, R;
+    int split;               // 1: grid.x runs over key tiles of one query tile
+    int split_tiles;         // scratch tiles per head
     float scale_log2;        // log2(e) / sqrt(D)
 };
 
@@ -115,7 +130,7 @@ cudaError_t launch_rope_append(const AppendCommon& c, const AppendJob* jobs, int
                                cudaStream_t s);
 cudaError_t launch_compact(const CompactCommon& c, const CompactJob* jobs, int n_jobs,
                            cudaStream_t s);
-cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int n_jobs,
+cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int n_jobs, int grid_x,
                             cudaStream_t s);
 cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, int total_work,
                             cudaStream_t s);

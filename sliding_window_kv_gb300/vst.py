@@ -36,10 +36,18 @@ class CtxInfo(ctypes.Structure):
                 ("n_compactions", ctypes.c_int64), ("k_ring", ctypes.c_void_p), ("v_ring", ctypes.c_void_p)]
 
 
+class ProfStat(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
+
+
+K_ROPE_APPEND, K_COMPACT, K_ENC_ATTN, K_DEC_STEP, K_COUNT = 0, 1, 2, 3, 4
+
 EXPORTS = ["vst_config_default", "vst_module_create", "vst_module_destroy", "vst_module_config",
            "vst_ctx_bytes", "vst_ctx_create", "vst_ctx_reset", "vst_ctx_destroy", "vst_ctx_info_get",
            "vst_ctx_check", "vst_enc_feed", "vst_enc_feed_batch", "vst_ctx_compact", "vst_enc_plan",
-           "vst_dec_step", "vst_dec_append", "vst_status_str", "vst_version"]
+           "vst_dec_step", "vst_dec_append", "vst_prof_enable", "vst_prof_read", "vst_launch_count",
+           "vst_kernel_name", "vst_status_str", "vst_version"]
 
 _lib = None
 
@@ -71,6 +79,10 @@ def lib():
                               ctypes.POINTER(I32), ctypes.POINTER(I64), ctypes.POINTER(I64)], I32),
             "vst_dec_step": ([PP, I32, P, P, P, P, P], I32),
             "vst_dec_append": ([P, P, P, I32, P], I32),
+            "vst_prof_enable": ([I32], I32),
+            "vst_prof_read": ([ctypes.POINTER(ProfStat), I32], I32),
+            "vst_launch_count": ([], I64),
+            "vst_kernel_name": ([I32], ctypes.c_char_p),
             "vst_status_str": ([I32], ctypes.c_char_p),
             "vst_version": ([], ctypes.c_char_p),
         }
@@ -248,3 +260,22 @@ class Ctx:
             self.close()
         except Exception:
             pass
+
+
+def prof_enable(on: bool):
+    _check(lib().vst_prof_enable(1 if on else 0), "vst_prof_enable")
+
+
+def prof_read() -> dict:
+    """{kernel name: (launches, total_ms)} for the launches timed since the last read."""
+    arr = (ProfStat * K_COUNT)()
+    _check(lib().vst_prof_read(arr, K_COUNT), "vst_prof_read")
+    return {kernel_name(a.kernel): (a.launches, a.total_ms) for a in arr}
+
+
+def launch_count() -> int:
+    return lib().vst_launch_count()
+
+
+def kernel_name(k: int) -> str:
+    return lib().vst_kernel_name(k).decode()

@@ -196,11 +196,14 @@ def test_enc_ring_after_compaction_bit_exact(dev, enc_module):
     ctx.close()
 
 
-def test_enc_batch_equals_single(dev, enc_module):
+@pytest.mark.parametrize("n_ctx,step", [(4, 300), (8, 100)])
+def test_enc_batch_equals_single(dev, enc_module, n_ctx, step):
     """Streams with staggered starts fed together through vst_enc_feed_batch give the same
-    bits as each stream fed alone."""
-    n_ctx, T, step = 4, 900, 300
-    offsets = [0, 96, 192, 700]
+    bits as each stream fed alone. With 8 contexts x 20 heads the batched launch runs one
+    CTA per query tile while a lone 100-frame feed splits its key tiles across CTAs: the two
+    launch shapes must agree bit for bit."""
+    T = 900
+    offsets = [0, 96, 192, 700, 13, 1536, 1537, 3000][:n_ctx]
     ins = [_enc_inputs(5, s, T) for s in range(n_ctx)]
     pres = [_enc_inputs(55, s, offsets[s]) if offsets[s] else None for s in range(n_ctx)]
 
