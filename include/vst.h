@@ -161,6 +161,27 @@ VST_API vst_status vst_enc_plan(const vst_config* cfg, int64_t n_kv, int64_t abs
  * q [n_streams][H][D], k/v [n_streams][Hk][D], out [n_streams][H][D]. */
 VST_API vst_status vst_dec_step(vst_ctx* const* ctxs, int32_t n_streams, const void* q, const void* k,
                         const void* v, void* out, void* stream);
+/* vst_dec_step for callers that cannot allocate device memory at call time. The paper
+ * (the pages this library follows) has no counterpart: this is a deployment variant.
+ * Some callers must not call cudaMalloc while they stream: a real-time audio thread that
+ * may not block (cudaMalloc can synchronise the device and take milliseconds), or a
+ * process whose device memory is owned by another allocator or fixed at start-up. This
+ * call computes exactly what vst_dec_step computes, but its scratch (split partials and
+ * merge counters) lives in one static device array of 4 MiB inside libvst, held on every
+ * GPU that loads the library until the process exits; the call itself allocates nothing.
+ *   - Limit: n_streams * per-stream scratch must fit in 4 MiB, where per-stream scratch is
+ *     H*S*2*4 + H*S*D*4 + Hk*4 bytes (each part rounded up to 256) and S = splits per
+ *     step, ceil((W-1)/512) + 1. For the pages' decoder (32 heads x 128, window 8192,
+ *     S = 17) that is 14 streams per call. Larger calls return VST_E_INVAL, nothing
+ *     enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call uses the same array and leaves its last contents there; each call clears
+ *     the counters it needs (stream-ordered) before its launch. Two calls that overlap on
+ *     the GPU (different streams, not ordered) race on the array: order them.
+ * Arguments, layouts, ownership and errors are those of vst_dec_step. */
+VST_API vst_status vst_dec_step_noalloc(vst_ctx* const* ctxs, int32_t n_streams, const void* q,
+                                        const void* k, const void* v, void* out, void* stream);
 /* Append n tokens of K/V (no attention) at positions abs_next .. abs_next + n - 1 of one
  * decoder ctx: k/v [n][Hk][D]. Used to fill a cache. */
 VST_API vst_status vst_dec_append(vst_ctx* c, const void* k, const void* v, int32_t n, void* stream);

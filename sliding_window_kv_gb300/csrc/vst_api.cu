@@ -754,3 +754,102 @@ vst_status vst_dec_append(vst_ctx* c, const void* k, const void* v, int32_t n, v
 }
 
 }  // extern "C"
+
+// ---- decoder step without allocation ---------------------------------------------------
+// Same computation as vst_dec_step, but the per-call scratch (split partials and the merge
+// counters) comes from one file-scope device array instead of the contexts' memory, so the
+// call itself allocates nothing. The array is fixed at kNoAllocScratchBytes; its device
+// address is looked up once per device with cudaGetSymbolAddress (in host code the symbol
+// is only a stand-in, not a device address).
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB per device, held until exit
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array on device `dev` (looked up on first use).
+cudaError_t noalloc_scratch(int dev, unsigned char** out)
+{
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return e;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = static_cast<unsigned char*>(g_noalloc_ptr[dev]);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+vst_status vst_dec_step_noalloc(vst_ctx* const* ctxs, int32_t n_streams, const void* q, const void* k, const void* v,
+                                void* out, void* stream)
+{
+    vst_status st = check_ctxs(ctxs, n_streams, VST_DEC);
+    if (st != VST_OK)
+        return st;
+    if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return VST_E_INVAL;
+    const vst_module* m = ctxs[0]->m;
+    const vst_config& cfg = m->cfg;
+    for (int i = 0; i < n_streams; ++i)
+        if (ctxs[i]->abs_next >= cfg.max_position)
+            return VST_E_INVAL;
+    const int H = cfg.n_heads, Hk = cfg.n_kv_heads, D = cfg.head_dim;
+    // per stream: m, l [H][S][2] and o [H][S][D] floats, then Hk counters (256-B aligned)
+    const size_t ml_bytes = align256((size_t)H * m->splits * 2 * sizeof(float));
+    const size_t o_bytes = align256((size_t)H * m->splits * D * sizeof(float));
+    const size_t cnt_bytes = align256((size_t)Hk * sizeof(unsigned));
+    const size_t per_stream = ml_bytes + o_bytes + cnt_bytes;
+    if ((size_t)n_streams * per_stream > kNoAllocScratchBytes || n_streams > kMaxJobs)
+        return VST_E_INVAL;  // more streams than the fixed scratch holds
+    DeviceGuard g(m->device);
+    if (!g.ok)
+        return fail_all(ctxs, n_streams);
+    unsigned char* scratch = nullptr;
+    if (noalloc_scratch(m->device, &scratch) != cudaSuccess)
+        return fail_all(ctxs, n_streams);
+    cudaStream_t s = as_stream(stream);
+    const auto* qb = static_cast<const __nv_bfloat16*>(q);
+    const auto* kb = static_cast<const __nv_bfloat16*>(k);
+    const auto* vb = static_cast<const __nv_bfloat16*>(v);
+    auto* ob = static_cast<__nv_bfloat16*>(out);
+    DecCommon dc{m->rope, n_streams, Hk, cfg.ring_slots, cfg.window, m->splits,
+                 (float)(1.4426950408889634 / std::sqrt((double)D))};
+    DecJob jobs[kMaxJobs];
+    int work = 0;
+    for (int i = 0; i < n_streams; ++i) {
+        vst_ctx* c = ctxs[i];
+        unsigned char* base = scratch + (size_t)i * per_stream;
+        const long long pos = c->abs_next;
+        const long long lo = pos - cfg.window + 1 > 0 ? pos - cfg.window + 1 : 0;
+        const int sig0 = (int)(lo / kDecSplit);
+        const int nsp = (int)(pos / kDecSplit) - sig0 + 1;
+        jobs[i] = DecJob{qb + (long long)i * H * D, kb + (long long)i * Hk * D, vb + (long long)i * Hk * D,
+                         ob + (long long)i * H * D, c->k_ring, c->v_ring, c->tmap_k, c->tmap_v,
+                         reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + ml_bytes),
+                         reinterpret_cast<unsigned*>(base + ml_bytes + o_bytes), c->err, pos, sig0, nsp, work, 0};
+        work += nsp;
+    }
+    // The merge counters must start at zero; the kernel re-arms them, but the array is
+    // shared by every call, so clear this call's counters first (stream-ordered).
+    for (int i = 0; i < n_streams; ++i)
+        if (cudaMemsetAsync(scratch + (size_t)i * per_stream + ml_bytes + o_bytes, 0, cnt_bytes, s) != cudaSuccess)
+            return fail_all(ctxs, n_streams);
+    if (launch_dec_step(dc, jobs, n_streams, work, s) != cudaSuccess)
+        return fail_all(ctxs, n_streams);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    for (int i = 0; i < n_streams; ++i)
+        ctxs[i]->abs_next += 1;
+    return VST_OK;
+}
+
+}  // extern "C"
