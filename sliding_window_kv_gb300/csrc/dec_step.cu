@@ -9,14 +9,17 @@
 // Work item: one CTA per (stream, KV head g, split), a split being the 512 absolute
 // positions [512*sigma, 512*sigma + 512) -- four key tiles of 128 -- cut to the step's
 // window [max(0, pos-W+1), pos]. The CTA streams its tiles through a two-stage TMA ring
-// (K and V of a tile, 64 KB per stage, 128-B swizzle, slots 128*tau mod R) and for each tile:
+// (K and V of a tile, 64 KB per stage, 128-B swizzle, slots 128*tau mod R). Per tile:
 //   S^T = K Q'^T     tcgen05.mma M=128 keys, N=16 (the 4 query heads of the group, zero
-//                    padded), K=128 dims; A = K tile (K-major), B = Q' (K-major); in TMEM
-//   softmax          one key per thread (TMEM lane); per head: tile max and sum by warp
-//                    shuffles then across the 4 warps in fixed order; P^T -> smem (bf16)
+//                    padded), K=128 dims; A = K tile (K-major), B = Q' (K-major); TMEM,
+//                    double-buffered so the next tile's scores are computed during this
+//                    tile's softmax
+//   softmax          512 threads: thread (head h, key k) holds one score; per head the
+//                    tile max and sum go through warp shuffles and the head's 4 warps
+//                    (fixed order); P^T -> smem (bf16)
 //   O^T = V^T P^T    tcgen05.mma M=128 dims, N=16, K=128 keys; A = V tile read as
-//                    MN-major (dims contiguous), B = P^T (K-major); in TMEM
-//   fold             thread d folds (m_t, l_t, O_t[d]) of the 4 heads into registers.
+//                    MN-major (dims contiguous), B = P^T (K-major); TMEM
+//   fold             thread (head h, dim d) folds (m_t, l_t, O_t[h][d]) into registers.
 // The query heads are rotated in the prologue; if the split holds pos, the new key is
 // rotated too, patched into its tile row in shared memory, and stored (K', V) to ring slot
 // pos % R by this CTA. Each CTA writes its split's (m, l, o) per head; the last CTA of
@@ -31,20 +34,22 @@ namespace vst {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 512;
 constexpr int kD = 128;
 constexpr int kG = 4;                       // query heads per KV head
 constexpr int kTile = kDecTile;             // keys per tile
 constexpr int kTilesPerSplit = kDecSplit / kTile;
+constexpr int kMaxSplits = 32;              // merge register budget (S <= 32: W <= 15873)
 constexpr uint32_t kBox = 128u * 128u;      // 128 keys x 64 dims x 2 B
 constexpr uint32_t kStage = 4 * kBox;       // K lo, K hi, V lo, V hi
 constexpr uint32_t kOffQ = 2 * kStage;      // Q' [16 rows][128 dims]: 2 blocks of 2 KB
 constexpr uint32_t kOffP = kOffQ + 4096;    // P^T [16 rows][128 keys]: 2 blocks of 2 KB
 constexpr uint32_t kOffNew = kOffP + 4096;  // new K' row, new V row (bf16 x 128 each)
-constexpr uint32_t kOffRed = kOffNew + 512; // float [2][4 warps][4 heads]
+constexpr uint32_t kOffRed = kOffNew + 512; // float [2][4 heads][4 warps]
 constexpr uint32_t kOffBar = kOffRed + 128;
 constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;
-constexpr uint32_t kTmemCols = 32;          // S^T in [0,16), O^T in [16,32)
+constexpr uint32_t kTmemCols = 64;          // S^T buffers at [0,16) and [16,32); O^T at [32,48)
+constexpr uint32_t kTmO = 32;
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 16, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 16, true, false);
@@ -63,6 +68,12 @@ __device__ __forceinline__ float warp_sum(float x)
     for (int o = 16; o > 0; o >>= 1)
         x = __fadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
     return x;
+}
+
+// Barrier over the 4 warps (128 threads) of one head group.
+__device__ __forceinline__ void head_sync(int hh)
+{
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + hh) : "memory");
 }
 
 // Fold a tile-local (or split-local) softmax state into a running one (one value of o).
@@ -92,16 +103,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ int s_last;
+    __shared__ int s_fail;
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* sQ = smem + kOffQ;
     uint8_t* sP = smem + kOffP;
     __nv_bfloat16* snew = reinterpret_cast<__nv_bfloat16*>(smem + kOffNew);
-    float* sred = reinterpret_cast<float*>(smem + kOffRed);
+    float* red_m = reinterpret_cast<float*>(smem + kOffRed);  // [4 heads][4 warps]
+    float* red_l = red_m + 16;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
     const uint32_t bar_full0 = smem_u32(&bars[0]);
     const uint32_t bar_full1 = smem_u32(&bars[1]);
-    const uint32_t bar_m = smem_u32(&bars[2]);
+    const uint32_t bar_s0 = smem_u32(&bars[2]);
+    const uint32_t bar_s1 = smem_u32(&bars[3]);
+    const uint32_t bar_o = smem_u32(&bars[4]);
 
     const DecCommon& c = p.c;
     const int item = blockIdx.x;
@@ -112,7 +127,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = blockIdx.y;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int sl = item - job.work_begin;  // split index within this step
+    const int hh = warp >> 2;                 // query head of the group owned by this thread
+    const int row = 32 * (warp & 3) + lane;   // TMEM lane: key of the tile (S), dim (O)
+    const int sl = item - job.work_begin;     // split index within this step
     const long long pos = job.pos;
     const long long lo = max(0LL, pos - c.W + 1);
     const long long sig = job.sigma0 + sl;
@@ -120,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long tau_hi = min(sig * kTilesPerSplit + kTilesPerSplit - 1, pos / kTile);
     const int n_tiles = (int)(tau_hi - tau_lo + 1);
     const long long tau_new = pos / kTile;  // tile holding this step's key
+    const bool has_new = tau_new >= tau_lo && tau_new <= tau_hi;
 
     auto issue_tile = [&](int i) {
         const int st = i & 1;
@@ -134,9 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (tid == 0) {
-        mbar_init(bar_full0, 1);
-        mbar_init(bar_full1, 1);
-        mbar_init(bar_m, 1);
+        s_fail = 0;
+        for (int b = 0; b < 5; ++b)
+            mbar_init(smem_u32(&bars[b]), 1);
         fence_mbar_init();
         tmap_acquire(job.tmap_k);
         tmap_acquire(job.tmap_v);
@@ -149,188 +167,170 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
 
-    // ---- Q' (4 rotated heads, bf16) and zero padding rows 4..15 of Q' and P^T
-    for (int e = tid; e < 12 * 16; e += kThreads) {  // 12 rows x 16 chunks of zeros, both tiles
-        const int row = 4 + e / 16, ch = e % 16;
-        const uint32_t off = (uint32_t)((ch >> 3) * 2048) + sw128_offset(row, ch & 7);
-        *reinterpret_cast<uint4*>(sQ + off) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sP + off) = make_uint4(0, 0, 0, 0);
-    }
-    {
-        const int hh = warp;  // one warp per query head, lane owns pairs (2l, 2l+1)
-        const __nv_bfloat16* q = job.q + (long long)(g * kG + hh) * kD;
-        const float2* cs = c.rope + pos * (kD / 2);
-        const uint32_t a = *reinterpret_cast<const uint32_t*>(q + 2 * lane);
-        const uint32_t b = *reinterpret_cast<const uint32_t*>(q + 64 + 2 * lane);
-        float y1, y2, y3, y4;
-        rope_pair(bf16lo(a), bf16lo(b), cs[2 * lane], y1, y2);
-        rope_pair(bf16hi(a), bf16hi(b), cs[2 * lane + 1], y3, y4);
-        *reinterpret_cast<uint32_t*>(sQ + sw16(hh, 2 * lane)) = pack_bf16(y1, y3);
-        *reinterpret_cast<uint32_t*>(sQ + sw16(hh, 64 + 2 * lane)) = pack_bf16(y2, y4);
-    }
-    const bool has_new = tau_new >= tau_lo && tau_new <= tau_hi;
-    if (has_new && warp == 0) {
-        const __nv_bfloat16* k = job.k + (long long)g * kD;
-        const __nv_bfloat16* v = job.v + (long long)g * kD;
-        const float2* cs = c.rope + pos * (kD / 2);
-        const uint32_t a = *reinterpret_cast<const uint32_t*>(k + 2 * lane);
-        const uint32_t b = *reinterpret_cast<const uint32_t*>(k + 64 + 2 * lane);
-        float y1, y2, y3, y4;
-        rope_pair(bf16lo(a), bf16lo(b), cs[2 * lane], y1, y2);
-        rope_pair(bf16hi(a), bf16hi(b), cs[2 * lane + 1], y3, y4);
-        reinterpret_cast<uint32_t*>(snew)[lane] = pack_bf16(y1, y3);
-        reinterpret_cast<uint32_t*>(snew)[32 + lane] = pack_bf16(y2, y4);
-        reinterpret_cast<uint32_t*>(snew + kD)[lane] = *reinterpret_cast<const uint32_t*>(v + 2 * lane);
-        reinterpret_cast<uint32_t*>(snew + kD)[32 + lane] = *reinterpret_cast<const uint32_t*>(v + 64 + 2 * lane);
+    // ---- Q' (4 rotated heads, bf16), the new K'/V row, zero padding rows 4..15
+    if (tid < 256) {
+        const int h = tid >> 6, i = tid & 63;  // pair (i, i + 64) of head h
+        const __nv_bfloat16* q = job.q + (long long)(g * kG + h) * kD;
+        float y1, y2;
+        rope_pair(__bfloat162float(q[i]), __bfloat162float(q[i + 64]), c.rope[pos * (kD / 2) + i], y1, y2);
+        *reinterpret_cast<__nv_bfloat16*>(sQ + sw16(h, i)) = __float2bfloat16_rn(y1);
+        *reinterpret_cast<__nv_bfloat16*>(sQ + sw16(h, i + 64)) = __float2bfloat16_rn(y2);
+    } else if (tid < 320) {
+        if (has_new) {
+            const int i = tid - 256;
+            const __nv_bfloat16* k = job.k + (long long)g * kD;
+            const __nv_bfloat16* v = job.v + (long long)g * kD;
+            float y1, y2;
+            rope_pair(__bfloat162float(k[i]), __bfloat162float(k[i + 64]), c.rope[pos * (kD / 2) + i], y1, y2);
+            snew[i] = __float2bfloat16_rn(y1);
+            snew[i + 64] = __float2bfloat16_rn(y2);
+            snew[kD + i] = v[i];
+            snew[kD + i + 64] = v[i + 64];
+        }
+    } else {
+        for (int e = tid - 320; e < 12 * 16; e += kThreads - 320) {  // 12 rows x 16 chunks
+            const int r = 4 + e / 16, ch = e % 16;
+            const uint32_t off = (uint32_t)((ch >> 3) * 2048) + sw128_offset(r, ch & 7);
+            *reinterpret_cast<uint4*>(sQ + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sP + off) = make_uint4(0, 0, 0, 0);
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    // running state: thread tid owns dimension d = tid of the 4 heads
-    float m[kG], l[kG], o[kG];
-#pragma unroll
-    for (int h = 0; h < kG; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.f;
-        o[h] = 0.f;
-    }
-    int fail = 0, aborted = 0;
-    uint32_t ph_m = 0;
-    int issued = n_tiles < 2 ? n_tiles : 2;  // tiles whose loads thread 0 has issued
-    int consumed = 0;                       // tiles whose loads have landed
-
-    for (int i = 0; i < n_tiles; ++i) {
-        const long long tau = tau_lo + i;
+    // Warp 0: wait for tile i's K/V, patch the new row in if it is there, and (thread 0)
+    // issue S^T for it into S buffer i & 1. Returns false if the wait gave up.
+    auto prepare_and_issue_s = [&](int i) -> bool {
         const int st = i & 1;
         uint8_t* sK = smem + st * kStage;
-        uint8_t* sV = sK + 2 * kBox;
-        if (!mbar_wait(st ? bar_full1 : bar_full0, (uint32_t)((i >> 1) & 1)))
-            fail = 1;
-        else
-            consumed = i + 1;
-        if (!fail && has_new && tau == tau_new && tid < 16) {
-            // chunk tid of the new 256-byte row: dims [8*tid, 8*tid+8)
-            const int rr = (int)(pos - tau * kTile);
-            const int half = tid >> 3, ch = tid & 7;
-            const uint4 kw = reinterpret_cast<const uint4*>(snew)[tid];
-            const uint4 vw = reinterpret_cast<const uint4*>(snew + kD)[tid];
+        bool ok = mbar_wait(st ? bar_full1 : bar_full0, (uint32_t)((i >> 1) & 1));
+        if (ok && has_new && tau_lo + i == tau_new && lane < 16) {
+            // chunk `lane` of the new 256-byte row: dims [8*lane, 8*lane+8)
+            const int rr = (int)(pos - tau_new * kTile);
+            const int half = lane >> 3, ch = lane & 7;
+            const uint4 kw = reinterpret_cast<const uint4*>(snew)[lane];
+            const uint4 vw = reinterpret_cast<const uint4*>(snew + kD)[lane];
             *reinterpret_cast<uint4*>(sK + half * kBox + sw128_offset(rr, ch)) = kw;
-            *reinterpret_cast<uint4*>(sV + half * kBox + sw128_offset(rr, ch)) = vw;
-            const long long gofs = ((long long)g * c.R + pos % c.R) * kD + 8 * tid;
+            *reinterpret_cast<uint4*>(sK + 2 * kBox + half * kBox + sw128_offset(rr, ch)) = vw;
+            const long long gofs = ((long long)g * c.R + pos % c.R) * kD + 8 * lane;
             *reinterpret_cast<uint4*>(job.k_ring + gofs) = kw;
             *reinterpret_cast<uint4*>(job.v_ring + gofs) = vw;
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(fail)) {
-            aborted = 1;
-            break;
-        }
-        tc_fence_after();
-
-        // ---- S^T = K Q'^T
-        if (tid == 0) {
+        __syncwarp();
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (ok && lane == 0) {
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t ad = smem_desc_sw128(smem_u32(sK) + (kk >> 2) * kBox + 32 * (kk & 3), 16, 1024);
                 const uint64_t bd = smem_desc_sw128(smem_u32(sQ) + (kk >> 2) * 2048 + 32 * (kk & 3), 16, 1024);
-                mma_bf16_ss(tmem + 0, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+                mma_bf16_ss(tmem + 16 * st, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
             }
-            mma_commit(bar_m);
+            mma_commit(st ? bar_s1 : bar_s0);
         }
-        if (!mbar_wait(bar_m, ph_m))
-            fail = 1;
-        ph_m ^= 1;
-        tc_fence_after();
+        return ok;
+    };
 
-        // ---- tile softmax: thread tid owns key 128*tau + tid
-        uint32_t sv[32];
-        tmem_ld_32x32b_x32(tmem + lane_base, sv);
+    // running state of (head hh, dim row)
+    float m = -INFINITY, l = 0.f, o = 0.f;
+    int fail = 0, aborted = 0;
+    uint32_t ph_o = 0;
+    int issued = n_tiles < 2 ? n_tiles : 2;  // tiles whose loads thread 0 has issued
+    int landed = 0;                         // tiles whose loads warp 0 has seen land
+
+    if (warp == 0) {
+        if (prepare_and_issue_s(0))
+            landed = 1;
+        else
+            fail = 1;
+    }
+    for (int i = 0; i < n_tiles; ++i) {
+        const int st = i & 1;
+        // ---- S^T of tile i; warp 0 starts the next tile's S^T right away
+        if (__syncthreads_or(fail)) {
+            aborted = 1;
+            break;
+        }
+        if (!mbar_wait(st ? bar_s1 : bar_s0, (uint32_t)((i >> 1) & 1)))
+            fail = 1;
+        tc_fence_after();
+        if (warp == 0 && !fail && i + 1 < n_tiles) {
+            if (prepare_and_issue_s(i + 1))
+                landed = i + 2;
+            else
+                fail = 1;
+        }
+        uint32_t sv[4];
+        tmem_ld_32x32b_x4(tmem + lane_base + 16 * st, sv);
         tmem_ld_wait();
-        const long long kp = tau * kTile + tid;
+
+        // ---- softmax of head hh over the tile's 128 keys (thread: key `row`)
+        const long long kp = (tau_lo + i) * kTile + row;
         const bool valid = kp >= lo && kp <= pos;
-        float sc[kG];
-#pragma unroll
-        for (int h = 0; h < kG; ++h) {
-            sc[h] = valid ? __fmul_rn(__uint_as_float(sv[h]), c.scale_log2) : -INFINITY;
-            const float wm = warp_max(sc[h]);
-            if (lane == 0)
-                sred[warp * kG + h] = wm;
-        }
-        __syncthreads();
-        float mt[kG], pv[kG];
-#pragma unroll
-        for (int h = 0; h < kG; ++h) {
-            mt[h] = fmaxf(fmaxf(sred[h], sred[kG + h]), fmaxf(sred[2 * kG + h], sred[3 * kG + h]));
-            pv[h] = valid ? ex2(__fsub_rn(sc[h], mt[h])) : 0.f;
-            const float ws = warp_sum(pv[h]);
-            if (lane == 0)
-                sred[16 + warp * kG + h] = ws;
-        }
-#pragma unroll
-        for (int h = 0; h < kG; ++h)
-            *reinterpret_cast<__nv_bfloat16*>(sP + sw16(h, tid)) = __float2bfloat16_rn(pv[h]);
+        const float sc = valid ? __fmul_rn(__uint_as_float(sv[hh]), c.scale_log2) : -INFINITY;
+        const float wm = warp_max(sc);
+        if (lane == 0)
+            red_m[hh * 4 + (warp & 3)] = wm;
+        head_sync(hh);
+        const float mt = fmaxf(fmaxf(red_m[hh * 4], red_m[hh * 4 + 1]), fmaxf(red_m[hh * 4 + 2], red_m[hh * 4 + 3]));
+        const float pv = valid ? ex2(__fsub_rn(sc, mt)) : 0.f;
+        *reinterpret_cast<__nv_bfloat16*>(sP + sw16(hh, row)) = __float2bfloat16_rn(pv);
+        const float ws = warp_sum(pv);
+        if (lane == 0)
+            red_l[hh * 4 + (warp & 3)] = ws;
         fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        float lt[kG];
-#pragma unroll
-        for (int h = 0; h < kG; ++h)
-            lt[h] = __fadd_rn(__fadd_rn(sred[16 + h], sred[16 + kG + h]),
-                              __fadd_rn(sred[16 + 2 * kG + h], sred[16 + 3 * kG + h]));
-
-        // ---- O^T = V^T P^T
-        if (tid == 0) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t ad = smem_desc_sw128(smem_u32(sV) + 2048 * kk, kBox, 1024);
-                const uint64_t bd = smem_desc_sw128(smem_u32(sP) + (kk >> 2) * 2048 + 32 * (kk & 3), 16, 1024);
-                mma_bf16_ss(tmem + 16, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(bar_m);
-        }
-        if (!mbar_wait(bar_m, ph_m))
-            fail = 1;
-        ph_m ^= 1;
-        tc_fence_after();
-        if (tid == 0 && !fail && i + 2 < n_tiles) {  // this stage is free: fetch tile i + 2
-            issue_tile(i + 2);
-            issued = i + 3;
-        }
-        uint32_t ov[32];
-        tmem_ld_32x32b_x32(tmem + lane_base, ov);
-        tmem_ld_wait();
-#pragma unroll
-        for (int h = 0; h < kG; ++h)
-            fold1(m[h], l[h], o[h], mt[h], lt[h], __uint_as_float(ov[16 + h]));
         tc_fence_before();
         if (__syncthreads_or(fail)) {
             aborted = 1;
             break;
         }
         tc_fence_after();
+        const float lt = __fadd_rn(__fadd_rn(red_l[hh * 4], red_l[hh * 4 + 1]), __fadd_rn(red_l[hh * 4 + 2], red_l[hh * 4 + 3]));
+
+        // ---- O^T = V^T P^T; afterwards the stage is free for tile i + 2
+        if (tid == 0) {
+            uint8_t* sV = smem + st * kStage + 2 * kBox;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t ad = smem_desc_sw128(smem_u32(sV) + 2048 * kk, kBox, 1024);
+                const uint64_t bd = smem_desc_sw128(smem_u32(sP) + (kk >> 2) * 2048 + 32 * (kk & 3), 16, 1024);
+                mma_bf16_ss(tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar_o);
+        }
+        if (!mbar_wait(bar_o, ph_o))
+            fail = 1;
+        ph_o ^= 1;
+        tc_fence_after();
+        if (tid == 0 && !fail && i + 2 < n_tiles) {
+            issue_tile(i + 2);
+            issued = i + 3;
+        }
+        uint32_t ov[4];
+        tmem_ld_32x32b_x4(tmem + lane_base + kTmO, ov);
+        tmem_ld_wait();
+        fold1(m, l, o, mt, lt, __uint_as_float(ov[hh]));
+        tc_fence_before();
     }
 
     if (aborted) {
         if (tid == 0) {
             // A bounded wait gave up: record it, let copies still in flight land, release TMEM.
             atomicExch(job.err, kErrTimeout);
-            for (int k = consumed; k < issued; ++k)
+            for (int k = landed; k < issued; ++k)
                 mbar_wait((k & 1) ? bar_full1 : bar_full0, (uint32_t)((k >> 1) & 1));
         }
     } else {
         // ---- this split's partial; the last CTA of (stream, g) folds all splits in order
-#pragma unroll
-        for (int h = 0; h < kG; ++h)
-            job.part_o[((long long)(g * kG + h) * c.S + sl) * kD + tid] = o[h];
-        if (tid < kG)
-            *reinterpret_cast<float2*>(job.part_ml + ((long long)(g * kG + tid) * c.S + sl) * 2) =
-                make_float2(m[tid], l[tid]);
+        const int hq = g * kG + hh;
+        job.part_o[((long long)hq * c.S + sl) * kD + row] = o;
+        if ((warp & 3) == 0 && lane == 0)
+            *reinterpret_cast<float2*>(job.part_ml + ((long long)hq * c.S + sl) * 2) = make_float2(m, l);
         __threadfence();
         __syncthreads();
         if (tid == 0) {
@@ -340,39 +340,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (s_last) {
             __threadfence();
-            const int hh = warp;
-            const int hq = g * kG + hh;
-            const int d4 = lane * 4;
-            float mm = -INFINITY, ll = 0.f;
-            float oo[4] = {0.f, 0.f, 0.f, 0.f};
             const float* pml = job.part_ml + (long long)hq * c.S * 2;
-            const float* po = job.part_o + (long long)hq * c.S * kD + d4;
-            for (int s0 = 0; s0 < job.n_splits; s0 += 8) {
-                float2 ml[8];
-                float4 ov4[8];
+            const float* po = job.part_o + (long long)hq * c.S * kD + row;
+            float2 ml[kMaxSplits];
+            float ov[kMaxSplits];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    if (s0 + u < job.n_splits) {
-                        ml[u] = __ldcg(reinterpret_cast<const float2*>(pml + (s0 + u) * 2));
-                        ov4[u] = __ldcg(reinterpret_cast<const float4*>(po + (long long)(s0 + u) * kD));
-                    }
+            for (int u = 0; u < kMaxSplits; ++u)
+                if (u < job.n_splits) {
+                    ml[u] = __ldcg(reinterpret_cast<const float2*>(pml + u * 2));
+                    ov[u] = __ldcg(po + (long long)u * kD);
                 }
+            float mm = -INFINITY, ll = 0.f, oo = 0.f;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    if (s0 + u < job.n_splits) {
-                        float m0 = mm, l0 = ll;
-                        fold1(m0, l0, oo[0], ml[u].x, ml[u].y, ov4[u].x);
-                        float m1 = mm, l1 = ll;
-                        fold1(m1, l1, oo[1], ml[u].x, ml[u].y, ov4[u].y);
-                        float m2 = mm, l2 = ll;
-                        fold1(m2, l2, oo[2], ml[u].x, ml[u].y, ov4[u].z);
-                        fold1(mm, ll, oo[3], ml[u].x, ml[u].y, ov4[u].w);
-                    }
-                }
-            }
-            const uint32_t w0 = pack_bf16(__fdiv_rn(oo[0], ll), __fdiv_rn(oo[1], ll));
-            const uint32_t w1 = pack_bf16(__fdiv_rn(oo[2], ll), __fdiv_rn(oo[3], ll));
-            *reinterpret_cast<uint2*>(job.out + (long long)hq * kD + d4) = make_uint2(w0, w1);
+            for (int u = 0; u < kMaxSplits; ++u)
+                if (u < job.n_splits)
+                    fold1(mm, ll, oo, ml[u].x, ml[u].y, ov[u]);
+            job.out[(long long)hq * kD + row] = __float2bfloat16_rn(__fdiv_rn(oo, ll));
             if (tid == 0)
                 job.counters[g] = 0u;
         }
@@ -408,6 +391,8 @@ cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, 
 {
     if (n_jobs == 0 || total_work == 0)
         return cudaSuccess;
+    if (c.S > kMaxSplits)
+        return cudaErrorInvalidValue;
     return with_params(c, jobs, n_jobs, [&](const auto& p) {
         return launch_dec_j<sizeof(p.jobs) / sizeof(p.jobs[0])>(p, total_work, s);
     });

@@ -29,9 +29,10 @@
 //
 // Two launch shapes, chosen by the host from the amount of work, give the same bits:
 //   loop mode  -- one CTA per (context, head, 128-query tile) folds its tiles in registers;
-//   split mode -- one CTA per (context, head, key tile) of a single query tile writes its
-//                 tile's (m_t, l_t, O_t) to scratch, and the last CTA of the (context,
-//                 head) folds the tiles in ascending order with the same fold function.
+//   split mode -- one CTA per (context, head, group of `split` consecutive key tiles) of a
+//                 single query tile writes each tile's (m_t, l_t, O_t) to scratch, and the
+//                 last CTA of the (context, head) folds the tiles in ascending order with
+//                 the same fold function.
 // Tiles are fixed by absolute position and folded in ascending order, so a row's result
 // depends only on its own window -- never on how the stream was cut into feeds, on when
 // the ring was compacted, or on the launch shape.
@@ -187,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long p_last = p_first + nrows - 1;
     const long long t_lo = max(0LL, p_first - c.W + 1) / 128;
     const long long t_hi = p_last / 128;
-    const long long t_begin = split ? t_lo + blockIdx.x : t_lo;
-    const long long t_end = split ? t_begin : t_hi;
+    const long long t_begin = split ? t_lo + (long long)blockIdx.x * c.split : t_lo;
+    const long long t_end = split ? min(t_begin + c.split - 1, t_hi) : t_hi;
     if (t_begin > t_hi)
         return;  // split mode: this job has fewer tiles than the grid
 
@@ -395,36 +396,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (s.tid == 0) {
             const unsigned prev = atomicAdd(job.counters + h, 1u);
-            s_last = prev == (unsigned)(t_hi - t_lo);
+            s_last = prev == (unsigned)((t_hi - t_lo) / c.split);  // CTAs of this (job, head) - 1
         }
         __syncthreads();
         if (s_last) {
             __threadfence();
             if (r < nrows) {
+                // fold the tiles in ascending order; the next tile's partial is loaded
+                // before the current one is folded so the L2 round trips overlap
                 const int nt = (int)(t_hi - t_lo + 1);
-                const long long base = (long long)h * c.split_tiles;
-                for (int u0 = 0; u0 < nt; u0 += 8) {
-                    float2 ml[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (u0 + u < nt)
-                            ml[u] = __ldcg(reinterpret_cast<const float2*>(job.part_ml + ((base + u0 + u) * 128 + r) * 2));
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        if (u0 + u < nt && ml[u].x != -INFINITY) {
-                            const float* po = job.part_o + ((base + u0 + u) * 128 + r) * kD + kDq * s.q;
-                            float ot[kDq];
-#pragma unroll
-                            for (int d = 0; d < kDq; d += 4) {
-                                const float4 x = __ldcg(reinterpret_cast<const float4*>(po + d));
-                                ot[d] = x.x;
-                                ot[d + 1] = x.y;
-                                ot[d + 2] = x.z;
-                                ot[d + 3] = x.w;
-                            }
-                            fold_tile(m_run, l_run, o, ml[u].x, ml[u].y, ot);
-                        }
+                const float* pml = job.part_ml + ((long long)h * c.split_tiles * 128 + r) * 2;
+                const float* po = job.part_o + ((long long)h * c.split_tiles * 128 + r) * kD + kDq * s.q;
+                float2 ml = __ldcg(reinterpret_cast<const float2*>(pml));
+                float4 x0 = __ldcg(reinterpret_cast<const float4*>(po));
+                float4 x1 = __ldcg(reinterpret_cast<const float4*>(po + 4));
+                float4 x2 = __ldcg(reinterpret_cast<const float4*>(po + 8));
+                float4 x3 = __ldcg(reinterpret_cast<const float4*>(po + 12));
+                for (int u = 0; u < nt; ++u) {
+                    const float2 cml = ml;
+                    const float ot[kDq] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                           x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+                    if (u + 1 < nt) {
+                        const long long step = (long long)(u + 1) * 128;
+                        ml = __ldcg(reinterpret_cast<const float2*>(pml + step * 2));
+                        x0 = __ldcg(reinterpret_cast<const float4*>(po + step * kD));
+                        x1 = __ldcg(reinterpret_cast<const float4*>(po + step * kD + 4));
+                        x2 = __ldcg(reinterpret_cast<const float4*>(po + step * kD + 8));
+                        x3 = __ldcg(reinterpret_cast<const float4*>(po + step * kD + 12));
                     }
+                    if (cml.x != -INFINITY)
+                        fold_tile(m_run, l_run, o, cml.x, cml.y, ot);
                 }
                 store_out_quarter(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, s.q);
             }

@@ -102,8 +102,10 @@ vst_status check_config(const vst_config* c)
     if (c->kind == VST_DEC) {
         if (c->ring_slots < c->window)
             return VST_E_INVAL;
-        // kernel (c): head dim 128, 4 query heads per KV head, ring a multiple of the split.
-        if (c->head_dim != 128 || c->n_heads != 4 * c->n_kv_heads || c->ring_slots % kDecTile != 0)
+        // kernel (c): head dim 128, 4 query heads per KV head, ring a multiple of the tile,
+        // at most 32 splits per step (window <= 31 * 512 + 1).
+        if (c->head_dim != 128 || c->n_heads != 4 * c->n_kv_heads || c->ring_slots % kDecTile != 0 ||
+            dec_splits(*c) > 32)
             return VST_E_UNSUPPORTED;
         return VST_OK;
     }
@@ -613,9 +615,12 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
             if (ncj > 0 && tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc, cj, ncj, s); }) != cudaSuccess)
                 return fail_all(ctxs, n_ctx);
             // Launch shape: one CTA per (ctx, head, query tile) when that fills the GPU;
-            // otherwise (a single query tile) one CTA per (ctx, head, key tile). Same bits.
+            // otherwise (a single query tile) one CTA per (ctx, head, group of key tiles),
+            // with groups just large enough that every CTA starts in the first wave (one
+            // CTA per SM). Same bits either way.
             const bool split = q_tiles == 1 && (long long)nj * H < m->n_sms;
             int grid_x = q_tiles;
+            int max_tiles = 0;
             for (int i = 0; i < nj; ++i) {
                 vst_ctx* c = ctxs[c0 + i];
                 const long long row = (long long)(c0 + i) * n_new + off;
@@ -625,12 +630,19 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
                 if (split) {
                     const long long lo = c->abs_next - cfg.window + 1 > 0 ? c->abs_next - cfg.window + 1 : 0;
                     const int tiles = (int)((c->abs_next + b - 1) / kEncTileN - lo / kEncTileN + 1);
-                    grid_x = tiles > grid_x ? tiles : grid_x;
+                    max_tiles = tiles > max_tiles ? tiles : max_tiles;
                 }
+            }
+            int per_cta = 0;
+            if (split) {
+                per_cta = 1;
+                while ((long long)nj * H * ((max_tiles + per_cta - 1) / per_cta) > m->n_sms)
+                    ++per_cta;
+                grid_x = (max_tiles + per_cta - 1) / per_cta;
             }
             EncAttnCommon e2 = ec;
             e2.n_rows = b;
-            e2.split = split ? 1 : 0;
+            e2.split = per_cta;
             if (tracked(VST_K_ENC_ATTN, s, [&] { return launch_enc_attn(e2, ej, nj, grid_x, s); }) != cudaSuccess)
                 return fail_all(ctxs, n_ctx);
             for (int i = 0; i < nj; ++i) {

@@ -84,7 +84,7 @@ struct EncAttnJob {
 struct EncAttnCommon {
     const float2* rope;
     int n_rows, H, W, R;
-    int split;               // 1: grid.x runs over key tiles of one query tile
+    int split;               // 0: loop mode; k > 0: split mode, k key tiles per CTA
     int split_tiles;         // scratch tiles per head
     float scale_log2;        // log2(e) / sqrt(D)
 };
