@@ -8,24 +8,28 @@
 //
 // Work item: one CTA per (stream, KV head g, split), a split being the 512 absolute
 // positions [512*sigma, 512*sigma + 512) -- four key tiles of 128 -- cut to the step's
-// window [max(0, pos-W+1), pos]. The CTA streams its tiles through a two-stage TMA ring
-// (K and V of a tile, 64 KB per stage, 128-B swizzle, slots 128*tau mod R). Per tile:
+// window [max(0, pos-W+1), pos]. Each key tile (K and V, 32 KB each, two 64-dim boxes with
+// 128-B swizzle, ring slots 128*tau mod R) arrives by TMA. Per tile:
 //   S^T = K Q'^T     tcgen05.mma M=128 keys, N=16 (the 4 query heads of the group, zero
-//                    padded), K=128 dims; A = K tile (K-major), B = Q' (K-major); TMEM,
-//                    double-buffered so the next tile's scores are computed during this
-//                    tile's softmax
+//                    padded), K=128 dims; A = K tile (K-major), B = Q' (K-major); TMEM
 //   softmax          512 threads: thread (head h, key k) holds one score; per head the
 //                    tile max and sum go through warp shuffles and the head's 4 warps
 //                    (fixed order); P^T -> smem (bf16)
 //   O^T = V^T P^T    tcgen05.mma M=128 dims, N=16, K=128 keys; A = V tile read as
 //                    MN-major (dims contiguous), B = P^T (K-major); TMEM
 //   fold             thread (head h, dim d) folds (m_t, l_t, O_t[h][d]) into registers.
+// Two pipelines compute the same bits:
+//   STAGES = 2 -- two K/V stages (one CTA per SM); the next tile's S^T is computed during
+//                 this tile's softmax (S^T double-buffered in TMEM). For small launches.
+//   STAGES = 1 -- one K/V stage (two CTAs per SM, so one CTA's prologue and merge overlap
+//                 the other's streaming); the next K is fetched as soon as S^T is done and
+//                 the next V as soon as O^T is done. For large launches.
 // The query heads are rotated in the prologue; if the split holds pos, the new key is
 // rotated too, patched into its tile row in shared memory, and stored (K', V) to ring slot
 // pos % R by this CTA. Each CTA writes its split's (m, l, o) per head; the last CTA of
 // (stream, g) folds the splits in ascending order and writes the output. Tiles and splits
 // are fixed by absolute position, so a stream's output is the same bits alone or in a
-// batch, and whatever the ring size.
+// batch, with either pipeline, and whatever the ring size.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "vst_internal.h"
@@ -39,17 +43,20 @@ constexpr int kD = 128;
 constexpr int kG = 4;                       // query heads per KV head
 constexpr int kTile = kDecTile;             // keys per tile
 constexpr int kTilesPerSplit = kDecSplit / kTile;
-constexpr int kMaxSplits = 32;              // merge register budget (S <= 32: W <= 15873)
 constexpr uint32_t kBox = 128u * 128u;      // 128 keys x 64 dims x 2 B
 constexpr uint32_t kStage = 4 * kBox;       // K lo, K hi, V lo, V hi
-constexpr uint32_t kOffQ = 2 * kStage;      // Q' [16 rows][128 dims]: 2 blocks of 2 KB
-constexpr uint32_t kOffP = kOffQ + 4096;    // P^T [16 rows][128 keys]: 2 blocks of 2 KB
-constexpr uint32_t kOffNew = kOffP + 4096;  // new K' row, new V row (bf16 x 128 each)
-constexpr uint32_t kOffRed = kOffNew + 512; // float [2][4 heads][4 warps]
-constexpr uint32_t kOffBar = kOffRed + 128;
-constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;
 constexpr uint32_t kTmemCols = 64;          // S^T buffers at [0,16) and [16,32); O^T at [32,48)
 constexpr uint32_t kTmO = 32;
+
+template <int STAGES>
+struct Layout {
+    static constexpr uint32_t kOffQ = STAGES * kStage;  // Q' [16 rows][128 dims]: 2 blocks of 2 KB
+    static constexpr uint32_t kOffP = kOffQ + 4096;     // P^T [16 rows][128 keys]: 2 blocks of 2 KB
+    static constexpr uint32_t kOffNew = kOffP + 4096;   // new K' row, new V row (bf16 x 128 each)
+    static constexpr uint32_t kOffRed = kOffNew + 512;  // float [2][4 heads][4 warps]
+    static constexpr uint32_t kOffBar = kOffRed + 128;  // 2*STAGES + 3 mbarriers
+    static constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;
+};
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 16, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 16, true, false);
@@ -96,27 +103,27 @@ __device__ __forceinline__ uint32_t sw16(int row, int col)
 
 }  // namespace
 
-template <int J>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int J, int STAGES>
+__global__ void __launch_bounds__(kThreads, 2)
     dec_step_kernel(const __grid_constant__ KParams<DecCommon, DecJob, J> p)
 {
+    using L = Layout<STAGES>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ int s_last;
-    __shared__ int s_fail;
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    uint8_t* sQ = smem + kOffQ;
-    uint8_t* sP = smem + kOffP;
-    __nv_bfloat16* snew = reinterpret_cast<__nv_bfloat16*>(smem + kOffNew);
-    float* red_m = reinterpret_cast<float*>(smem + kOffRed);  // [4 heads][4 warps]
+    uint8_t* sQ = smem + L::kOffQ;
+    uint8_t* sP = smem + L::kOffP;
+    __nv_bfloat16* snew = reinterpret_cast<__nv_bfloat16*>(smem + L::kOffNew);
+    float* red_m = reinterpret_cast<float*>(smem + L::kOffRed);  // [4 heads][4 warps]
     float* red_l = red_m + 16;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    const uint32_t bar_full0 = smem_u32(&bars[0]);
-    const uint32_t bar_full1 = smem_u32(&bars[1]);
-    const uint32_t bar_s0 = smem_u32(&bars[2]);
-    const uint32_t bar_s1 = smem_u32(&bars[3]);
-    const uint32_t bar_o = smem_u32(&bars[4]);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+    // bars: K landed [STAGES], V landed [STAGES], S^T done [2], O^T done
+    auto bar_k = [&](int st) { return smem_u32(&bars[st]); };
+    auto bar_v = [&](int st) { return smem_u32(&bars[STAGES + st]); };
+    auto bar_s = [&](int b) { return smem_u32(&bars[2 * STAGES + b]); };
+    const uint32_t bar_o = smem_u32(&bars[2 * STAGES + 2]);
 
     const DecCommon& c = p.c;
     const int item = blockIdx.x;
@@ -139,33 +146,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long tau_new = pos / kTile;  // tile holding this step's key
     const bool has_new = tau_new >= tau_lo && tau_new <= tau_hi;
 
-    auto issue_tile = [&](int i) {
-        const int st = i & 1;
-        const uint32_t base = smem_u32(smem) + st * kStage;
-        const uint32_t bar = st ? bar_full1 : bar_full0;
-        const int slot = (int)(((tau_lo + i) * kTile) % c.R);
-        mbar_arrive_expect_tx(bar, kStage);
-        tma_load_3d(base, job.tmap_k, bar, 0, slot, g);
-        tma_load_3d(base + kBox, job.tmap_k, bar, 64, slot, g);
-        tma_load_3d(base + 2 * kBox, job.tmap_v, bar, 0, slot, g);
-        tma_load_3d(base + 3 * kBox, job.tmap_v, bar, 64, slot, g);
+    auto stage_k = [&](int i) { return smem + (i % STAGES) * kStage; };
+    auto stage_v = [&](int i) { return smem + (i % STAGES) * kStage + 2 * kBox; };
+    auto parity = [&](int i) { return (uint32_t)((i / STAGES) & 1); };
+    auto slot_of = [&](int i) { return (int)(((tau_lo + i) * kTile) % c.R); };
+    auto issue_k = [&](int i) {
+        const uint32_t dst = smem_u32(stage_k(i));
+        mbar_arrive_expect_tx(bar_k(i % STAGES), 2 * kBox);
+        tma_load_3d(dst, job.tmap_k, bar_k(i % STAGES), 0, slot_of(i), g);
+        tma_load_3d(dst + kBox, job.tmap_k, bar_k(i % STAGES), 64, slot_of(i), g);
+    };
+    auto issue_v = [&](int i) {
+        const uint32_t dst = smem_u32(stage_v(i));
+        mbar_arrive_expect_tx(bar_v(i % STAGES), 2 * kBox);
+        tma_load_3d(dst, job.tmap_v, bar_v(i % STAGES), 0, slot_of(i), g);
+        tma_load_3d(dst + kBox, job.tmap_v, bar_v(i % STAGES), 64, slot_of(i), g);
+    };
+    auto issue_first = [&]() {
+        for (int i = 0; i < STAGES && i < n_tiles; ++i) {
+            issue_k(i);
+            issue_v(i);
+        }
     };
 
+    // Prologue. The first ring tiles may be requested before the previous kernel in the
+    // stream has finished when the host says that kernel did not touch this ring (early);
+    // everything else waits for it.
     if (tid == 0) {
-        s_fail = 0;
-        for (int b = 0; b < 5; ++b)
+        for (int b = 0; b < 2 * STAGES + 3; ++b)
             mbar_init(smem_u32(&bars[b]), 1);
         fence_mbar_init();
         tmap_acquire(job.tmap_k);
         tmap_acquire(job.tmap_v);
-        issue_tile(0);
-        if (n_tiles > 1)
-            issue_tile(1);
+        if (c.early)
+            issue_first();
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
         tmem_relinquish();
     }
+    griddep_wait();
+    if (tid == 0 && !c.early)
+        issue_first();
 
     // ---- Q' (4 rotated heads, bf16), the new K'/V row, zero padding rows 4..15
     if (tid < 256) {
@@ -201,24 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = s_tmem;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int rr_new = (int)(pos - tau_new * kTile);  // row of the new key in its tile
 
-    // Warp 0: wait for tile i's K/V, patch the new row in if it is there, and (thread 0)
-    // issue S^T for it into S buffer i & 1. Returns false if the wait gave up.
+    // Warp 0: wait for tile i's K, patch the new key in if it is there, and (lane 0) issue
+    // S^T for it into S buffer i & 1. Returns false if the wait gave up.
     auto prepare_and_issue_s = [&](int i) -> bool {
-        const int st = i & 1;
-        uint8_t* sK = smem + st * kStage;
-        bool ok = mbar_wait(st ? bar_full1 : bar_full0, (uint32_t)((i >> 1) & 1));
+        uint8_t* sK = stage_k(i);
+        bool ok = mbar_wait(bar_k(i % STAGES), parity(i));
         if (ok && has_new && tau_lo + i == tau_new && lane < 16) {
-            // chunk `lane` of the new 256-byte row: dims [8*lane, 8*lane+8)
-            const int rr = (int)(pos - tau_new * kTile);
-            const int half = lane >> 3, ch = lane & 7;
-            const uint4 kw = reinterpret_cast<const uint4*>(snew)[lane];
-            const uint4 vw = reinterpret_cast<const uint4*>(snew + kD)[lane];
-            *reinterpret_cast<uint4*>(sK + half * kBox + sw128_offset(rr, ch)) = kw;
-            *reinterpret_cast<uint4*>(sK + 2 * kBox + half * kBox + sw128_offset(rr, ch)) = vw;
-            const long long gofs = ((long long)g * c.R + pos % c.R) * kD + 8 * lane;
-            *reinterpret_cast<uint4*>(job.k_ring + gofs) = kw;
-            *reinterpret_cast<uint4*>(job.v_ring + gofs) = vw;
+            const uint4 kw = reinterpret_cast<const uint4*>(snew)[lane];  // dims [8 lane, 8 lane + 8)
+            *reinterpret_cast<uint4*>(sK + (lane >> 3) * kBox + sw128_offset(rr_new, lane & 7)) = kw;
+            *reinterpret_cast<uint4*>(job.k_ring + ((long long)g * c.R + pos % c.R) * kD + 8 * lane) = kw;
             fence_proxy_async_smem();
         }
         __syncwarp();
@@ -229,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t ad = smem_desc_sw128(smem_u32(sK) + (kk >> 2) * kBox + 32 * (kk & 3), 16, 1024);
                 const uint64_t bd = smem_desc_sw128(smem_u32(sQ) + (kk >> 2) * 2048 + 32 * (kk & 3), 16, 1024);
-                mma_bf16_ss(tmem + 16 * st, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+                mma_bf16_ss(tmem + 16 * (i & 1), ad, bd, kIdescS, kk > 0 ? 1u : 0u);
             }
-            mma_commit(st ? bar_s1 : bar_s0);
+            mma_commit(bar_s(i & 1));
         }
         return ok;
     };
@@ -240,33 +255,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY, l = 0.f, o = 0.f;
     int fail = 0, aborted = 0;
     uint32_t ph_o = 0;
-    int issued = n_tiles < 2 ? n_tiles : 2;  // tiles whose loads thread 0 has issued
-    int landed = 0;                         // tiles whose loads warp 0 has seen land
 
-    if (warp == 0) {
-        if (prepare_and_issue_s(0))
-            landed = 1;
-        else
-            fail = 1;
-    }
     for (int i = 0; i < n_tiles; ++i) {
-        const int st = i & 1;
-        // ---- S^T of tile i; warp 0 starts the next tile's S^T right away
+        // ---- S^T of tile i (two stages: already issued during the previous tile)
+        if (warp == 0 && (STAGES == 1 || i == 0) && !prepare_and_issue_s(i))
+            fail = 1;
         if (__syncthreads_or(fail)) {
             aborted = 1;
             break;
         }
-        if (!mbar_wait(st ? bar_s1 : bar_s0, (uint32_t)((i >> 1) & 1)))
+        if (!mbar_wait(bar_s(i & 1), (uint32_t)((i >> 1) & 1)))
             fail = 1;
         tc_fence_after();
-        if (warp == 0 && !fail && i + 1 < n_tiles) {
-            if (prepare_and_issue_s(i + 1))
-                landed = i + 2;
-            else
-                fail = 1;
+        if (STAGES == 1) {
+            if (tid == 0 && !fail && i + 1 < n_tiles)
+                issue_k(i + 1);  // the K buffer is free once S^T of tile i is done
+        } else if (warp == 0 && !fail && i + 1 < n_tiles && !prepare_and_issue_s(i + 1)) {
+            fail = 1;
         }
         uint32_t sv[4];
-        tmem_ld_32x32b_x4(tmem + lane_base + 16 * st, sv);
+        tmem_ld_32x32b_x4(tmem + lane_base + 16 * (i & 1), sv);
         tmem_ld_wait();
 
         // ---- softmax of head hh over the tile's 128 keys (thread: key `row`)
@@ -283,6 +291,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float ws = warp_sum(pv);
         if (lane == 0)
             red_l[hh * 4 + (warp & 3)] = ws;
+
+        // ---- V of tile i (new value patched in), then O^T = V^T P^T
+        uint8_t* sV = stage_v(i);
+        if (!mbar_wait(bar_v(i % STAGES), parity(i)))
+            fail = 1;
+        if (!fail && has_new && tau_lo + i == tau_new && tid < 16) {
+            const uint4 vw = reinterpret_cast<const uint4*>(snew + kD)[tid];
+            *reinterpret_cast<uint4*>(sV + (tid >> 3) * kBox + sw128_offset(rr_new, tid & 7)) = vw;
+            *reinterpret_cast<uint4*>(job.v_ring + ((long long)g * c.R + pos % c.R) * kD + 8 * tid) = vw;
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         if (__syncthreads_or(fail)) {
@@ -291,10 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const float lt = __fadd_rn(__fadd_rn(red_l[hh * 4], red_l[hh * 4 + 1]), __fadd_rn(red_l[hh * 4 + 2], red_l[hh * 4 + 3]));
-
-        // ---- O^T = V^T P^T; afterwards the stage is free for tile i + 2
         if (tid == 0) {
-            uint8_t* sV = smem + st * kStage + 2 * kBox;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t ad = smem_desc_sw128(smem_u32(sV) + 2048 * kk, kBox, 1024);
@@ -307,9 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             fail = 1;
         ph_o ^= 1;
         tc_fence_after();
-        if (tid == 0 && !fail && i + 2 < n_tiles) {
-            issue_tile(i + 2);
-            issued = i + 3;
+        if (tid == 0 && !fail) {
+            if (STAGES == 1 && i + 1 < n_tiles)
+                issue_v(i + 1);  // the V buffer is free once O^T of tile i is done
+            else if (STAGES == 2 && i + 2 < n_tiles) {
+                issue_k(i + 2);  // the whole stage is free
+                issue_v(i + 2);
+            }
         }
         uint32_t ov[4];
         tmem_ld_32x32b_x4(tmem + lane_base + kTmO, ov);
@@ -318,12 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
     }
 
+    griddep_launch_dependents();
     if (aborted) {
         if (tid == 0) {
-            // A bounded wait gave up: record it, let copies still in flight land, release TMEM.
+            // A bounded wait gave up: record it, give copies in flight a bounded chance to
+            // land, release TMEM and leave.
             atomicExch(job.err, kErrTimeout);
-            for (int k = landed; k < issued; ++k)
-                mbar_wait((k & 1) ? bar_full1 : bar_full0, (uint32_t)((k >> 1) & 1));
+            for (int st = 0; st < STAGES; ++st) {
+                mbar_wait(bar_k(st), 0);
+                mbar_wait(bar_v(st), 0);
+            }
         }
     } else {
         // ---- this split's partial; the last CTA of (stream, g) folds all splits in order
@@ -342,19 +365,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             __threadfence();
             const float* pml = job.part_ml + (long long)hq * c.S * 2;
             const float* po = job.part_o + (long long)hq * c.S * kD + row;
-            float2 ml[kMaxSplits];
-            float ov[kMaxSplits];
-#pragma unroll
-            for (int u = 0; u < kMaxSplits; ++u)
-                if (u < job.n_splits) {
-                    ml[u] = __ldcg(reinterpret_cast<const float2*>(pml + u * 2));
-                    ov[u] = __ldcg(po + (long long)u * kD);
-                }
             float mm = -INFINITY, ll = 0.f, oo = 0.f;
+            for (int u0 = 0; u0 < job.n_splits; u0 += 8) {  // loads of 8 splits in flight at once
+                float2 ml[8];
+                float ov[8];
 #pragma unroll
-            for (int u = 0; u < kMaxSplits; ++u)
-                if (u < job.n_splits)
-                    fold1(mm, ll, oo, ml[u].x, ml[u].y, ov[u]);
+                for (int u = 0; u < 8; ++u)
+                    if (u0 + u < job.n_splits) {
+                        ml[u] = __ldcg(reinterpret_cast<const float2*>(pml + (u0 + u) * 2));
+                        ov[u] = __ldcg(po + (long long)(u0 + u) * kD);
+                    }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (u0 + u < job.n_splits)
+                        fold1(mm, ll, oo, ml[u].x, ml[u].y, ov[u]);
+            }
             job.out[(long long)hq * kD + row] = __float2bfloat16_rn(__fdiv_rn(oo, ll));
             if (tid == 0)
                 job.counters[g] = 0u;
@@ -368,22 +393,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int J>
+template <int J, int STAGES>
 static cudaError_t launch_dec_j(const KParams<DecCommon, DecJob, J>& p, int total_work, cudaStream_t s)
 {
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
+    const uint32_t smem = Layout<STAGES>::kSmemBytes;
     if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(dec_step_kernel<J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(dec_step_kernel<J, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
         if (e != cudaSuccess)
             return e;
         configured[dev] = 1;
     }
     const dim3 grid((unsigned)total_work, (unsigned)p.c.Hk);
-    dec_step_kernel<J><<<grid, kThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(dec_step_kernel<J, STAGES>, grid, dim3(kThreads), smem, s, p);
 }
 
 cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, int total_work,
@@ -391,10 +416,15 @@ cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, 
 {
     if (n_jobs == 0 || total_work == 0)
         return cudaSuccess;
-    if (c.S > kMaxSplits)
-        return cudaErrorInvalidValue;
+    // one CTA per SM with two stages while the launch fits in one wave; beyond that two
+    // CTAs per SM with one stage each
+    int dev = 0, n_sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool big = (long long)total_work * c.Hk > n_sms;
     return with_params(c, jobs, n_jobs, [&](const auto& p) {
-        return launch_dec_j<sizeof(p.jobs) / sizeof(p.jobs[0])>(p, total_work, s);
+        constexpr int J = sizeof(p.jobs) / sizeof(p.jobs[0]);
+        return big ? launch_dec_j<J, 1>(p, total_work, s) : launch_dec_j<J, 2>(p, total_work, s);
     });
 }
 

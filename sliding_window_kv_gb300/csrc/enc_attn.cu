@@ -211,6 +211,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.r = 32 * (s.warp & 3) + (s.tid & 31);  // TMEM lane = query row of this thread
     s.q = s.warp >> 2;                       // quarter of the row
 
+    // Prologue. The first ring tiles may be requested before the previous kernel in the
+    // stream has finished when the host says that kernel did not touch this ring (early);
+    // everything else waits for it.
+    auto issue_first_tile = [&]() {
+        const int slot = (int)(t_begin * 128 - job.abs_base);
+        mbar_arrive_expect_tx(s.bar_k, kTileBytes);
+        tma_load_3d(smem_u32(s.sK), job.tmap_k, s.bar_k, 0, slot, h);
+        mbar_arrive_expect_tx(s.bar_v, kTileBytes);
+        tma_load_3d(smem_u32(s.sV), job.tmap_v, s.bar_v, 0, slot, h);
+    };
     if (s.tid == 0) {
         mbar_init(s.bar_k, 1);
         mbar_init(s.bar_v, 1);
@@ -218,16 +228,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         tmap_acquire(job.tmap_k);
         tmap_acquire(job.tmap_v);
-        const int slot = (int)(t_begin * 128 - job.abs_base);
-        mbar_arrive_expect_tx(s.bar_k, kTileBytes);
-        tma_load_3d(smem_u32(s.sK), job.tmap_k, s.bar_k, 0, slot, h);
-        mbar_arrive_expect_tx(s.bar_v, kTileBytes);
-        tma_load_3d(smem_u32(s.sV), job.tmap_v, s.bar_v, 0, slot, h);
+        if (c.early)
+            issue_first_tile();
     }
     if (s.warp == 0) {
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
         tmem_relinquish();
     }
+    griddep_wait();
+    if (s.tid == 0 && !c.early)
+        issue_first_tile();
 
     // ---- this thread's quarter of query row r, rotated, into sQ
     const int r = s.r;
@@ -377,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
     }
 
+    griddep_launch_dependents();
     if (aborted) {
         if (s.tid == 0) {
             // A bounded wait gave up: record it, let copies still in flight land, then release
@@ -456,8 +467,7 @@ static cudaError_t launch_enc_attn_j(const KParams<EncAttnCommon, EncAttnJob, J>
         configured[dev] = 1;
     }
     const dim3 grid((unsigned)grid_x, (unsigned)p.c.H, (unsigned)n_jobs);
-    enc_attn_kernel<J><<<grid, kThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(enc_attn_kernel<J>, grid, dim3(kThreads), kSmemBytes, s, p);
 }
 
 cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int n_jobs, int grid_x, cudaStream_t s)

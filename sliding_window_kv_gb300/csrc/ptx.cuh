@@ -215,6 +215,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
            | ((uint32_t)(M >> 4) << 24);            // M / 16
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Wait until the grid this launch depends on (the previous kernel in the stream) has
+// completed and its memory is visible. A no-op when the launch has no such dependency.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel in the stream start launching (its pre-wait prologue may then overlap
+// the rest of this grid).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- math
 
 // Hardware base-2 exponential (ex2.approx, flush-to-zero); ex2(-inf) = +0.

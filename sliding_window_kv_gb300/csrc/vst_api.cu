@@ -15,6 +15,7 @@
 #include <atomic>
 #include <mutex>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "vst_internal.h"
@@ -217,6 +218,30 @@ cudaError_t tracked(int kid, cudaStream_t s, F&& f)
 }
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// ---- programmatic dependent launch bookkeeping
+// The contexts the most recent kernel of this library touched, per stream. A chunk
+// attention or decode launch may request ring tiles before the previous kernel in the
+// stream has finished only if that kernel touched none of its contexts (it cannot then be
+// writing those rings). Any other producer in between -- a kernel of the caller, a memset
+// -- starts only after our earlier kernels complete, so it cannot open a race.
+std::mutex g_touch_mu;
+std::unordered_map<cudaStream_t, std::vector<const vst_ctx*>> g_last_touch;
+
+// Record that the next launch on s touches ctxs[0..n) and return whether it may start its
+// ring loads early.
+int record_touch(cudaStream_t s, const vst_ctx* const* ctxs, int n)
+{
+    std::lock_guard<std::mutex> lk(g_touch_mu);
+    std::vector<const vst_ctx*>& prev = g_last_touch[s];
+    int early = 1;
+    for (const vst_ctx* p : prev)
+        for (int i = 0; i < n && early; ++i)
+            if (p == ctxs[i])
+                early = 0;
+    prev.assign(ctxs, ctxs + n);
+    return early;
+}
 
 // Zero the error word, counters and both rings (not the tensor maps).
 cudaError_t clear_ctx(vst_ctx* c, cudaStream_t s)
@@ -591,9 +616,10 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
     auto* ob = static_cast<__nv_bfloat16*>(out);
 
     const CompactCommon cc{Hk, cfg.ring_slots, D, cfg.window};
-    const EncAttnCommon ec{m->rope, 0, H, cfg.window, cfg.ring_slots, 0, m->splits,
+    const EncAttnCommon ec{m->rope, 0, H, cfg.window, cfg.ring_slots, 0, m->splits, 0,
                            (float)(1.4426950408889634 / std::sqrt((double)D))};
     CompactJob cj[kMaxJobs];
+    const vst_ctx* cctx[kMaxJobs];
     EncAttnJob ej[kMaxJobs];
 
     for (int32_t off = 0; off < n_new;) {
@@ -606,14 +632,18 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
                 vst_ctx* c = ctxs[c0 + i];
                 if (c->n_kv + b > cfg.ring_slots) {
                     const int64_t keep = c->n_kv < cfg.window ? c->n_kv : cfg.window;
+                    cctx[ncj] = c;
                     cj[ncj++] = CompactJob{c->k_ring, c->v_ring, c->n_kv - keep};
                     c->abs_base += c->n_kv - keep;
                     c->n_kv = keep;
                     c->n_compactions += 1;
                 }
             }
-            if (ncj > 0 && tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc, cj, ncj, s); }) != cudaSuccess)
-                return fail_all(ctxs, n_ctx);
+            if (ncj > 0) {
+                record_touch(s, cctx, ncj);
+                if (tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc, cj, ncj, s); }) != cudaSuccess)
+                    return fail_all(ctxs, n_ctx);
+            }
             // Launch shape: one CTA per (ctx, head, query tile) when that fills the GPU;
             // otherwise (a single query tile) one CTA per (ctx, head, group of key tiles),
             // with groups just large enough that every CTA starts in the first wave (one
@@ -643,6 +673,7 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
             EncAttnCommon e2 = ec;
             e2.n_rows = b;
             e2.split = per_cta;
+            e2.early = record_touch(s, ctxs + c0, nj);
             if (tracked(VST_K_ENC_ATTN, s, [&] { return launch_enc_attn(e2, ej, nj, grid_x, s); }) != cudaSuccess)
                 return fail_all(ctxs, n_ctx);
             for (int i = 0; i < nj; ++i) {
@@ -674,6 +705,7 @@ vst_status vst_ctx_compact(vst_ctx* c, void* stream)
     const CompactCommon cc{cfg.n_kv_heads, cfg.ring_slots, cfg.head_dim, cfg.window};
     const CompactJob cj{c->k_ring, c->v_ring, c->n_kv - cfg.window};
     cudaStream_t s = as_stream(stream);
+    record_touch(s, cs, 1);
     if (tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc, &cj, 1, s); }) != cudaSuccess)
         return fail_all(cs, 1);
     c->abs_base += c->n_kv - cfg.window;
@@ -704,7 +736,7 @@ vst_status vst_dec_step(vst_ctx* const* ctxs, int32_t n_streams, const void* q, 
     const auto* kb = static_cast<const __nv_bfloat16*>(k);
     const auto* vb = static_cast<const __nv_bfloat16*>(v);
     auto* ob = static_cast<__nv_bfloat16*>(out);
-    const DecCommon dc0{m->rope, 0, Hk, cfg.ring_slots, cfg.window, m->splits,
+    const DecCommon dc0{m->rope, 0, Hk, cfg.ring_slots, cfg.window, m->splits, 0,
                         (float)(1.4426950408889634 / std::sqrt((double)D))};
     DecJob jobs[kMaxJobs];
     for (int c0 = 0; c0 < n_streams; c0 += kMaxJobs) {
@@ -724,6 +756,7 @@ vst_status vst_dec_step(vst_ctx* const* ctxs, int32_t n_streams, const void* q, 
         }
         DecCommon dc = dc0;
         dc.n_jobs = nj;
+        dc.early = record_touch(s, ctxs + c0, nj);
         if (tracked(VST_K_DEC_STEP, s, [&] { return launch_dec_step(dc, jobs, nj, work, s); }) != cudaSuccess)
             return fail_all(ctxs, n_streams);
         for (int i = 0; i < nj; ++i)
@@ -758,6 +791,7 @@ vst_status vst_dec_append(vst_ctx* c, const void* k, const void* v, int32_t n, v
         const AppendJob aj{kb + (long long)off * Hk * D, vb + (long long)off * Hk * D, c->k_ring, c->v_ring,
                            c->abs_next, 0};
         cudaStream_t s = as_stream(stream);
+        record_touch(s, cs, 1);
         if (tracked(VST_K_ROPE_APPEND, s, [&] { return launch_rope_append(ac, &aj, 1, s); }) != cudaSuccess)
             return fail_all(cs, 1);
         c->abs_next += rows;
@@ -834,7 +868,7 @@ vst_status vst_dec_step_noalloc(vst_ctx* const* ctxs, int32_t n_streams, const v
     const auto* kb = static_cast<const __nv_bfloat16*>(k);
     const auto* vb = static_cast<const __nv_bfloat16*>(v);
     auto* ob = static_cast<__nv_bfloat16*>(out);
-    DecCommon dc{m->rope, n_streams, Hk, cfg.ring_slots, cfg.window, m->splits,
+    DecCommon dc{m->rope, n_streams, Hk, cfg.ring_slots, cfg.window, m->splits, 0,
                  (float)(1.4426950408889634 / std::sqrt((double)D))};
     DecJob jobs[kMaxJobs];
     int work = 0;
@@ -856,6 +890,7 @@ vst_status vst_dec_step_noalloc(vst_ctx* const* ctxs, int32_t n_streams, const v
     for (int i = 0; i < n_streams; ++i)
         if (cudaMemsetAsync(scratch + (size_t)i * per_stream + ml_bytes + o_bytes, 0, cnt_bytes, s) != cudaSuccess)
             return fail_all(ctxs, n_streams);
+    record_touch(s, ctxs, n_streams);  // dc.early stays 0: this launch follows the memsets
     if (launch_dec_step(dc, jobs, n_streams, work, s) != cudaSuccess)
         return fail_all(ctxs, n_streams);
     g_launches.fetch_add(1, std::memory_order_relaxed);

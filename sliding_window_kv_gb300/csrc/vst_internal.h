@@ -86,6 +86,7 @@ struct EncAttnCommon {
     int n_rows, H, W, R;
     int split;               // 0: loop mode; k > 0: split mode, k key tiles per CTA
     int split_tiles;         // scratch tiles per head
+    int early;               // 1: ring loads may start before the previous kernel completes
     float scale_log2;        // log2(e) / sqrt(D)
 };
 
@@ -112,6 +113,7 @@ struct DecJob {
 struct DecCommon {
     const float2* rope;
     int n_jobs, Hk, R, W, S;
+    int early;               // 1: ring loads may start before the previous kernel completes
     float scale_log2;
 };
 
@@ -134,6 +136,26 @@ cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int 
                             cudaStream_t s);
 cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, int total_work,
                             cudaStream_t s);
+
+// Launch with programmatic stream serialization: the kernel may start while the previous
+// kernel in the stream is finishing; it runs griddep_wait() before touching anything that
+// kernel may produce or consume.
+template <class Kernel, class Params>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Params& p)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 // Copy jobs into a KParams<J> with the smallest J in {1, 8, 64} that fits and call
 // f(params) with it.

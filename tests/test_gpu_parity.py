@@ -343,3 +343,44 @@ def test_dec_append_ring_contents(dev, dec_module):
     assert torch.equal(ctx.v_ring, ctx2.v_ring)
     ctx.close()
     ctx2.close()
+
+
+def test_interleaved_contexts_bit_exact(dev, enc_module, dec_module):
+    """Layers of a stream are different contexts called one after another on one CUDA
+    stream; a launch may then fetch its ring tiles while the previous kernel (another
+    context) is still running. Feeding three encoder contexts and three decoder contexts
+    round-robin must give the same bits as running each context alone."""
+    # encoder: 3 contexts, 900 frames each, alternating 50-frame feeds with one 300-frame feed
+    ins = [_enc_inputs(31, l, 900) for l in range(3)]
+    alone = [_feed(enc_module, *ins[l], [50] * 6 + [300] + [50] * 6)[0] for l in range(3)]
+    ctxs = [vst.Ctx(enc_module) for _ in range(3)]
+    outs = [torch.empty_like(ins[l][0], device=dev) for l in range(3)]
+    dins = [[t.to(dev) for t in ins[l]] for l in range(3)]
+    t = 0
+    for n in [50] * 6 + [300] + [50] * 6:
+        for l in range(3):
+            q, k, v = dins[l]
+            vst.enc_feed(ctxs[l].handle, q[t:t + n], k[t:t + n], v[t:t + n], outs[l][t:t + n])
+        t += n
+    torch.cuda.synchronize()
+    for l in range(3):
+        assert torch.equal(outs[l], alone[l]), l
+        ctxs[l].close()
+    # decoder: 3 contexts with different fills, 6 steps round-robin
+    fills = [100, 8190, 9001]
+    seqs = [_dec_seq(32, s, 0, f + 6) for s, f in enumerate(fills)]
+    alone = [_run_dec(dec_module, *seqs[s], fill=f, steps=6) for s, f in enumerate(fills)]
+    dctx = [vst.Ctx(dec_module) for _ in fills]
+    for c, (q, k, v), f in zip(dctx, seqs, fills):
+        vst.dec_append(c.handle, k[:f].to(dev), v[:f].to(dev))
+    got = [torch.empty((6, 32, 128), dtype=torch.bfloat16, device=dev) for _ in fills]
+    dseq = [[x.to(dev) for x in sq] for sq in seqs]
+    for st in range(6):
+        for s, f in enumerate(fills):
+            q, k, v = dseq[s]
+            vst.dec_step([dctx[s].handle], q[f + st:f + st + 1], k[f + st:f + st + 1], v[f + st:f + st + 1],
+                         got[s][st:st + 1])
+    torch.cuda.synchronize()
+    for s in range(3):
+        assert torch.equal(got[s], alone[s]), s
+        dctx[s].close()
