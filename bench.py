@@ -421,14 +421,27 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def dram_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it is current."""
+KERNEL_SOURCES = {"enc_attn_kernel": "enc_attn.cu", "dec_step_kernel": "dec_step.cu", "compact_kernel": "compact.cu"}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    import hashlib
+    src = os.path.join(ROOT, "sliding_window_kv_gb300", "csrc", KERNEL_SOURCES[kernel])
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def dram_traffic(kernel: str, units_per_launch: float):
+    """DRAM bytes (read + write) per launch from the committed ncu capture, scaled from the
+    captured case to this launch by the work units it processes; None when there is no
+    capture or the kernel's source changed since it was taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
-        d = json.load(open(p))
-        return d.get(kernel)
+        d = json.load(open(p)).get(kernel)
+        if not d or d.get("source_sha") != kernel_source_sha(kernel):
+            return None
+        return d["dram_bytes_per_unit"] * units_per_launch
     except Exception:
         return None
 
@@ -552,7 +565,8 @@ def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu):
     out = {"value": steps_per_s, "unit": "dec steps/s", "config": workload_config("", spec),
            "ms_per_step": ms / w.steps, "gpu_launches": launches,
            "roofline": {"kernel": "dec_step_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm,
-                        "unit": "GB/s", "frac": achieved / hbm, "traffic": dram_traffic("dec_step_kernel"),
+                        "unit": "GB/s", "frac": achieved / hbm,
+                        "traffic": dram_traffic("dec_step_kernel", bytes_per_launch),
                         "peak_source": src, "launches": nl, "avg_launch_us": 1e3 * kms / nl,
                         "algorithmic_bytes_per_launch": bytes_per_launch}}
     if want_cpu:
@@ -622,7 +636,8 @@ def run_vst(args, dist):
         line.update({"value": value, "unit": "enc frames/s", "ms_per_step": ms / args.steps,
                      "config": workload_config(args.workload, spec),
                      "roofline": {"kernel": "enc_attn_kernel", "bound": "tensor", "achieved": achieved, "peak": tf,
-                                  "unit": "TFLOP/s", "frac": achieved / tf, "traffic": dram_traffic("enc_attn_kernel"),
+                                  "unit": "TFLOP/s", "frac": achieved / tf,
+                                  "traffic": dram_traffic("enc_attn_kernel", flops_per_launch),
                                   "peak_source": src + " bf16 burst", "launches": nl,
                                   "avg_launch_us": 1e3 * kms / nl, "algorithmic_flops_per_launch": flops_per_launch},
                      "kernels": {k: {"launches": v[0], "total_ms": v[1]} for k, v in prof.items() if v[0]},
