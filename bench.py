@@ -421,13 +421,17 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-KERNEL_SOURCES = {"enc_attn_kernel": "enc_attn.cu", "dec_step_kernel": "dec_step.cu", "compact_kernel": "compact.cu"}
+# sources of each profiled kernel id (the encoder attention id covers all its launch shapes)
+KERNEL_SOURCES = {"enc_attn_kernel": ("enc_attn.cu", "enc_common.cuh"),
+                  "dec_step_kernel": ("dec_step.cu",), "compact_kernel": ("compact.cu",)}
 
 
 def kernel_source_sha(kernel: str) -> str:
     import hashlib
-    src = os.path.join(ROOT, "sliding_window_kv_gb300", "csrc", KERNEL_SOURCES[kernel])
-    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "sliding_window_kv_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def dram_traffic(kernel: str, units_per_launch: float):

@@ -37,6 +37,7 @@
 // depends only on its own window -- never on how the stream was cut into feeds, on when
 // the ring was compacted, or on the launch shape.
 #include "common.cuh"
+#include "enc_common.cuh"
 #include "ptx.cuh"
 #include "vst_internal.h"
 
@@ -62,41 +63,10 @@ constexpr uint32_t kTmO = 128;  // O tile: columns [128, 192)
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64, false, true);
 
-// The one fold used by both launch shapes (and so the reason they agree bit for bit):
-// merge the tile-local softmax state (mt, lt, ot) into the running state (m, l, o).
-__device__ __forceinline__ void fold_tile(float& m, float& l, float* o, float mt, float lt, const float* ot)
-{
-    const float mn = fmaxf(m, mt);
-    const float a = ex2(__fsub_rn(m, mn));
-    const float b = ex2(__fsub_rn(mt, mn));
-    l = __fmaf_rn(l, a, __fmul_rn(lt, b));
-#pragma unroll
-    for (int d = 0; d < kDq; ++d)
-        o[d] = __fmaf_rn(o[d], a, __fmul_rn(ot[d], b));
-    m = mn;
-}
-
-// Rotate pairs [8q, 8q+8) of a 64-value head row (NEOX: element i pairs with i + 32) at the
-// angle table row cs, and write them as chunks q and 4 + q of a swizzled 128-byte row.
-__device__ __forceinline__ void rotate_quarter(const __nv_bfloat16* src, const float2* cs, uint8_t* tile, int row,
-                                               int q)
-{
-    const uint4 a = *reinterpret_cast<const uint4*>(src + 8 * q);
-    const uint4 b = *reinterpret_cast<const uint4*>(src + 32 + 8 * q);
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-    uint32_t ya[4], yb[4];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        float y1a, y2a, y1b, y2b;
-        rope_pair(bf16lo(aw[w]), bf16lo(bw[w]), cs[8 * q + 2 * w], y1a, y2a);
-        rope_pair(bf16hi(aw[w]), bf16hi(bw[w]), cs[8 * q + 2 * w + 1], y1b, y2b);
-        ya[w] = pack_bf16(y1a, y1b);
-        yb[w] = pack_bf16(y2a, y2b);
-    }
-    *reinterpret_cast<uint4*>(tile + sw128_offset(row, q)) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-    *reinterpret_cast<uint4*>(tile + sw128_offset(row, 4 + q)) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
-}
+using enc::fold_tile;
+using enc::quarter_exp;
+using enc::quarter_max;
+using enc::rotate_quarter;
 
 struct Cta {
     uint8_t *sQ, *sK, *sV, *sP;
@@ -156,16 +126,6 @@ __device__ __forceinline__ void issue_o_mma(const Cta& s)
         mma_bf16_ss(s.tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
     }
     mma_commit(s.bar_m);
-}
-
-__device__ __forceinline__ void store_out_quarter(__nv_bfloat16* orow, const float* o, float l, int q)
-{
-    uint32_t w[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-        w[e] = pack_bf16(__fdiv_rn(o[2 * e], l), __fdiv_rn(o[2 * e + 1], l));
-    *reinterpret_cast<uint4*>(orow + kDq * q) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(orow + kDq * q + 8) = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 }  // namespace
@@ -300,35 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             hi = (int)max(-1LL, min(128LL, pq - kbase));
         }
         const int c0 = 32 * s.q;
-        const bool full = lo <= c0 && hi >= c0 + 31;
         uint32_t sv[32];
         tmem_ld_32x32b_x32(s.tmem + s.lane_base + kTmS + c0, sv);
         tmem_ld_wait();
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (full || (c0 + j >= lo && c0 + j <= hi))
-                m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(sv[j]));
-        s.red_m[s.q * 128 + r] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        s.red_m[s.q * 128 + r] = quarter_max(sv, c0, lo, hi);
         __syncthreads();
         const float mraw = fmaxf(fmaxf(s.red_m[r], s.red_m[128 + r]), fmaxf(s.red_m[256 + r], s.red_m[384 + r]));
         const float mt = __fmul_rn(mraw, c.scale_log2);  // -inf when the row sees nothing here
-        const float neg = -mt;
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
-        float pv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const bool ok = full || (c0 + j >= lo && c0 + j <= hi);
-            pv[j] = ok ? ex2(__fmaf_rn(__uint_as_float(sv[j]), c.scale_log2, neg)) : 0.f;
-            l4[j & 3] = __fadd_rn(l4[j & 3], pv[j]);
-        }
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {
-            const uint4 w = make_uint4(pack_bf16(pv[8 * qd + 0], pv[8 * qd + 1]), pack_bf16(pv[8 * qd + 2], pv[8 * qd + 3]),
-                                       pack_bf16(pv[8 * qd + 4], pv[8 * qd + 5]), pack_bf16(pv[8 * qd + 6], pv[8 * qd + 7]));
-            *reinterpret_cast<uint4*>(s.sP + (s.q >> 1) * kTileBytes + sw128_offset(r, (s.q & 1) * 4 + qd)) = w;
-        }
-        s.red_l[s.q * 128 + r] = __fadd_rn(__fadd_rn(l4[0], l4[1]), __fadd_rn(l4[2], l4[3]));
+        s.red_l[s.q * 128 + r] = quarter_exp(sv, c0, lo, hi, c.scale_log2, -mt, s.sP, r);
 
         // ---- V of tile t in smem (new rows patched in), then O_t = P V
         if (!mbar_wait(s.bar_v, ph_v))
@@ -377,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (s.q == 0)
                 *reinterpret_cast<float2*>(job.part_ml + (slot_t * 128 + r) * 2) = make_float2(mt, lt);
         } else if (mt != -INFINITY) {
-            fold_tile(m_run, l_run, o, mt, lt, ot);
+            fold_tile<kDq>(m_run, l_run, o, mt, lt, ot);
         }
         tc_fence_before();
         if (__syncthreads_or(fail)) {
@@ -400,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (!split) {
         if (r < nrows)
-            store_out_quarter(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, s.q);
+            enc::store_out<kDq>(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, kDq * s.q);
     } else {
         // split mode: the last CTA of (job, head) folds all tiles in ascending order
         __threadfence();
@@ -436,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         x3 = __ldcg(reinterpret_cast<const float4*>(po + step * kD + 12));
                     }
                     if (cml.x != -INFINITY)
-                        fold_tile(m_run, l_run, o, cml.x, cml.y, ot);
+                        fold_tile<kDq>(m_run, l_run, o, cml.x, cml.y, ot);
                 }
-                store_out_quarter(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, s.q);
+                enc::store_out<kDq>(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, kDq * s.q);
             }
             if (s.tid == 0)
                 job.counters[h] = 0u;

@@ -1,0 +1,132 @@
+// enc_common.cuh -- the per-row arithmetic of the chunk attention, shared by every launch
+// shape of it (enc_attn.cu, enc_attn_pair.cu). Each shape splits a 128-column score row
+// over a different number of threads, but all of them call these functions on the same
+// 32-column quarters in the same order, so every shape produces the same bits.
+//
+// Row softmax of one 128-key tile, for a row whose visible columns are [lo, hi]:
+//   quarter max    max over the quarter's visible columns (4 interleaved partial maxima)
+//   row max        max of the 4 quarter maxima (exact in any order), m_t = max * log2e/sqrt(D)
+//   quarter sum    p = 2^(s * log2e/sqrt(D) - m_t) over the quarter (0 where not visible),
+//                  accumulated into 4 interleaved partial sums, combined (l0+l1)+(l2+l3)
+//   row sum        l_t = (Q0 + Q1) + (Q2 + Q3)
+#pragma once
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace vst {
+namespace enc {
+
+constexpr int kD = 64;
+constexpr uint32_t kTileBytes = 128u * 128u;  // 128 rows x 128 B
+
+// Max over the visible columns of the quarter [c0, c0 + 32) held in sv.
+__device__ __forceinline__ float quarter_max(const uint32_t (&sv)[32], int c0, int lo, int hi)
+{
+    const bool full = lo <= c0 && hi >= c0 + 31;
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (full || (c0 + j >= lo && c0 + j <= hi))
+            m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(sv[j]));
+    return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+
+// Probabilities of the quarter [c0, c0 + 32) of row `row` (neg = -m_t): written as bf16
+// into the K-major P operand (two 64-key blocks, 128-B swizzle); returns the quarter sum.
+// Columns are taken in ascending order, eight at a time.
+__device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], int c0, int lo, int hi, float scale_log2,
+                                             float neg, uint8_t* sP, int row)
+{
+    const bool full = lo <= c0 && hi >= c0 + 31;
+    float l4[4] = {0.f, 0.f, 0.f, 0.f};
+    const int q = c0 >> 5;
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+        float pv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int j = 8 * qd + e;
+            const bool ok = full || (c0 + j >= lo && c0 + j <= hi);
+            pv[e] = ok ? ex2(__fmaf_rn(__uint_as_float(sv[j]), scale_log2, neg)) : 0.f;
+            l4[j & 3] = __fadd_rn(l4[j & 3], pv[e]);
+        }
+        const uint4 w = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
+                                   pack_bf16(pv[6], pv[7]));
+        *reinterpret_cast<uint4*>(sP + (q >> 1) * kTileBytes + sw128_offset(row, (q & 1) * 4 + qd)) = w;
+    }
+    return __fadd_rn(__fadd_rn(l4[0], l4[1]), __fadd_rn(l4[2], l4[3]));
+}
+
+// Merge of a tile-local softmax state (mt, lt, ot) into a running state (m, l, o):
+//   mn = max(m, mt), a = 2^(m - mn), b = 2^(mt - mn), l <- l a + lt b, o <- o a + ot b.
+struct FoldCoef {
+    float a, b, mn;
+};
+
+__device__ __forceinline__ FoldCoef fold_coef(float m, float mt)
+{
+    const float mn = fmaxf(m, mt);
+    return FoldCoef{ex2(__fsub_rn(m, mn)), ex2(__fsub_rn(mt, mn)), mn};
+}
+
+// o <- o a + ot b for N dims (the same element-wise operations for any split of the dims).
+template <int N>
+__device__ __forceinline__ void fold_apply(float* o, const float* ot, const FoldCoef& f)
+{
+#pragma unroll
+    for (int d = 0; d < N; ++d)
+        o[d] = __fmaf_rn(o[d], f.a, __fmul_rn(ot[d], f.b));
+}
+
+__device__ __forceinline__ void fold_finish(float& m, float& l, float lt, const FoldCoef& f)
+{
+    l = __fmaf_rn(l, f.a, __fmul_rn(lt, f.b));
+    m = f.mn;
+}
+
+template <int N>
+__device__ __forceinline__ void fold_tile(float& m, float& l, float* o, float mt, float lt, const float* ot)
+{
+    const FoldCoef f = fold_coef(m, mt);
+    fold_apply<N>(o, ot, f);
+    fold_finish(m, l, lt, f);
+}
+
+// Rotate pairs [8q, 8q+8) of a 64-value head row (NEOX: element i pairs with i + 32) at the
+// angle table row cs, and write them as chunks q and 4 + q of a swizzled 128-byte row.
+__device__ __forceinline__ void rotate_quarter(const __nv_bfloat16* src, const float2* cs, uint8_t* tile, int row,
+                                               int q)
+{
+    const uint4 a = *reinterpret_cast<const uint4*>(src + 8 * q);
+    const uint4 b = *reinterpret_cast<const uint4*>(src + 32 + 8 * q);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+    uint32_t ya[4], yb[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float y1a, y2a, y1b, y2b;
+        rope_pair(bf16lo(aw[w]), bf16lo(bw[w]), cs[8 * q + 2 * w], y1a, y2a);
+        rope_pair(bf16hi(aw[w]), bf16hi(bw[w]), cs[8 * q + 2 * w + 1], y1b, y2b);
+        ya[w] = pack_bf16(y1a, y1b);
+        yb[w] = pack_bf16(y2a, y2b);
+    }
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, q)) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, 4 + q)) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+}
+
+// Store N consecutive output dims starting at dim d0 of an output row: o / l as bf16.
+template <int N>
+__device__ __forceinline__ void store_out(__nv_bfloat16* orow, const float* o, float l, int d0)
+{
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(__fdiv_rn(o[8 * c + 2 * e], l), __fdiv_rn(o[8 * c + 2 * e + 1], l));
+        *reinterpret_cast<uint4*>(orow + d0 + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+}  // namespace enc
+}  // namespace vst

@@ -68,6 +68,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     return true;
 }
 
+// Plain arrival on an mbarrier (counts one of its expected arrivals).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32) with an OR of `pred` across them.
+__device__ __forceinline__ int bar_sync_or(int id, int count, int pred)
+{
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.s32 p, %2, 0;\n\t"
+        "bar.red.or.pred q, %1, %3, p;\n\t"
+        "selp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(pred), "r"(count)
+        : "memory");
+    return r;
+}
+
 // ---------------------------------------------------------------- TMA
 
 // Order this thread's generic-proxy shared-memory writes before later async-proxy reads
