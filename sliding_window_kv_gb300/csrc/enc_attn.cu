@@ -54,11 +54,15 @@ constexpr uint32_t kOffK = kOffQ + kTileBytes;
 constexpr uint32_t kOffV = kOffK + kTileBytes;
 constexpr uint32_t kOffP = kOffV + kTileBytes;       // two 64-key blocks
 constexpr uint32_t kOffRed = kOffP + 2 * kTileBytes; // float [2][4][128]: row max / row sum quarters
-constexpr uint32_t kOffBar = kOffRed + 2 * 4 * 128 * 4;
+constexpr uint32_t kOffKn = kOffRed + 2 * 4 * 128 * 4; // split mode: new rows of the first key tile,
+constexpr uint32_t kOffVn = kOffKn + kTileBytes;       // K rotated and V, staged in the prologue
+constexpr uint32_t kOffBar = kOffVn + kTileBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmS = 0;    // S tile: columns [0, 128)
 constexpr uint32_t kTmO = 128;  // O tile: columns [128, 192)
+
+constexpr int kMergeGroup = 8;  // split mode: tile partials loaded together by the last CTA
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64, false, true);
@@ -69,7 +73,7 @@ using enc::quarter_max;
 using enc::rotate_quarter;
 
 struct Cta {
-    uint8_t *sQ, *sK, *sV, *sP;
+    uint8_t *sQ, *sK, *sV, *sP, *sKn, *sVn;
     float *red_m, *red_l;  // [4][128]
     uint32_t bar_k, bar_v, bar_m;
     uint32_t tmem, lane_base;
@@ -104,6 +108,42 @@ __device__ __forceinline__ void patch_new_row(const Cta& s, const EncAttnCommon&
         *reinterpret_cast<uint4*>(ring + 8 * ch0) = *reinterpret_cast<const uint4*>(tile + sw128_offset(s.r, ch0));
         *reinterpret_cast<uint4*>(ring + 8 * ch1) = *reinterpret_cast<const uint4*>(tile + sw128_offset(s.r, ch1));
     }
+}
+
+// Split mode prologue: thread (r, q) rotates its quarter of new row r of key tile t (if that
+// row is new) into the staging tiles and stores it to the ring, so that the global loads of
+// the new rows overlap those of the queries; returns whether row r of tile t is new.
+__device__ __forceinline__ bool stage_new_row(const Cta& s, const EncAttnCommon& c, const EncAttnJob& job, int h,
+                                              long long t)
+{
+    const long long p = t * 128 + s.r;
+    const long long i = p - job.pos0;  // batch row
+    if (i < 0 || i >= c.n_rows)
+        return false;
+    rotate_quarter(job.k + (i * c.H + h) * kD, c.rope + p * (kD / 2), s.sKn, s.r, s.q);
+    const __nv_bfloat16* vrow = job.v + (i * c.H + h) * kD;
+    const uint4 v0 = *reinterpret_cast<const uint4*>(vrow + 16 * s.q);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(vrow + 16 * s.q + 8);
+    *reinterpret_cast<uint4*>(s.sVn + sw128_offset(s.r, 2 * s.q)) = v0;
+    *reinterpret_cast<uint4*>(s.sVn + sw128_offset(s.r, 2 * s.q + 1)) = v1;
+    __nv_bfloat16* kring = job.k_ring + ((long long)h * c.R + (job.slot0 + i)) * kD;
+    __nv_bfloat16* vring = job.v_ring + ((long long)h * c.R + (job.slot0 + i)) * kD;
+    *reinterpret_cast<uint4*>(kring + 8 * s.q) = *reinterpret_cast<const uint4*>(s.sKn + sw128_offset(s.r, s.q));
+    *reinterpret_cast<uint4*>(kring + 32 + 8 * s.q) =
+        *reinterpret_cast<const uint4*>(s.sKn + sw128_offset(s.r, 4 + s.q));
+    *reinterpret_cast<uint4*>(vring + 16 * s.q) = v0;
+    *reinterpret_cast<uint4*>(vring + 16 * s.q + 8) = v1;
+    return true;
+}
+
+// Copy this thread's chunks of a staged row into the loaded tile.
+__device__ __forceinline__ void unstage_row(const Cta& s, bool is_k)
+{
+    const int ch0 = is_k ? s.q : 2 * s.q, ch1 = is_k ? 4 + s.q : 2 * s.q + 1;
+    const uint8_t* src = is_k ? s.sKn : s.sVn;
+    uint8_t* dst = is_k ? s.sK : s.sV;
+    *reinterpret_cast<uint4*>(dst + sw128_offset(s.r, ch0)) = *reinterpret_cast<const uint4*>(src + sw128_offset(s.r, ch0));
+    *reinterpret_cast<uint4*>(dst + sw128_offset(s.r, ch1)) = *reinterpret_cast<const uint4*>(src + sw128_offset(s.r, ch1));
 }
 
 __device__ __forceinline__ void issue_s_mma(const Cta& s)
@@ -160,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     s.sK = smem + kOffK;
     s.sV = smem + kOffV;
     s.sP = smem + kOffP;
+    s.sKn = smem + kOffKn;
+    s.sVn = smem + kOffVn;
     s.red_m = reinterpret_cast<float*>(smem + kOffRed);
     s.red_l = s.red_m + 4 * 128;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -208,6 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(s.sQ + sw128_offset(r, s.q)) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(s.sQ + sw128_offset(r, 4 + s.q)) = make_uint4(0, 0, 0, 0);
     }
+    // split mode: the first key tile's new rows are rotated and stored to the ring now
+    const bool staged = split && (t_begin + 1) * 128 > job.pos0 && stage_new_row(s, c, job, h, t_begin);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -231,8 +275,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ph_k ^= 1;
         if (s.tid == 0)
             pend_k = false;
-        if (!fail && has_new)
-            patch_new_row(s, c, job, h, t, row0, row0 + nrows, true);
+        if (!fail && has_new) {
+            if (t == t_begin && split) {
+                if (staged)
+                    unstage_row(s, true);
+            } else {
+                patch_new_row(s, c, job, h, t, row0, row0 + nrows, true);
+            }
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         if (__syncthreads_or(fail)) {
@@ -275,8 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ph_v ^= 1;
         if (s.tid == 0)
             pend_v = false;
-        if (!fail && has_new)
-            patch_new_row(s, c, job, h, t, row0, row0 + nrows, false);
+        if (!fail && has_new) {
+            if (t == t_begin && split) {
+                if (staged)
+                    unstage_row(s, false);
+            } else {
+                patch_new_row(s, c, job, h, t, row0, row0 + nrows, false);
+            }
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         if (__syncthreads_or(fail)) {
@@ -341,41 +397,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r < nrows)
             enc::store_out<kDq>(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, kDq * s.q);
     } else {
-        // split mode: the last CTA of (job, head) folds all tiles in ascending order
-        __threadfence();
+        // split mode: the last CTA of (job, head) folds all tiles in ascending order. The
+        // CTA barrier orders every thread's partial before thread 0's fence and counter
+        // update (cumulative), and the last CTA's thread 0 fences again before the barrier
+        // that releases its readers.
         __syncthreads();
         if (s.tid == 0) {
+            __threadfence();
             const unsigned prev = atomicAdd(job.counters + h, 1u);
             s_last = prev == (unsigned)((t_hi - t_lo) / c.split);  // CTAs of this (job, head) - 1
+            if (s_last)
+                __threadfence();
         }
         __syncthreads();
         if (s_last) {
-            __threadfence();
             if (r < nrows) {
-                // fold the tiles in ascending order; the next tile's partial is loaded
-                // before the current one is folded so the L2 round trips overlap
+                // Tiles in groups of up to kMergeGroup: the group's loads are all issued before
+                // its folds, first for dims [0, 8) of this thread's 16, then for [8, 16); the
+                // (m, l) sequence is the same in both passes.
                 const int nt = (int)(t_hi - t_lo + 1);
                 const float* pml = job.part_ml + ((long long)h * c.split_tiles * 128 + r) * 2;
                 const float* po = job.part_o + ((long long)h * c.split_tiles * 128 + r) * kD + kDq * s.q;
-                float2 ml = __ldcg(reinterpret_cast<const float2*>(pml));
-                float4 x0 = __ldcg(reinterpret_cast<const float4*>(po));
-                float4 x1 = __ldcg(reinterpret_cast<const float4*>(po + 4));
-                float4 x2 = __ldcg(reinterpret_cast<const float4*>(po + 8));
-                float4 x3 = __ldcg(reinterpret_cast<const float4*>(po + 12));
-                for (int u = 0; u < nt; ++u) {
-                    const float2 cml = ml;
-                    const float ot[kDq] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
-                                           x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
-                    if (u + 1 < nt) {
-                        const long long step = (long long)(u + 1) * 128;
-                        ml = __ldcg(reinterpret_cast<const float2*>(pml + step * 2));
-                        x0 = __ldcg(reinterpret_cast<const float4*>(po + step * kD));
-                        x1 = __ldcg(reinterpret_cast<const float4*>(po + step * kD + 4));
-                        x2 = __ldcg(reinterpret_cast<const float4*>(po + step * kD + 8));
-                        x3 = __ldcg(reinterpret_cast<const float4*>(po + step * kD + 12));
+                for (int g0 = 0; g0 < nt; g0 += kMergeGroup) {
+                    const int ng = min(kMergeGroup, nt - g0);
+                    float2 ml[kMergeGroup];
+#pragma unroll
+                    for (int u = 0; u < kMergeGroup; ++u)
+                        if (u < ng)
+                            ml[u] = __ldcg(reinterpret_cast<const float2*>(pml + (long long)(g0 + u) * 128 * 2));
+                    float m_pass = m_run, l_pass = l_run;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float4 xa[kMergeGroup], xb[kMergeGroup];
+#pragma unroll
+                        for (int u = 0; u < kMergeGroup; ++u) {
+                            if (u < ng) {
+                                const float* src = po + (long long)(g0 + u) * 128 * kD + 8 * hf;
+                                xa[u] = __ldcg(reinterpret_cast<const float4*>(src));
+                                xb[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+                            }
+                        }
+                        m_pass = m_run;
+                        l_pass = l_run;
+#pragma unroll
+                        for (int u = 0; u < kMergeGroup; ++u) {
+                            if (u < ng && ml[u].x != -INFINITY) {
+                                const float ot[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w,
+                                                     xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+                                fold_tile<8>(m_pass, l_pass, o + 8 * hf, ml[u].x, ml[u].y, ot);
+                            }
+                        }
                     }
-                    if (cml.x != -INFINITY)
-                        fold_tile<kDq>(m_run, l_run, o, cml.x, cml.y, ot);
+                    m_run = m_pass;
+                    l_run = l_pass;
                 }
                 enc::store_out<kDq>(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, kDq * s.q);
             }

@@ -1,5 +1,5 @@
 // enc_common.cuh -- the per-row arithmetic of the chunk attention, shared by every launch
-// shape of it (enc_attn.cu, enc_attn_pair.cu). Each shape splits a 128-column score row
+// shape of it (enc_attn.cu). Each shape splits a 128-column score row
 // over a different number of threads, but all of them call these functions on the same
 // 32-column quarters in the same order, so every shape produces the same bits.
 //
@@ -19,25 +19,37 @@ namespace enc {
 constexpr int kD = 64;
 constexpr uint32_t kTileBytes = 128u * 128u;  // 128 rows x 128 B
 
+// Visible columns of the quarter [c0, c0 + 32) as a bit mask: bit j is set iff column
+// c0 + j lies in [lo, hi]. One mask and a select per column compile to straight-line code
+// (a per-column range test with an early-out does not).
+__device__ __forceinline__ uint32_t visible_mask(int c0, int lo, int hi)
+{
+    const int a = min(max(lo - c0, 0), 32), b = min(max(hi - c0 + 1, 0), 32);
+    const uint32_t below_b = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+    const uint32_t below_a = a >= 32 ? 0xffffffffu : ((1u << a) - 1u);
+    return below_b & ~below_a;
+}
+
 // Max over the visible columns of the quarter [c0, c0 + 32) held in sv.
 __device__ __forceinline__ float quarter_max(const uint32_t (&sv)[32], int c0, int lo, int hi)
 {
-    const bool full = lo <= c0 && hi >= c0 + 31;
+    const uint32_t mask = visible_mask(c0, lo, hi);
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-        if (full || (c0 + j >= lo && c0 + j <= hi))
-            m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(sv[j]));
+    for (int j = 0; j < 32; ++j) {
+        const float x = (mask >> j) & 1u ? __uint_as_float(sv[j]) : -INFINITY;
+        m4[j & 3] = fmaxf(m4[j & 3], x);
+    }
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
 // Probabilities of the quarter [c0, c0 + 32) of row `row` (neg = -m_t): written as bf16
 // into the K-major P operand (two 64-key blocks, 128-B swizzle); returns the quarter sum.
-// Columns are taken in ascending order, eight at a time.
+// Columns are taken in ascending order, eight at a time; a hidden column is 0.
 __device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], int c0, int lo, int hi, float scale_log2,
                                              float neg, uint8_t* sP, int row)
 {
-    const bool full = lo <= c0 && hi >= c0 + 31;
+    const uint32_t mask = visible_mask(c0, lo, hi);
     float l4[4] = {0.f, 0.f, 0.f, 0.f};
     const int q = c0 >> 5;
 #pragma unroll
@@ -46,8 +58,8 @@ __device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], int c0, i
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int j = 8 * qd + e;
-            const bool ok = full || (c0 + j >= lo && c0 + j <= hi);
-            pv[e] = ok ? ex2(__fmaf_rn(__uint_as_float(sv[j]), scale_log2, neg)) : 0.f;
+            const float p = ex2(__fmaf_rn(__uint_as_float(sv[j]), scale_log2, neg));
+            pv[e] = (mask >> j) & 1u ? p : 0.f;
             l4[j & 3] = __fadd_rn(l4[j & 3], pv[e]);
         }
         const uint4 w = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
