@@ -363,9 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ot[j] = __uint_as_float(ov[j]);
         }
         if (split) {
-            // tile partial of (row r, quarter q) -> scratch [h][tile][row]
+            // tile partial of (row r, quarter q) -> scratch [h][tile][q][row][16]: a warp's
+            // 32 rows of one quarter are 2 KB contiguous
             const long long slot_t = (long long)h * c.split_tiles + (t - t_lo);
-            float* po = job.part_o + (slot_t * 128 + r) * kD + kDq * s.q;
+            float* po = job.part_o + ((slot_t * 4 + s.q) * 128 + r) * kDq;
 #pragma unroll
             for (int d = 0; d < kDq; d += 4)
                 *reinterpret_cast<float4*>(po + d) = make_float4(ot[d], ot[d + 1], ot[d + 2], ot[d + 3]);
@@ -411,47 +412,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         if (s_last) {
-            if (r < nrows) {
-                // Tiles in groups of up to kMergeGroup: the group's loads are all issued before
-                // its folds, first for dims [0, 8) of this thread's 16, then for [8, 16); the
-                // (m, l) sequence is the same in both passes.
-                const int nt = (int)(t_hi - t_lo + 1);
-                const float* pml = job.part_ml + ((long long)h * c.split_tiles * 128 + r) * 2;
-                const float* po = job.part_o + ((long long)h * c.split_tiles * 128 + r) * kD + kDq * s.q;
+            // All threads of the CTA share the merge: item (row, g) folds dims [8g, 8g+8) of
+            // a row over the tiles in ascending order, in groups of up to kMergeGroup tiles
+            // whose loads are all issued before their folds.
+            const int nt = (int)(t_hi - t_lo + 1);
+            const float* pml0 = job.part_ml + (long long)h * c.split_tiles * 128 * 2;
+            const float* po0 = job.part_o + (long long)h * c.split_tiles * 128 * kD;
+            for (int it = s.tid; it < nrows * 8; it += kThreads) {
+                const int row = it >> 3, g = it & 7;  // dims [8g, 8g+8): quarter g / 2, half g % 2
+                float m = -INFINITY, l = 0.f, om[8];
+#pragma unroll
+                for (int d = 0; d < 8; ++d)
+                    om[d] = 0.f;
                 for (int g0 = 0; g0 < nt; g0 += kMergeGroup) {
                     const int ng = min(kMergeGroup, nt - g0);
                     float2 ml[kMergeGroup];
+                    float4 xa[kMergeGroup], xb[kMergeGroup];
 #pragma unroll
-                    for (int u = 0; u < kMergeGroup; ++u)
-                        if (u < ng)
-                            ml[u] = __ldcg(reinterpret_cast<const float2*>(pml + (long long)(g0 + u) * 128 * 2));
-                    float m_pass = m_run, l_pass = l_run;
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        float4 xa[kMergeGroup], xb[kMergeGroup];
-#pragma unroll
-                        for (int u = 0; u < kMergeGroup; ++u) {
-                            if (u < ng) {
-                                const float* src = po + (long long)(g0 + u) * 128 * kD + 8 * hf;
-                                xa[u] = __ldcg(reinterpret_cast<const float4*>(src));
-                                xb[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
-                            }
-                        }
-                        m_pass = m_run;
-                        l_pass = l_run;
-#pragma unroll
-                        for (int u = 0; u < kMergeGroup; ++u) {
-                            if (u < ng && ml[u].x != -INFINITY) {
-                                const float ot[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w,
-                                                     xb[u].x, xb[u].y, xb[u].z, xb[u].w};
-                                fold_tile<8>(m_pass, l_pass, o + 8 * hf, ml[u].x, ml[u].y, ot);
-                            }
+                    for (int u = 0; u < kMergeGroup; ++u) {
+                        if (u < ng) {
+                            const long long tile = g0 + u;
+                            ml[u] = __ldcg(reinterpret_cast<const float2*>(pml0 + (tile * 128 + row) * 2));
+                            const float* src = po0 + ((tile * 4 + (g >> 1)) * 128 + row) * kDq + 8 * (g & 1);
+                            xa[u] = __ldcg(reinterpret_cast<const float4*>(src));
+                            xb[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
                         }
                     }
-                    m_run = m_pass;
-                    l_run = l_pass;
+#pragma unroll
+                    for (int u = 0; u < kMergeGroup; ++u) {
+                        if (u < ng && ml[u].x != -INFINITY) {
+                            const float ot[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w,
+                                                 xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+                            fold_tile<8>(m, l, om, ml[u].x, ml[u].y, ot);
+                        }
+                    }
                 }
-                enc::store_out<kDq>(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, kDq * s.q);
+                enc::store_out<8>(job.out + ((long long)(row0 + row) * c.H + h) * kD, om, l, 8 * g);
             }
             if (s.tid == 0)
                 job.counters[h] = 0u;

@@ -111,14 +111,18 @@ __device__ __forceinline__ void rotate_quarter(const __nv_bfloat16* src, const f
 {
     const uint4 a = *reinterpret_cast<const uint4*>(src + 8 * q);
     const uint4 b = *reinterpret_cast<const uint4*>(src + 32 + 8 * q);
+    const float4* cs4 = reinterpret_cast<const float4*>(cs + 8 * q);  // 8 (cos, sin) pairs, 16-B aligned
+    const float4 c01 = cs4[0], c23 = cs4[1], c45 = cs4[2], c67 = cs4[3];
+    const float2 cw[8] = {{c01.x, c01.y}, {c01.z, c01.w}, {c23.x, c23.y}, {c23.z, c23.w},
+                          {c45.x, c45.y}, {c45.z, c45.w}, {c67.x, c67.y}, {c67.z, c67.w}};
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
     const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
     uint32_t ya[4], yb[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
         float y1a, y2a, y1b, y2b;
-        rope_pair(bf16lo(aw[w]), bf16lo(bw[w]), cs[8 * q + 2 * w], y1a, y2a);
-        rope_pair(bf16hi(aw[w]), bf16hi(bw[w]), cs[8 * q + 2 * w + 1], y1b, y2b);
+        rope_pair(bf16lo(aw[w]), bf16lo(bw[w]), cw[2 * w], y1a, y2a);
+        rope_pair(bf16hi(aw[w]), bf16hi(bw[w]), cw[2 * w + 1], y1b, y2b);
         ya[w] = pack_bf16(y1a, y1b);
         yb[w] = pack_bf16(y2a, y2b);
     }
@@ -126,16 +130,18 @@ __device__ __forceinline__ void rotate_quarter(const __nv_bfloat16* src, const f
     *reinterpret_cast<uint4*>(tile + sw128_offset(row, 4 + q)) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
 }
 
-// Store N consecutive output dims starting at dim d0 of an output row: o / l as bf16.
+// Store N consecutive output dims starting at dim d0 of an output row: o * (1 / l) as bf16
+// (one correctly rounded reciprocal per row, then a multiply per dim).
 template <int N>
 __device__ __forceinline__ void store_out(__nv_bfloat16* orow, const float* o, float l, int d0)
 {
+    const float inv = __frcp_rn(l);
 #pragma unroll
     for (int c = 0; c < N / 8; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16(__fdiv_rn(o[8 * c + 2 * e], l), __fdiv_rn(o[8 * c + 2 * e + 1], l));
+            w[e] = pack_bf16(__fmul_rn(o[8 * c + 2 * e], inv), __fmul_rn(o[8 * c + 2 * e + 1], inv));
         *reinterpret_cast<uint4*>(orow + d0 + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
