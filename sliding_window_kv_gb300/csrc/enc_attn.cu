@@ -364,14 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (split) {
             // tile partial of (row r, quarter q) -> scratch [h][tile][q][row][16]: a warp's
-            // 32 rows of one quarter are 2 KB contiguous
+            // 32 rows of one quarter are 2 KB contiguous; only rows of the batch are kept
             const long long slot_t = (long long)h * c.split_tiles + (t - t_lo);
-            float* po = job.part_o + ((slot_t * 4 + s.q) * 128 + r) * kDq;
+            if (r < nrows) {
+                float* po = job.part_o + ((slot_t * 4 + s.q) * 128 + r) * kDq;
 #pragma unroll
-            for (int d = 0; d < kDq; d += 4)
-                *reinterpret_cast<float4*>(po + d) = make_float4(ot[d], ot[d + 1], ot[d + 2], ot[d + 3]);
-            if (s.q == 0)
-                *reinterpret_cast<float2*>(job.part_ml + (slot_t * 128 + r) * 2) = make_float2(mt, lt);
+                for (int d = 0; d < kDq; d += 4)
+                    *reinterpret_cast<float4*>(po + d) = make_float4(ot[d], ot[d + 1], ot[d + 2], ot[d + 3]);
+                if (s.q == 0)
+                    *reinterpret_cast<float2*>(job.part_ml + (slot_t * 128 + r) * 2) = make_float2(mt, lt);
+            }
         } else if (mt != -INFINITY) {
             fold_tile<kDq>(m_run, l_run, o, mt, lt, ot);
         }
@@ -430,6 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4 xa[kMergeGroup], xb[kMergeGroup];
 #pragma unroll
                     for (int u = 0; u < kMergeGroup; ++u) {
+                        ml[u] = make_float2(-INFINITY, 0.f);
+                        xa[u] = xb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                         if (u < ng) {
                             const long long tile = g0 + u;
                             ml[u] = __ldcg(reinterpret_cast<const float2*>(pml0 + (tile * 128 + row) * 2));
@@ -440,11 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int u = 0; u < kMergeGroup; ++u) {
-                        if (u < ng && ml[u].x != -INFINITY) {
-                            const float ot[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w,
-                                                 xb[u].x, xb[u].y, xb[u].z, xb[u].w};
-                            fold_tile<8>(m, l, om, ml[u].x, ml[u].y, ot);
-                        }
+                        const float ot[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w, xb[u].x, xb[u].y, xb[u].z, xb[u].w};
+                        enc::fold_tile_if<8>(ml[u].x != -INFINITY, m, l, om, ml[u].x, ml[u].y, ot);
                     }
                 }
                 enc::store_out<8>(job.out + ((long long)(row0 + row) * c.H + h) * kD, om, l, 8 * g);

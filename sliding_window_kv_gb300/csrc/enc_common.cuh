@@ -34,6 +34,8 @@ __device__ __forceinline__ uint32_t visible_mask(int c0, int lo, int hi)
 __device__ __forceinline__ float quarter_max(const uint32_t (&sv)[32], int c0, int lo, int hi)
 {
     const uint32_t mask = visible_mask(c0, lo, hi);
+    if (mask == 0u)
+        return -INFINITY;
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
@@ -50,8 +52,15 @@ __device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], int c0, i
                                              float neg, uint8_t* sP, int row)
 {
     const uint32_t mask = visible_mask(c0, lo, hi);
-    float l4[4] = {0.f, 0.f, 0.f, 0.f};
     const int q = c0 >> 5;
+    if (mask == 0u) {  // nothing visible: P = 0 and the sum is 0, as below, without the exps
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd)
+            *reinterpret_cast<uint4*>(sP + (q >> 1) * kTileBytes + sw128_offset(row, (q & 1) * 4 + qd)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        return 0.f;
+    }
+    float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
         float pv[8];
@@ -102,6 +111,23 @@ __device__ __forceinline__ void fold_tile(float& m, float& l, float* o, float mt
     const FoldCoef f = fold_coef(m, mt);
     fold_apply<N>(o, ot, f);
     fold_finish(m, l, lt, f);
+}
+
+// fold_tile when `seen`, else no change; branch-free (the skipped fold's values, which may
+// be NaN when both maxima are -inf, are computed and discarded by a select).
+template <int N>
+__device__ __forceinline__ void fold_tile_if(bool seen, float& m, float& l, float* o, float mt, float lt,
+                                             const float* ot)
+{
+    const FoldCoef f = fold_coef(m, mt);
+#pragma unroll
+    for (int d = 0; d < N; ++d) {
+        const float on = __fmaf_rn(o[d], f.a, __fmul_rn(ot[d], f.b));
+        o[d] = seen ? on : o[d];
+    }
+    const float ln = __fmaf_rn(l, f.a, __fmul_rn(lt, f.b));
+    l = seen ? ln : l;
+    m = seen ? f.mn : m;
 }
 
 // Rotate pairs [8q, 8q+8) of a 64-value head row (NEOX: element i pairs with i + 32) at the
