@@ -53,8 +53,8 @@ struct Layout {
     static constexpr uint32_t kOffQ = STAGES * kStage;  // Q' [16 rows][128 dims]: 2 blocks of 2 KB
     static constexpr uint32_t kOffP = kOffQ + 4096;     // P^T [16 rows][128 keys]: 2 blocks of 2 KB
     static constexpr uint32_t kOffNew = kOffP + 4096;   // new K' row, new V row (bf16 x 128 each)
-    static constexpr uint32_t kOffRed = kOffNew + 512;  // float [2][4 heads][4 warps]
-    static constexpr uint32_t kOffBar = kOffRed + 128;  // 2*STAGES + 3 mbarriers
+    static constexpr uint32_t kOffRed = kOffNew + 512;  // float [2][4 heads][4 warps]; merge coefficients
+    static constexpr uint32_t kOffBar = kOffRed + 4 * 32 * 3 * 4;  // 2*STAGES + 3 mbarriers
     static constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;
 };
 
@@ -273,14 +273,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         } else if (warp == 0 && !fail && i + 1 < n_tiles && !prepare_and_issue_s(i + 1)) {
             fail = 1;
         }
-        uint32_t sv[4];
-        tmem_ld_32x32b_x4(tmem + lane_base + 16 * (i & 1), sv);
+        const uint32_t sv = tmem_ld_32x32b_x1(tmem + lane_base + 16 * (i & 1) + hh);  // head hh's column
         tmem_ld_wait();
 
         // ---- softmax of head hh over the tile's 128 keys (thread: key `row`)
         const long long kp = (tau_lo + i) * kTile + row;
         const bool valid = kp >= lo && kp <= pos;
-        const float sc = valid ? __fmul_rn(__uint_as_float(sv[hh]), c.scale_log2) : -INFINITY;
+        const float sc = valid ? __fmul_rn(__uint_as_float(sv), c.scale_log2) : -INFINITY;
         const float wm = warp_max(sc);
         if (lane == 0)
             red_m[hh * 4 + (warp & 3)] = wm;
@@ -330,10 +329,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 issue_v(i + 2);
             }
         }
-        uint32_t ov[4];
-        tmem_ld_32x32b_x4(tmem + lane_base + kTmO, ov);
+        const uint32_t ov = tmem_ld_32x32b_x1(tmem + lane_base + kTmO + hh);
         tmem_ld_wait();
-        fold1(m, l, o, mt, lt, __uint_as_float(ov[hh]));
+        fold1(m, l, o, mt, lt, __uint_as_float(ov));
         tc_fence_before();
     }
 
@@ -349,36 +347,70 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
     } else {
-        // ---- this split's partial; the last CTA of (stream, g) folds all splits in order
+        // ---- this split's partial; the last CTA of (stream, g) folds all splits in order.
+        // The CTA barrier orders every thread's partial before thread 0's fence and counter
+        // update; the last CTA's thread 0 fences again before the barrier that releases it.
         const int hq = g * kG + hh;
         job.part_o[((long long)hq * c.S + sl) * kD + row] = o;
         if ((warp & 3) == 0 && lane == 0)
             *reinterpret_cast<float2*>(job.part_ml + ((long long)hq * c.S + sl) * 2) = make_float2(m, l);
-        __threadfence();
         __syncthreads();
         if (tid == 0) {
+            __threadfence();
             const unsigned prev = atomicAdd(job.counters + g, 1u);
             s_last = prev == (unsigned)(job.n_splits - 1);
+            if (s_last)
+                __threadfence();
         }
         __syncthreads();
         if (s_last) {
-            __threadfence();
-            const float* pml = job.part_ml + (long long)hq * c.S * 2;
+            // The fold of split u is (m, l, o) <- (max(m, m_u), l a_u + l_u b_u, o a_u + o_u b_u)
+            // with a_u = 2^(m - max), b_u = 2^(m_u - max): the coefficients depend on the
+            // head only, so the head's first warp computes them once (the running max is an
+            // exact prefix max), and every thread replays the same FMA chain for its dim.
+            const int ns = job.n_splits;
+            float* coef = red_m;  // [4 heads][32 splits][a, b, l_u]: reuses the reduction area
+            // this dim's partials of the first 16 splits: in flight while the coefficients
+            // are computed
             const float* po = job.part_o + (long long)hq * c.S * kD + row;
-            float mm = -INFINITY, ll = 0.f, oo = 0.f;
-            for (int u0 = 0; u0 < job.n_splits; u0 += 8) {  // loads of 8 splits in flight at once
-                float2 ml[8];
-                float ov[8];
+            float ov0[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (u0 + u < job.n_splits) {
-                        ml[u] = __ldcg(reinterpret_cast<const float2*>(pml + (u0 + u) * 2));
-                        ov[u] = __ldcg(po + (long long)(u0 + u) * kD);
+            for (int u = 0; u < 16; ++u)
+                ov0[u] = u < ns ? __ldcg(po + (long long)u * kD) : 0.f;
+            if ((warp & 3) == 0) {
+                float2 mlv = make_float2(-INFINITY, 0.f);
+                if (lane < ns)
+                    mlv = __ldcg(reinterpret_cast<const float2*>(job.part_ml + ((long long)hq * c.S + lane) * 2));
+                float mpre = mlv.x;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float t = __shfl_up_sync(0xFFFFFFFFu, mpre, off);
+                    if (lane >= off)
+                        mpre = fmaxf(mpre, t);
+                }
+                float mprev = __shfl_up_sync(0xFFFFFFFFu, mpre, 1);
+                if (lane == 0)
+                    mprev = -INFINITY;
+                coef[(hh * 32 + lane) * 3 + 0] = ex2(__fsub_rn(mprev, mpre));
+                coef[(hh * 32 + lane) * 3 + 1] = ex2(__fsub_rn(mlv.x, mpre));
+                coef[(hh * 32 + lane) * 3 + 2] = mlv.y;
+            }
+            head_sync(hh);
+            const float* cf = coef + hh * 32 * 3;
+            float oo = 0.f, ll = 0.f;
+            for (int u0 = 0; u0 < ns; u0 += 16) {
+                float ov[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    ov[u] = u0 == 0 ? ov0[u] : (u0 + u < ns ? __ldcg(po + (long long)(u0 + u) * kD) : 0.f);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    if (u0 + u < ns) {
+                        const float a = cf[(u0 + u) * 3], b = cf[(u0 + u) * 3 + 1], lu = cf[(u0 + u) * 3 + 2];
+                        ll = __fmaf_rn(ll, a, __fmul_rn(lu, b));
+                        oo = __fmaf_rn(oo, a, __fmul_rn(ov[u], b));
                     }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (u0 + u < job.n_splits)
-                        fold1(mm, ll, oo, ml[u].x, ml[u].y, ov[u]);
+                }
             }
             job.out[(long long)hq * kD + row] = __float2bfloat16_rn(__fdiv_rn(oo, ll));
             if (tid == 0)
