@@ -436,7 +436,7 @@ TIMING_NOTE = ("avg_launch_us: timed region / launches, split between kernels by
                "shares; isolated_launch_us: events around each launch (no overlap with neighbours)")
 
 # sources of each profiled kernel id (the encoder attention id covers all its launch shapes)
-KERNEL_SOURCES = {"enc_attn_kernel": ("enc_attn.cu", "enc_common.cuh"),
+KERNEL_SOURCES = {"enc_attn_kernel": ("enc_attn.cu", "enc_attn_split.cu", "enc_common.cuh"),
                   "dec_step_kernel": ("dec_step.cu",), "compact_kernel": ("compact.cu",)}
 
 

@@ -13,8 +13,8 @@
 // ring slots 128t - abs_base (rows outside the ring read as zero). Rows of a tile that
 // belong to this batch (positions >= pos0) are not in the ring yet: every CTA that loads
 // such a tile rotates those keys itself from the input and patches them into shared
-// memory; the CTA whose query tile holds a new row also stores it (K rotated, V) to ring
-// slot n_kv_before + row. Per tile:
+// memory; the CTA that owns a new row also stores it (K rotated, V) to ring slot
+// n_kv_before + row. Per tile:
 //   S   = Q' K'^T      tcgen05.mma M=128 N=128 K=64, A/B K-major bf16 in smem, D in TMEM
 //   softmax            tile-local max m_t, p = 2^(s*log2e/sqrt(D) - m_t), l_t = sum p;
 //                      P -> smem as bf16
@@ -22,20 +22,18 @@
 //   fold               (m, l, o) <- fold((m, l, o), (m_t, l_t, O_t)), ascending t
 // A tile where a row sees no key is skipped for that row (exact no-op).
 //
-// Threads: 512 per CTA. Query row r (TMEM lane r) is shared by the four threads
-// (r, q), q = 0..3, one in each group of four warps: thread (r, q) owns score columns
-// [32q, 32q+32), output dims [16q, 16q+16) and RoPE pairs [8q, 8q+8). Row max and row sum
-// are combined from the four quarters through shared memory in fixed order q = 0..3.
+// Threads: 256 per CTA, two CTAs per SM. Query row r (TMEM lane r) is shared by the two
+// threads (r, half), one in each group of four warps: thread (r, half) owns score quarters
+// 2 half and 2 half + 1 (columns [64 half, 64 half + 64)), output dims [32 half, 32 half
+// + 32) and RoPE pairs [16 half, 16 half + 16). Row max and row sum are combined from the
+// two halves through shared memory, (Q0 + Q1) + (Q2 + Q3) (enc_common.cuh).
 //
-// Two launch shapes, chosen by the host from the amount of work, give the same bits:
-//   loop mode  -- one CTA per (context, head, 128-query tile) folds its tiles in registers;
-//   split mode -- one CTA per (context, head, group of `split` consecutive key tiles) of a
-//                 single query tile writes each tile's (m_t, l_t, O_t) to scratch, and the
-//                 last CTA of the (context, head) folds the tiles in ascending order with
-//                 the same fold function.
-// Tiles are fixed by absolute position and folded in ascending order, so a row's result
-// depends only on its own window -- never on how the stream was cut into feeds, on when
-// the ring was compacted, or on the launch shape.
+// Launch shape (loop): one CTA per (context, head, 128-query tile) folds its key tiles in
+// registers. The split shape for a single query tile (enc_attn_split.cu) gives the same
+// bits: tiles are fixed by absolute position and folded in ascending order, and every
+// row's arithmetic comes from enc_common.cuh -- so a row's result depends only on its own
+// window, never on how the stream was cut into feeds, on when the ring was compacted, or
+// on the launch shape.
 #include "common.cuh"
 #include "enc_common.cuh"
 #include "ptx.cuh"
@@ -45,244 +43,171 @@ namespace vst {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kD = 64;
-constexpr int kDq = kD / 4;                   // output dims per thread
-constexpr uint32_t kTileBytes = 128u * 128u;  // 128 rows x 128 B
+constexpr int kDh = kD / 2;                            // output dims per thread
+constexpr uint32_t kTileBytes = 128u * 128u;           // 128 rows x 128 B
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;
 constexpr uint32_t kOffV = kOffK + kTileBytes;
-constexpr uint32_t kOffP = kOffV + kTileBytes;       // two 64-key blocks
-constexpr uint32_t kOffRed = kOffP + 2 * kTileBytes; // float [2][4][128]: row max / row sum quarters
-constexpr uint32_t kOffKn = kOffRed + 2 * 4 * 128 * 4; // split mode: new rows of the first key tile,
-constexpr uint32_t kOffVn = kOffKn + kTileBytes;       // K rotated and V, staged in the prologue
-constexpr uint32_t kOffBar = kOffVn + kTileBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;  // + slack to align the base to 1024
+constexpr uint32_t kOffP = kOffV + kTileBytes;         // two 64-key blocks
+constexpr uint32_t kOffRed = kOffP + 2 * kTileBytes;   // float [2][2 halves][128]: row max / sum halves
+constexpr uint32_t kOffBar = kOffRed + 2 * 2 * 128 * 4;
+constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;   // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmS = 0;    // S tile: columns [0, 128)
 constexpr uint32_t kTmO = 128;  // O tile: columns [128, 192)
 
-constexpr int kMergeGroup = 8;  // split mode: tile partials loaded together by the last CTA
-
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64, false, true);
 
-using enc::fold_tile;
-using enc::quarter_exp;
-using enc::quarter_max;
-using enc::rotate_quarter;
-
-struct Cta {
-    uint8_t *sQ, *sK, *sV, *sP, *sKn, *sVn;
-    float *red_m, *red_l;  // [4][128]
-    uint32_t bar_k, bar_v, bar_m;
-    uint32_t tmem, lane_base;
-    int tid, warp, r, q;
-};
-
-// New rows of key tile t (positions >= pos0) are not in the ring yet: thread (r, q) replaces
-// its quarter of row r of the smem tile with K' = RoPE(k) (is_k) or V from the input; the
-// CTA whose query tile owns the row also stores that quarter to ring slot slot0 + row.
-__device__ __forceinline__ void patch_new_row(const Cta& s, const EncAttnCommon& c, const EncAttnJob& job, int h,
-                                              long long t, int own_lo, int own_hi, bool is_k)
+// Thread (r, half)'s chunks of a swizzled 128-byte K or V row: K' quarters 2 half and
+// 2 half + 1 are chunks {q, 4 + q}; V dims [32 half, 32 half + 32) are chunks 4 half .. + 3.
+__device__ __forceinline__ int row_chunk(bool is_k, int half, int e)
 {
-    const long long p = t * 128 + s.r;
-    const long long i = p - job.pos0;  // batch row
+    if (is_k) {
+        const int q = 2 * half + (e & 1);
+        return e < 2 ? q : 4 + q;
+    }
+    return 4 * half + e;
+}
+
+// New row `r` of key tile t (position 128t + r >= pos0): thread (r, half) writes its half
+// of the row into the smem tile -- K rotated at its absolute position, or V as is -- and,
+// for rows in [own_lo, own_hi) of the batch, to the ring.
+__device__ __forceinline__ void patch_row(const EncAttnCommon& c, const EncAttnJob& job, int h, long long t,
+                                          int r, int half, uint8_t* tile, bool is_k, int own_lo, int own_hi)
+{
+    const long long pk = t * 128 + r;
+    const long long i = pk - job.pos0;  // batch row
     if (i < 0 || i >= c.n_rows)
         return;
-    uint8_t* tile = is_k ? s.sK : s.sV;
-    int ch0, ch1;
     if (is_k) {
-        rotate_quarter(job.k + (i * c.H + h) * kD, c.rope + p * (kD / 2), tile, s.r, s.q);
-        ch0 = s.q;
-        ch1 = 4 + s.q;
+        const __nv_bfloat16* krow = job.k + (i * c.H + h) * kD;
+        enc::rotate_quarter(krow, c.rope + pk * (kD / 2), tile, r, 2 * half);
+        enc::rotate_quarter(krow, c.rope + pk * (kD / 2), tile, r, 2 * half + 1);
     } else {
         const __nv_bfloat16* vrow = job.v + (i * c.H + h) * kD;
-        ch0 = 2 * s.q;
-        ch1 = 2 * s.q + 1;
-        *reinterpret_cast<uint4*>(tile + sw128_offset(s.r, ch0)) = *reinterpret_cast<const uint4*>(vrow + 8 * ch0);
-        *reinterpret_cast<uint4*>(tile + sw128_offset(s.r, ch1)) = *reinterpret_cast<const uint4*>(vrow + 8 * ch1);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint4*>(tile + sw128_offset(r, 4 * half + e)) =
+                *reinterpret_cast<const uint4*>(vrow + 8 * (4 * half + e));
     }
     if (i >= own_lo && i < own_hi) {
         __nv_bfloat16* ring = (is_k ? job.k_ring : job.v_ring) + ((long long)h * c.R + (job.slot0 + i)) * kD;
-        *reinterpret_cast<uint4*>(ring + 8 * ch0) = *reinterpret_cast<const uint4*>(tile + sw128_offset(s.r, ch0));
-        *reinterpret_cast<uint4*>(ring + 8 * ch1) = *reinterpret_cast<const uint4*>(tile + sw128_offset(s.r, ch1));
-    }
-}
-
-// Split mode prologue: thread (r, q) rotates its quarter of new row r of key tile t (if that
-// row is new) into the staging tiles and stores it to the ring, so that the global loads of
-// the new rows overlap those of the queries; returns whether row r of tile t is new.
-__device__ __forceinline__ bool stage_new_row(const Cta& s, const EncAttnCommon& c, const EncAttnJob& job, int h,
-                                              long long t)
-{
-    const long long p = t * 128 + s.r;
-    const long long i = p - job.pos0;  // batch row
-    if (i < 0 || i >= c.n_rows)
-        return false;
-    rotate_quarter(job.k + (i * c.H + h) * kD, c.rope + p * (kD / 2), s.sKn, s.r, s.q);
-    const __nv_bfloat16* vrow = job.v + (i * c.H + h) * kD;
-    const uint4 v0 = *reinterpret_cast<const uint4*>(vrow + 16 * s.q);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(vrow + 16 * s.q + 8);
-    *reinterpret_cast<uint4*>(s.sVn + sw128_offset(s.r, 2 * s.q)) = v0;
-    *reinterpret_cast<uint4*>(s.sVn + sw128_offset(s.r, 2 * s.q + 1)) = v1;
-    __nv_bfloat16* kring = job.k_ring + ((long long)h * c.R + (job.slot0 + i)) * kD;
-    __nv_bfloat16* vring = job.v_ring + ((long long)h * c.R + (job.slot0 + i)) * kD;
-    *reinterpret_cast<uint4*>(kring + 8 * s.q) = *reinterpret_cast<const uint4*>(s.sKn + sw128_offset(s.r, s.q));
-    *reinterpret_cast<uint4*>(kring + 32 + 8 * s.q) =
-        *reinterpret_cast<const uint4*>(s.sKn + sw128_offset(s.r, 4 + s.q));
-    *reinterpret_cast<uint4*>(vring + 16 * s.q) = v0;
-    *reinterpret_cast<uint4*>(vring + 16 * s.q + 8) = v1;
-    return true;
-}
-
-// Copy this thread's chunks of a staged row into the loaded tile.
-__device__ __forceinline__ void unstage_row(const Cta& s, bool is_k)
-{
-    const int ch0 = is_k ? s.q : 2 * s.q, ch1 = is_k ? 4 + s.q : 2 * s.q + 1;
-    const uint8_t* src = is_k ? s.sKn : s.sVn;
-    uint8_t* dst = is_k ? s.sK : s.sV;
-    *reinterpret_cast<uint4*>(dst + sw128_offset(s.r, ch0)) = *reinterpret_cast<const uint4*>(src + sw128_offset(s.r, ch0));
-    *reinterpret_cast<uint4*>(dst + sw128_offset(s.r, ch1)) = *reinterpret_cast<const uint4*>(src + sw128_offset(s.r, ch1));
-}
-
-__device__ __forceinline__ void issue_s_mma(const Cta& s)
-{
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = smem_desc_sw128(smem_u32(s.sQ) + 32 * kk, 16, 1024);
-        const uint64_t bd = smem_desc_sw128(smem_u32(s.sK) + 32 * kk, 16, 1024);
-        mma_bf16_ss(s.tmem + kTmS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+        for (int e = 0; e < 4; ++e) {
+            const int ch = row_chunk(is_k, half, e);
+            *reinterpret_cast<uint4*>(ring + 8 * ch) = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, ch));
+        }
     }
-    mma_commit(s.bar_m);
-}
-
-__device__ __forceinline__ void issue_o_mma(const Cta& s)
-{
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = smem_desc_sw128(smem_u32(s.sP) + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024);
-        const uint64_t bd = smem_desc_sw128(smem_u32(s.sV) + 2048 * kk, kTileBytes, 1024);
-        mma_bf16_ss(s.tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
-    }
-    mma_commit(s.bar_m);
 }
 
 }  // namespace
 
 template <int J>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     enc_attn_kernel(const __grid_constant__ KParams<EncAttnCommon, EncAttnJob, J> p)
 {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
-    __shared__ int s_last;
     const EncAttnCommon& c = p.c;
     const EncAttnJob& job = p.jobs[blockIdx.z];
     const int h = blockIdx.y;
-    const bool split = c.split != 0;
-    const int qt = split ? 0 : blockIdx.x;
-    const int row0 = qt * 128;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = 32 * (warp & 3) + lane;  // TMEM lane = query row of this thread
+    const int half = warp >> 2;            // half of the row
+    const int row0 = (int)blockIdx.x * 128;
     const int nrows = min(128, c.n_rows - row0);
     const long long p_first = job.pos0 + row0;
-    const long long p_last = p_first + nrows - 1;
     const long long t_lo = max(0LL, p_first - c.W + 1) / 128;
-    const long long t_hi = p_last / 128;
-    const long long t_begin = split ? t_lo + (long long)blockIdx.x * c.split : t_lo;
-    const long long t_end = split ? min(t_begin + c.split - 1, t_hi) : t_hi;
-    if (t_begin > t_hi)
-        return;  // split mode: this job has fewer tiles than the grid
+    const long long t_hi = (p_first + nrows - 1) / 128;
+    // new rows this CTA stores to the ring: those of its query tile
+    const int own_lo = row0, own_hi = row0 + nrows;
 
-    Cta s;
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    s.sQ = smem + kOffQ;
-    s.sK = smem + kOffK;
-    s.sV = smem + kOffV;
-    s.sP = smem + kOffP;
-    s.sKn = smem + kOffKn;
-    s.sVn = smem + kOffVn;
-    s.red_m = reinterpret_cast<float*>(smem + kOffRed);
-    s.red_l = s.red_m + 4 * 128;
+    uint8_t* sQ = smem + kOffQ;
+    uint8_t* sK = smem + kOffK;
+    uint8_t* sV = smem + kOffV;
+    uint8_t* sP = smem + kOffP;
+    float* red_m = reinterpret_cast<float*>(smem + kOffRed);  // [2 halves][128]
+    float* red_l = red_m + 2 * 128;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    s.bar_k = smem_u32(&bars[0]);
-    s.bar_v = smem_u32(&bars[1]);
-    s.bar_m = smem_u32(&bars[2]);
-    s.tid = threadIdx.x;
-    s.warp = s.tid >> 5;
-    s.r = 32 * (s.warp & 3) + (s.tid & 31);  // TMEM lane = query row of this thread
-    s.q = s.warp >> 2;                       // quarter of the row
+    const uint32_t bar_k = smem_u32(&bars[0]), bar_v = smem_u32(&bars[1]), bar_m = smem_u32(&bars[2]);
 
     // Prologue. The first ring tiles may be requested before the previous kernel in the
     // stream has finished when the host says that kernel did not touch this ring (early);
     // everything else waits for it.
-    auto issue_first_tile = [&]() {
-        const int slot = (int)(t_begin * 128 - job.abs_base);
-        mbar_arrive_expect_tx(s.bar_k, kTileBytes);
-        tma_load_3d(smem_u32(s.sK), job.tmap_k, s.bar_k, 0, slot, h);
-        mbar_arrive_expect_tx(s.bar_v, kTileBytes);
-        tma_load_3d(smem_u32(s.sV), job.tmap_v, s.bar_v, 0, slot, h);
+    auto issue_k = [&](long long t) {
+        mbar_arrive_expect_tx(bar_k, kTileBytes);
+        tma_load_3d(smem_u32(sK), job.tmap_k, bar_k, 0, (int)(t * 128 - job.abs_base), h);
     };
-    if (s.tid == 0) {
-        mbar_init(s.bar_k, 1);
-        mbar_init(s.bar_v, 1);
-        mbar_init(s.bar_m, 1);
+    auto issue_v = [&](long long t) {
+        mbar_arrive_expect_tx(bar_v, kTileBytes);
+        tma_load_3d(smem_u32(sV), job.tmap_v, bar_v, 0, (int)(t * 128 - job.abs_base), h);
+    };
+    if (tid == 0) {
+        mbar_init(bar_k, 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_m, 1);
         fence_mbar_init();
         tmap_acquire(job.tmap_k);
         tmap_acquire(job.tmap_v);
-        if (c.early)
-            issue_first_tile();
+        if (c.early) {
+            issue_k(t_lo);
+            issue_v(t_lo);
+        }
     }
-    if (s.warp == 0) {
+    __syncwarp();
+    if (warp == 0) {
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
         tmem_relinquish();
     }
     griddep_wait();
-    if (s.tid == 0 && !c.early)
-        issue_first_tile();
-
-    // ---- this thread's quarter of query row r, rotated, into sQ
-    const int r = s.r;
-    const long long pq = p_first + r;
-    if (r < nrows) {
-        rotate_quarter(job.q + ((long long)(row0 + r) * c.H + h) * kD, c.rope + pq * (kD / 2), s.sQ, r, s.q);
-    } else {
-        *reinterpret_cast<uint4*>(s.sQ + sw128_offset(r, s.q)) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(s.sQ + sw128_offset(r, 4 + s.q)) = make_uint4(0, 0, 0, 0);
+    if (tid == 0 && !c.early) {
+        issue_k(t_lo);
+        issue_v(t_lo);
     }
-    // split mode: the first key tile's new rows are rotated and stored to the ring now
-    const bool staged = split && (t_begin + 1) * 128 > job.pos0 && stage_new_row(s, c, job, h, t_begin);
+    __syncwarp();
+
+    // ---- this thread's half of query row r, rotated, into sQ
+    const long long pq = p_first + r;
+    const bool row_real = r < nrows;
+    if (row_real) {
+        const __nv_bfloat16* qrow = job.q + ((long long)(row0 + r) * c.H + h) * kD;
+        enc::rotate_quarter(qrow, c.rope + pq * (kD / 2), sQ, r, 2 * half);
+        enc::rotate_quarter(qrow, c.rope + pq * (kD / 2), sQ, r, 2 * half + 1);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint4*>(sQ + sw128_offset(r, row_chunk(true, half, e))) = make_uint4(0, 0, 0, 0);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    s.tmem = s_tmem;
-    s.lane_base = (uint32_t)((s.warp & 3) * 32) << 16;
+    const uint32_t tmem = s_tmem;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    float o[kDq];
+    float o[kDh];
 #pragma unroll
-    for (int d = 0; d < kDq; ++d)
+    for (int d = 0; d < kDh; ++d)
         o[d] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
     uint32_t ph_k = 0, ph_v = 0, ph_m = 0;
-    bool pend_k = s.tid == 0, pend_v = s.tid == 0;
+    bool pend_k = tid == 0, pend_v = tid == 0;
     int fail = 0, aborted = 0;
 
-    for (long long t = t_begin; t <= t_end; ++t) {
+    for (long long t = t_lo; t <= t_hi; ++t) {
         const bool has_new = (t + 1) * 128 > job.pos0;
         // ---- K of tile t in smem (new rows patched in), then S = Q K^T
-        if (!mbar_wait(s.bar_k, ph_k))
+        if (!mbar_wait(bar_k, ph_k))
             fail = 1;
         ph_k ^= 1;
-        if (s.tid == 0)
+        if (tid == 0)
             pend_k = false;
-        if (!fail && has_new) {
-            if (t == t_begin && split) {
-                if (staged)
-                    unstage_row(s, true);
-            } else {
-                patch_new_row(s, c, job, h, t, row0, row0 + nrows, true);
-            }
-        }
+        if (!fail && has_new)
+            patch_row(c, job, h, t, r, half, sK, true, own_lo, own_hi);
         fence_proxy_async_smem();
         tc_fence_before();
         if (__syncthreads_or(fail)) {
@@ -290,49 +215,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
         tc_fence_after();
-        if (s.tid == 0)
-            issue_s_mma(s);
-        if (!mbar_wait(s.bar_m, ph_m))
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + kTmS, smem_desc_sw128(smem_u32(sQ) + 32 * kk, 16, 1024),
+                            smem_desc_sw128(smem_u32(sK) + 32 * kk, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+            mma_commit(bar_m);
+        }
+        __syncwarp();
+        if (!mbar_wait(bar_m, ph_m))
             fail = 1;
         ph_m ^= 1;
         tc_fence_after();
-        if (s.tid == 0 && !fail && t < t_end) {  // K buffer is free: fetch the next tile's K
-            mbar_arrive_expect_tx(s.bar_k, kTileBytes);
-            tma_load_3d(smem_u32(s.sK), job.tmap_k, s.bar_k, 0, (int)((t + 1) * 128 - job.abs_base), h);
+        if (tid == 0 && !fail && t < t_hi) {  // K buffer is free: fetch the next tile's K
+            issue_k(t + 1);
             pend_k = true;
         }
+        __syncwarp();
 
-        // ---- tile-local softmax: this thread's 32 columns of row r
-        const long long kbase = t * 128;
+        // ---- tile-local softmax of this thread's half of row r
         int lo = 1, hi = 0;  // visible columns of row r in this tile; empty unless r is real
-        if (r < nrows) {
-            lo = (int)max(-1LL, min(128LL, pq - c.W + 1 - kbase));
-            hi = (int)max(-1LL, min(128LL, pq - kbase));
+        if (row_real) {
+            lo = (int)max(-1LL, min(128LL, pq - c.W + 1 - t * 128));
+            hi = (int)max(-1LL, min(128LL, pq - t * 128));
         }
-        const int c0 = 32 * s.q;
-        uint32_t sv[32];
-        tmem_ld_32x32b_x32(s.tmem + s.lane_base + kTmS + c0, sv);
-        tmem_ld_wait();
-        s.red_m[s.q * 128 + r] = quarter_max(sv, c0, lo, hi);
+        float mh = -INFINITY;
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+            const int c0 = 64 * half + 32 * qq;
+            uint32_t sv[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + kTmS + c0, sv);
+            tmem_ld_wait();
+            mh = fmaxf(mh, enc::quarter_max(sv, c0, lo, hi));
+        }
+        red_m[half * 128 + r] = mh;
         __syncthreads();
-        const float mraw = fmaxf(fmaxf(s.red_m[r], s.red_m[128 + r]), fmaxf(s.red_m[256 + r], s.red_m[384 + r]));
-        const float mt = __fmul_rn(mraw, c.scale_log2);  // -inf when the row sees nothing here
-        s.red_l[s.q * 128 + r] = quarter_exp(sv, c0, lo, hi, c.scale_log2, -mt, s.sP, r);
+        const float mt = __fmul_rn(fmaxf(red_m[r], red_m[128 + r]), c.scale_log2);  // -inf: row sees nothing
+        float lq[2];
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+            const int c0 = 64 * half + 32 * qq;
+            uint32_t sv[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + kTmS + c0, sv);
+            tmem_ld_wait();
+            lq[qq] = enc::quarter_exp(sv, c0, lo, hi, c.scale_log2, -mt, sP, r);
+        }
+        red_l[half * 128 + r] = __fadd_rn(lq[0], lq[1]);
 
         // ---- V of tile t in smem (new rows patched in), then O_t = P V
-        if (!mbar_wait(s.bar_v, ph_v))
+        if (!mbar_wait(bar_v, ph_v))
             fail = 1;
         ph_v ^= 1;
-        if (s.tid == 0)
+        if (tid == 0)
             pend_v = false;
-        if (!fail && has_new) {
-            if (t == t_begin && split) {
-                if (staged)
-                    unstage_row(s, false);
-            } else {
-                patch_new_row(s, c, job, h, t, row0, row0 + nrows, false);
-            }
-        }
+        if (!fail && has_new)
+            patch_row(c, job, h, t, r, half, sV, false, own_lo, own_hi);
         fence_proxy_async_smem();
         tc_fence_before();
         if (__syncthreads_or(fail)) {
@@ -340,125 +277,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
         tc_fence_after();
-        if (s.tid == 0)
-            issue_o_mma(s);
-        const float lt = __fadd_rn(__fadd_rn(s.red_l[r], s.red_l[128 + r]), __fadd_rn(s.red_l[256 + r], s.red_l[384 + r]));
-        if (!mbar_wait(s.bar_m, ph_m))
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ss(tmem + kTmO,
+                            smem_desc_sw128(smem_u32(sP) + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024),
+                            smem_desc_sw128(smem_u32(sV) + 2048 * kk, kTileBytes, 1024), kIdescO, kk > 0 ? 1u : 0u);
+            mma_commit(bar_m);
+        }
+        __syncwarp();
+        const float lt = __fadd_rn(red_l[r], red_l[128 + r]);
+        if (!mbar_wait(bar_m, ph_m))
             fail = 1;
         ph_m ^= 1;
         tc_fence_after();
-        if (s.tid == 0 && !fail && t < t_end) {  // V buffer is free: fetch the next tile's V
-            mbar_arrive_expect_tx(s.bar_v, kTileBytes);
-            tma_load_3d(smem_u32(s.sV), job.tmap_v, s.bar_v, 0, (int)((t + 1) * 128 - job.abs_base), h);
+        if (tid == 0 && !fail && t < t_hi) {  // V buffer is free: fetch the next tile's V
+            issue_v(t + 1);
             pend_v = true;
         }
+        __syncwarp();
 
-        float ot[kDq];
-        {
-            uint32_t ov[16];
-            tmem_ld_32x32b_x16(s.tmem + s.lane_base + kTmO + kDq * s.q, ov);
-            tmem_ld_wait();
+        // ---- O_t of this thread's dims, folded into the running state
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kTmO + kDh * half, ov);
+        tmem_ld_wait();
+        if (mt != -INFINITY) {
+            float ot[kDh];
 #pragma unroll
-            for (int j = 0; j < kDq; ++j)
-                ot[j] = __uint_as_float(ov[j]);
-        }
-        if (split) {
-            // tile partial of (row r, quarter q) -> scratch [h][tile][q][row][16]: a warp's
-            // 32 rows of one quarter are 2 KB contiguous; only rows of the batch are kept
-            const long long slot_t = (long long)h * c.split_tiles + (t - t_lo);
-            if (r < nrows) {
-                float* po = job.part_o + ((slot_t * 4 + s.q) * 128 + r) * kDq;
-#pragma unroll
-                for (int d = 0; d < kDq; d += 4)
-                    *reinterpret_cast<float4*>(po + d) = make_float4(ot[d], ot[d + 1], ot[d + 2], ot[d + 3]);
-                if (s.q == 0)
-                    *reinterpret_cast<float2*>(job.part_ml + (slot_t * 128 + r) * 2) = make_float2(mt, lt);
-            }
-        } else if (mt != -INFINITY) {
-            fold_tile<kDq>(m_run, l_run, o, mt, lt, ot);
+            for (int d = 0; d < kDh; ++d)
+                ot[d] = __uint_as_float(ov[d]);
+            enc::fold_tile<kDh>(m_run, l_run, o, mt, lt, ot);
         }
         tc_fence_before();
-        if (__syncthreads_or(fail)) {
-            aborted = 1;
-            break;
-        }
-        tc_fence_after();
     }
 
     griddep_launch_dependents();
-    if (aborted) {
-        if (s.tid == 0) {
-            // A bounded wait gave up: record it, let copies still in flight land, then release
-            // TMEM and leave.
-            atomicExch(job.err, kErrTimeout);
-            if (pend_k)
-                mbar_wait(s.bar_k, ph_k);
-            if (pend_v)
-                mbar_wait(s.bar_v, ph_v);
-        }
-    } else if (!split) {
-        if (r < nrows)
-            enc::store_out<kDq>(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, kDq * s.q);
-    } else {
-        // split mode: the last CTA of (job, head) folds all tiles in ascending order. The
-        // CTA barrier orders every thread's partial before thread 0's fence and counter
-        // update (cumulative), and the last CTA's thread 0 fences again before the barrier
-        // that releases its readers.
-        __syncthreads();
-        if (s.tid == 0) {
-            __threadfence();
-            const unsigned prev = atomicAdd(job.counters + h, 1u);
-            s_last = prev == (unsigned)((t_hi - t_lo) / c.split);  // CTAs of this (job, head) - 1
-            if (s_last)
-                __threadfence();
-        }
-        __syncthreads();
-        if (s_last) {
-            // All threads of the CTA share the merge: item (row, g) folds dims [8g, 8g+8) of
-            // a row over the tiles in ascending order, in groups of up to kMergeGroup tiles
-            // whose loads are all issued before their folds.
-            const int nt = (int)(t_hi - t_lo + 1);
-            const float* pml0 = job.part_ml + (long long)h * c.split_tiles * 128 * 2;
-            const float* po0 = job.part_o + (long long)h * c.split_tiles * 128 * kD;
-            for (int it = s.tid; it < nrows * 8; it += kThreads) {
-                const int row = it >> 3, g = it & 7;  // dims [8g, 8g+8): quarter g / 2, half g % 2
-                float m = -INFINITY, l = 0.f, om[8];
-#pragma unroll
-                for (int d = 0; d < 8; ++d)
-                    om[d] = 0.f;
-                for (int g0 = 0; g0 < nt; g0 += kMergeGroup) {
-                    const int ng = min(kMergeGroup, nt - g0);
-                    float2 ml[kMergeGroup];
-                    float4 xa[kMergeGroup], xb[kMergeGroup];
-#pragma unroll
-                    for (int u = 0; u < kMergeGroup; ++u) {
-                        ml[u] = make_float2(-INFINITY, 0.f);
-                        xa[u] = xb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (u < ng) {
-                            const long long tile = g0 + u;
-                            ml[u] = __ldcg(reinterpret_cast<const float2*>(pml0 + (tile * 128 + row) * 2));
-                            const float* src = po0 + ((tile * 4 + (g >> 1)) * 128 + row) * kDq + 8 * (g & 1);
-                            xa[u] = __ldcg(reinterpret_cast<const float4*>(src));
-                            xb[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < kMergeGroup; ++u) {
-                        const float ot[8] = {xa[u].x, xa[u].y, xa[u].z, xa[u].w, xb[u].x, xb[u].y, xb[u].z, xb[u].w};
-                        enc::fold_tile_if<8>(ml[u].x != -INFINITY, m, l, om, ml[u].x, ml[u].y, ot);
-                    }
-                }
-                enc::store_out<8>(job.out + ((long long)(row0 + row) * c.H + h) * kD, om, l, 8 * g);
-            }
-            if (s.tid == 0)
-                job.counters[h] = 0u;
-        }
+    if (aborted && tid == 0) {
+        // A bounded wait gave up: record it and let copies still in flight land.
+        atomicExch(job.err, kErrTimeout);
+        if (pend_k)
+            mbar_wait(bar_k, ph_k);
+        if (pend_v)
+            mbar_wait(bar_v, ph_v);
     }
+    if (!aborted && row_real)
+        enc::store_out<kDh>(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, kDh * half);
     tc_fence_before();
     __syncthreads();
-    if (s.warp == 0) {
+    if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(s.tmem, kTmemCols);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -484,6 +352,8 @@ cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int 
 {
     if (n_jobs == 0 || c.n_rows == 0)
         return cudaSuccess;
+    if (c.split)
+        return cudaErrorInvalidValue;  // the split shape is launch_enc_attn_split
     return with_params(c, jobs, n_jobs, [&](const auto& p) {
         return launch_enc_attn_j<sizeof(p.jobs) / sizeof(p.jobs[0])>(p, n_jobs, grid_x, s);
     });

@@ -644,10 +644,10 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
                 if (tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc, cj, ncj, s); }) != cudaSuccess)
                     return fail_all(ctxs, n_ctx);
             }
-            // Launch shape: one CTA per (ctx, head, query tile) when that fills the GPU;
-            // otherwise (a single query tile) one CTA per (ctx, head, group of key tiles),
-            // with groups just large enough that every CTA starts in the first wave (one
-            // CTA per SM). Same bits either way.
+            // Launch shape, same bits either way: one CTA per (ctx, head, query tile) (two
+            // CTAs per SM) when that fills the GPU; otherwise (a single query tile) one CTA per
+            // (ctx, head, group of key tiles), with groups just large enough that every CTA
+            // starts in the first wave (one CTA per SM).
             const bool split = q_tiles == 1 && (long long)nj * H < m->n_sms;
             int grid_x = q_tiles;
             int max_tiles = 0;
@@ -674,7 +674,9 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
             e2.n_rows = b;
             e2.split = per_cta;
             e2.early = record_touch(s, ctxs + c0, nj);
-            if (tracked(VST_K_ENC_ATTN, s, [&] { return launch_enc_attn(e2, ej, nj, grid_x, s); }) != cudaSuccess)
+            if (tracked(VST_K_ENC_ATTN, s, [&] {
+                    return split ? launch_enc_attn_split(e2, ej, nj, grid_x, s) : launch_enc_attn(e2, ej, nj, grid_x, s);
+                }) != cudaSuccess)
                 return fail_all(ctxs, n_ctx);
             for (int i = 0; i < nj; ++i) {
                 ctxs[c0 + i]->n_kv += b;
