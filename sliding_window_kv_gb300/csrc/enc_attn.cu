@@ -9,12 +9,10 @@
 // multi-query prefill against <= 750 cached keys. Frame i attends to [i-749, i]
 // ("RECOMMENDED implementation").
 //
-// Keys are visited in tiles of 128 ABSOLUTE positions [128t, 128t+128), loaded by TMA from
-// ring slots 128t - abs_base (rows outside the ring read as zero). Rows of a tile that
-// belong to this batch (positions >= pos0) are not in the ring yet: every CTA that loads
-// such a tile rotates those keys itself from the input and patches them into shared
-// memory; the CTA that owns a new row also stores it (K rotated, V) to ring slot
-// n_kv_before + row. Per tile:
+// Keys are visited in tiles of 128 ABSOLUTE positions [128t, 128t+128), loaded whole by
+// TMA from ring slots 128t - abs_base (rows outside the ring read as zero): the batch's own
+// rows were rotated and appended to the ring by kernel (a) (rope_append.cu) just before
+// this launch. Per tile:
 //   S   = Q' K'^T      tcgen05.mma M=128 N=128 K=64, A/B K-major bf16 in smem, D in TMEM
 //   softmax            tile-local max m_t, p = 2^(s*log2e/sqrt(D) - m_t), l_t = sum p;
 //                      P -> smem as bf16
@@ -61,48 +59,6 @@ constexpr uint32_t kTmO = 128;  // O tile: columns [128, 192)
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64, false, true);
 
-// Thread (r, half)'s chunks of a swizzled 128-byte K or V row: K' quarters 2 half and
-// 2 half + 1 are chunks {q, 4 + q}; V dims [32 half, 32 half + 32) are chunks 4 half .. + 3.
-__device__ __forceinline__ int row_chunk(bool is_k, int half, int e)
-{
-    if (is_k) {
-        const int q = 2 * half + (e & 1);
-        return e < 2 ? q : 4 + q;
-    }
-    return 4 * half + e;
-}
-
-// New row `r` of key tile t (position 128t + r >= pos0): thread (r, half) writes its half
-// of the row into the smem tile -- K rotated at its absolute position, or V as is -- and,
-// for rows in [own_lo, own_hi) of the batch, to the ring.
-__device__ __forceinline__ void patch_row(const EncAttnCommon& c, const EncAttnJob& job, int h, long long t,
-                                          int r, int half, uint8_t* tile, bool is_k, int own_lo, int own_hi)
-{
-    const long long pk = t * 128 + r;
-    const long long i = pk - job.pos0;  // batch row
-    if (i < 0 || i >= c.n_rows)
-        return;
-    if (is_k) {
-        const __nv_bfloat16* krow = job.k + (i * c.H + h) * kD;
-        enc::rotate_quarter(krow, c.rope + pk * (kD / 2), tile, r, 2 * half);
-        enc::rotate_quarter(krow, c.rope + pk * (kD / 2), tile, r, 2 * half + 1);
-    } else {
-        const __nv_bfloat16* vrow = job.v + (i * c.H + h) * kD;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<uint4*>(tile + sw128_offset(r, 4 * half + e)) =
-                *reinterpret_cast<const uint4*>(vrow + 8 * (4 * half + e));
-    }
-    if (i >= own_lo && i < own_hi) {
-        __nv_bfloat16* ring = (is_k ? job.k_ring : job.v_ring) + ((long long)h * c.R + (job.slot0 + i)) * kD;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int ch = row_chunk(is_k, half, e);
-            *reinterpret_cast<uint4*>(ring + 8 * ch) = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, ch));
-        }
-    }
-}
-
 }  // namespace
 
 template <int J>
@@ -122,8 +78,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const long long p_first = job.pos0 + row0;
     const long long t_lo = max(0LL, p_first - c.W + 1) / 128;
     const long long t_hi = (p_first + nrows - 1) / 128;
-    // new rows this CTA stores to the ring: those of its query tile
-    const int own_lo = row0, own_hi = row0 + nrows;
 
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -180,9 +134,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         enc::rotate_quarter(qrow, c.rope + pq * (kD / 2), sQ, r, 2 * half + 1);
     } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<uint4*>(sQ + sw128_offset(r, row_chunk(true, half, e))) = make_uint4(0, 0, 0, 0);
+        for (int e = 0; e < 4; ++e)  // chunks {q, 4 + q} of quarters q = 2 half, 2 half + 1
+            *reinterpret_cast<uint4*>(sQ + sw128_offset(r, (e >> 1) * 4 + 2 * half + (e & 1))) = make_uint4(0, 0, 0, 0);
     }
+    fence_proxy_async_smem();  // Q' (generic stores) before the MMAs read it
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -199,16 +154,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     int fail = 0, aborted = 0;
 
     for (long long t = t_lo; t <= t_hi; ++t) {
-        const bool has_new = (t + 1) * 128 > job.pos0;
-        // ---- K of tile t in smem (new rows patched in), then S = Q K^T
+        // ---- K of tile t in smem, then S = Q K^T
         if (!mbar_wait(bar_k, ph_k))
             fail = 1;
         ph_k ^= 1;
         if (tid == 0)
             pend_k = false;
-        if (!fail && has_new)
-            patch_row(c, job, h, t, r, half, sK, true, own_lo, own_hi);
-        fence_proxy_async_smem();
         tc_fence_before();
         if (__syncthreads_or(fail)) {
             aborted = 1;
@@ -262,15 +213,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         red_l[half * 128 + r] = __fadd_rn(lq[0], lq[1]);
 
-        // ---- V of tile t in smem (new rows patched in), then O_t = P V
+        // ---- V of tile t in smem, then O_t = P V
         if (!mbar_wait(bar_v, ph_v))
             fail = 1;
         ph_v ^= 1;
         if (tid == 0)
             pend_v = false;
-        if (!fail && has_new)
-            patch_row(c, job, h, t, r, half, sV, false, own_lo, own_hi);
-        fence_proxy_async_smem();
+        fence_proxy_async_smem();  // P (generic stores) before the MMA reads it
         tc_fence_before();
         if (__syncthreads_or(fail)) {
             aborted = 1;
@@ -352,8 +301,8 @@ cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int 
 {
     if (n_jobs == 0 || c.n_rows == 0)
         return cudaSuccess;
-    if (c.split)
-        return cudaErrorInvalidValue;  // the split shape is launch_enc_attn_split
+    if (c.split || !c.appended)
+        return cudaErrorInvalidValue;  // split shape: launch_enc_attn_split; rows appended first
     return with_params(c, jobs, n_jobs, [&](const auto& p) {
         return launch_enc_attn_j<sizeof(p.jobs) / sizeof(p.jobs[0])>(p, n_jobs, grid_x, s);
     });

@@ -616,7 +616,7 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
     auto* ob = static_cast<__nv_bfloat16*>(out);
 
     const CompactCommon cc{Hk, cfg.ring_slots, D, cfg.window};
-    const EncAttnCommon ec{m->rope, 0, H, cfg.window, cfg.ring_slots, 0, m->splits, 0,
+    const EncAttnCommon ec{m->rope, 0, H, cfg.window, cfg.ring_slots, 0, m->splits, 0, 0,
                            (float)(1.4426950408889634 / std::sqrt((double)D))};
     CompactJob cj[kMaxJobs];
     const vst_ctx* cctx[kMaxJobs];
@@ -670,9 +670,24 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
                     ++per_cta;
                 grid_x = (max_tiles + per_cta - 1) / per_cta;
             }
+            if (!split) {
+                // Loop shape: the batch's K' and V rows go to the ring first (kernel a), so
+                // that every key tile of the attention arrives whole by TMA.
+                const AppendCommon ac{m->rope, b, Hk, D, cfg.ring_slots, 0};
+                AppendJob aj[kMaxJobs];
+                for (int i = 0; i < nj; ++i) {
+                    const vst_ctx* c = ctxs[c0 + i];
+                    const long long row = (long long)(c0 + i) * n_new + off;
+                    aj[i] = AppendJob{kb + row * Hk * D, vb + row * Hk * D, c->k_ring, c->v_ring, c->abs_next, c->n_kv};
+                }
+                record_touch(s, ctxs + c0, nj);
+                if (tracked(VST_K_ROPE_APPEND, s, [&] { return launch_rope_append(ac, aj, nj, s); }) != cudaSuccess)
+                    return fail_all(ctxs, n_ctx);
+            }
             EncAttnCommon e2 = ec;
             e2.n_rows = b;
             e2.split = per_cta;
+            e2.appended = split ? 0 : 1;
             e2.early = record_touch(s, ctxs + c0, nj);
             if (tracked(VST_K_ENC_ATTN, s, [&] {
                     return split ? launch_enc_attn_split(e2, ej, nj, grid_x, s) : launch_enc_attn(e2, ej, nj, grid_x, s);

@@ -87,6 +87,7 @@ struct EncAttnCommon {
     int split;               // 0: loop mode; k > 0: split mode, k key tiles per CTA
     int split_tiles;         // scratch tiles per head
     int early;               // 1: ring loads may start before the previous kernel completes
+    int appended;            // 1: the batch's K'/V rows are already in the ring (loop shape)
     float scale_log2;        // log2(e) / sqrt(D)
 };
 
