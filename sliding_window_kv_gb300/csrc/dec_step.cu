@@ -18,12 +18,10 @@
 //   O^T = V^T P^T    tcgen05.mma M=128 dims, N=16, K=128 keys; A = V tile read as
 //                    MN-major (dims contiguous), B = P^T (K-major); TMEM
 //   fold             thread (head h, dim d) folds (m_t, l_t, O_t[h][d]) into registers.
-// Two pipelines compute the same bits:
-//   STAGES = 2 -- two K/V stages (one CTA per SM); the next tile's S^T is computed during
-//                 this tile's softmax (S^T double-buffered in TMEM). For small launches.
-//   STAGES = 1 -- one K/V stage (two CTAs per SM, so one CTA's prologue and merge overlap
-//                 the other's streaming); the next K is fetched as soon as S^T is done and
-//                 the next V as soon as O^T is done. For large launches.
+// Pipeline: one K/V stage per CTA and two CTAs per SM, so that one CTA's prologue and
+// merge overlap another's streaming (also across launches: the next launch's CTAs share
+// the SM while this one finishes). The next K is fetched as soon as S^T is done, the next
+// V as soon as O^T is done; S^T alternates between two TMEM buffers.
 // The query heads are rotated in the prologue; if the split holds pos, the new key is
 // rotated too, patched into its tile row in shared memory, and stored (K', V) to ring slot
 // pos % R by this CTA. Each CTA writes its split's (m, l, o) per head; the last CTA of
@@ -48,13 +46,12 @@ constexpr uint32_t kStage = 4 * kBox;       // K lo, K hi, V lo, V hi
 constexpr uint32_t kTmemCols = 64;          // S^T buffers at [0,16) and [16,32); O^T at [32,48)
 constexpr uint32_t kTmO = 32;
 
-template <int STAGES>
 struct Layout {
-    static constexpr uint32_t kOffQ = STAGES * kStage;  // Q' [16 rows][128 dims]: 2 blocks of 2 KB
+    static constexpr uint32_t kOffQ = kStage;           // Q' [16 rows][128 dims]: 2 blocks of 2 KB
     static constexpr uint32_t kOffP = kOffQ + 4096;     // P^T [16 rows][128 keys]: 2 blocks of 2 KB
     static constexpr uint32_t kOffNew = kOffP + 4096;   // new K' row, new V row (bf16 x 128 each)
     static constexpr uint32_t kOffRed = kOffNew + 512;  // float [2][4 heads][4 warps]; merge coefficients
-    static constexpr uint32_t kOffBar = kOffRed + 4 * 32 * 3 * 4;  // 2*STAGES + 3 mbarriers
+    static constexpr uint32_t kOffBar = kOffRed + 4 * 32 * 3 * 4;  // 5 mbarriers
     static constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;
 };
 
@@ -103,11 +100,11 @@ __device__ __forceinline__ uint32_t sw16(int row, int col)
 
 }  // namespace
 
-template <int J, int STAGES>
+template <int J>
 __global__ void __launch_bounds__(kThreads, 2)
     dec_step_kernel(const __grid_constant__ KParams<DecCommon, DecJob, J> p)
 {
-    using L = Layout<STAGES>;
+    using L = Layout;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     __shared__ int s_last;
@@ -119,11 +116,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     float* red_m = reinterpret_cast<float*>(smem + L::kOffRed);  // [4 heads][4 warps]
     float* red_l = red_m + 16;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-    // bars: K landed [STAGES], V landed [STAGES], S^T done [2], O^T done
-    auto bar_k = [&](int st) { return smem_u32(&bars[st]); };
-    auto bar_v = [&](int st) { return smem_u32(&bars[STAGES + st]); };
-    auto bar_s = [&](int b) { return smem_u32(&bars[2 * STAGES + b]); };
-    const uint32_t bar_o = smem_u32(&bars[2 * STAGES + 2]);
+    // bars: K landed, V landed, S^T done [2], O^T done
+    const uint32_t bar_k = smem_u32(&bars[0]), bar_v = smem_u32(&bars[1]);
+    auto bar_s = [&](int b) { return smem_u32(&bars[2 + b]); };
+    const uint32_t bar_o = smem_u32(&bars[4]);
 
     const DecCommon& c = p.c;
     const int item = blockIdx.x;
@@ -146,34 +142,32 @@ __global__ void __launch_bounds__(kThreads, 2)
     const long long tau_new = pos / kTile;  // tile holding this step's key
     const bool has_new = tau_new >= tau_lo && tau_new <= tau_hi;
 
-    auto stage_k = [&](int i) { return smem + (i % STAGES) * kStage; };
-    auto stage_v = [&](int i) { return smem + (i % STAGES) * kStage + 2 * kBox; };
-    auto parity = [&](int i) { return (uint32_t)((i / STAGES) & 1); };
+    uint8_t* const sK = smem;             // K tile: two 64-dim boxes
+    uint8_t* const sV = smem + 2 * kBox;  // V tile
+    auto parity = [&](int i) { return (uint32_t)(i & 1); };
     auto slot_of = [&](int i) { return (int)(((tau_lo + i) * kTile) % c.R); };
     auto issue_k = [&](int i) {
-        const uint32_t dst = smem_u32(stage_k(i));
-        mbar_arrive_expect_tx(bar_k(i % STAGES), 2 * kBox);
-        tma_load_3d(dst, job.tmap_k, bar_k(i % STAGES), 0, slot_of(i), g);
-        tma_load_3d(dst + kBox, job.tmap_k, bar_k(i % STAGES), 64, slot_of(i), g);
+        const uint32_t dst = smem_u32(sK);
+        mbar_arrive_expect_tx(bar_k, 2 * kBox);
+        tma_load_3d(dst, job.tmap_k, bar_k, 0, slot_of(i), g);
+        tma_load_3d(dst + kBox, job.tmap_k, bar_k, 64, slot_of(i), g);
     };
     auto issue_v = [&](int i) {
-        const uint32_t dst = smem_u32(stage_v(i));
-        mbar_arrive_expect_tx(bar_v(i % STAGES), 2 * kBox);
-        tma_load_3d(dst, job.tmap_v, bar_v(i % STAGES), 0, slot_of(i), g);
-        tma_load_3d(dst + kBox, job.tmap_v, bar_v(i % STAGES), 64, slot_of(i), g);
+        const uint32_t dst = smem_u32(sV);
+        mbar_arrive_expect_tx(bar_v, 2 * kBox);
+        tma_load_3d(dst, job.tmap_v, bar_v, 0, slot_of(i), g);
+        tma_load_3d(dst + kBox, job.tmap_v, bar_v, 64, slot_of(i), g);
     };
-    auto issue_first = [&]() {
-        for (int i = 0; i < STAGES && i < n_tiles; ++i) {
-            issue_k(i);
-            issue_v(i);
-        }
+    auto issue_first = [&]() {  // every split has at least one tile
+        issue_k(0);
+        issue_v(0);
     };
 
     // Prologue. The first ring tiles may be requested before the previous kernel in the
     // stream has finished when the host says that kernel did not touch this ring (early);
     // everything else waits for it.
     if (tid == 0) {
-        for (int b = 0; b < 2 * STAGES + 3; ++b)
+        for (int b = 0; b < 5; ++b)
             mbar_init(smem_u32(&bars[b]), 1);
         fence_mbar_init();
         tmap_acquire(job.tmap_k);
@@ -228,8 +222,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // Warp 0: wait for tile i's K, patch the new key in if it is there, and (lane 0) issue
     // S^T for it into S buffer i & 1. Returns false if the wait gave up.
     auto prepare_and_issue_s = [&](int i) -> bool {
-        uint8_t* sK = stage_k(i);
-        bool ok = mbar_wait(bar_k(i % STAGES), parity(i));
+        bool ok = mbar_wait(bar_k, parity(i));
         if (ok && has_new && tau_lo + i == tau_new && lane < 16) {
             const uint4 kw = reinterpret_cast<const uint4*>(snew)[lane];  // dims [8 lane, 8 lane + 8)
             *reinterpret_cast<uint4*>(sK + (lane >> 3) * kBox + sw128_offset(rr_new, lane & 7)) = kw;
@@ -257,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t ph_o = 0;
 
     for (int i = 0; i < n_tiles; ++i) {
-        // ---- S^T of tile i (two stages: already issued during the previous tile)
-        if (warp == 0 && (STAGES == 1 || i == 0) && !prepare_and_issue_s(i))
+        // ---- S^T of tile i
+        if (warp == 0 && !prepare_and_issue_s(i))
             fail = 1;
         if (__syncthreads_or(fail)) {
             aborted = 1;
@@ -267,12 +260,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!mbar_wait(bar_s(i & 1), (uint32_t)((i >> 1) & 1)))
             fail = 1;
         tc_fence_after();
-        if (STAGES == 1) {
-            if (tid == 0 && !fail && i + 1 < n_tiles)
-                issue_k(i + 1);  // the K buffer is free once S^T of tile i is done
-        } else if (warp == 0 && !fail && i + 1 < n_tiles && !prepare_and_issue_s(i + 1)) {
-            fail = 1;
-        }
+        if (tid == 0 && !fail && i + 1 < n_tiles)
+            issue_k(i + 1);  // the K buffer is free once S^T of tile i is done
         const uint32_t sv = tmem_ld_32x32b_x1(tmem + lane_base + 16 * (i & 1) + hh);  // head hh's column
         tmem_ld_wait();
 
@@ -292,8 +281,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             red_l[hh * 4 + (warp & 3)] = ws;
 
         // ---- V of tile i (new value patched in), then O^T = V^T P^T
-        uint8_t* sV = stage_v(i);
-        if (!mbar_wait(bar_v(i % STAGES), parity(i)))
+        if (!mbar_wait(bar_v, parity(i)))
             fail = 1;
         if (!fail && has_new && tau_lo + i == tau_new && tid < 16) {
             const uint4 vw = reinterpret_cast<const uint4*>(snew + kD)[tid];
@@ -321,14 +309,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             fail = 1;
         ph_o ^= 1;
         tc_fence_after();
-        if (tid == 0 && !fail) {
-            if (STAGES == 1 && i + 1 < n_tiles)
-                issue_v(i + 1);  // the V buffer is free once O^T of tile i is done
-            else if (STAGES == 2 && i + 2 < n_tiles) {
-                issue_k(i + 2);  // the whole stage is free
-                issue_v(i + 2);
-            }
-        }
+        if (tid == 0 && !fail && i + 1 < n_tiles)
+            issue_v(i + 1);  // the V buffer is free once O^T of tile i is done
         const uint32_t ov = tmem_ld_32x32b_x1(tmem + lane_base + kTmO + hh);
         tmem_ld_wait();
         fold1(m, l, o, mt, lt, __uint_as_float(ov));
@@ -341,10 +323,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             // A bounded wait gave up: record it, give copies in flight a bounded chance to
             // land, release TMEM and leave.
             atomicExch(job.err, kErrTimeout);
-            for (int st = 0; st < STAGES; ++st) {
-                mbar_wait(bar_k(st), 0);
-                mbar_wait(bar_v(st), 0);
-            }
+            mbar_wait(bar_k, 0);
+            mbar_wait(bar_v, 0);
         }
     } else {
         // ---- this split's partial; the last CTA of (stream, g) folds all splits in order.
@@ -425,22 +405,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-template <int J, int STAGES>
+template <int J>
 static cudaError_t launch_dec_j(const KParams<DecCommon, DecJob, J>& p, int total_work, cudaStream_t s)
 {
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    const uint32_t smem = Layout<STAGES>::kSmemBytes;
+    const uint32_t smem = Layout::kSmemBytes;
     if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(dec_step_kernel<J, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(dec_step_kernel<J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess)
             return e;
         configured[dev] = 1;
     }
     const dim3 grid((unsigned)total_work, (unsigned)p.c.Hk);
-    return launch_pdl(dec_step_kernel<J, STAGES>, grid, dim3(kThreads), smem, s, p);
+    return launch_pdl(dec_step_kernel<J>, grid, dim3(kThreads), smem, s, p);
 }
 
 cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, int total_work,
@@ -448,15 +428,8 @@ cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, 
 {
     if (n_jobs == 0 || total_work == 0)
         return cudaSuccess;
-    // one CTA per SM with two stages while the launch fits in one wave; beyond that two
-    // CTAs per SM with one stage each
-    int dev = 0, n_sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
-    const bool big = (long long)total_work * c.Hk > n_sms;
     return with_params(c, jobs, n_jobs, [&](const auto& p) {
-        constexpr int J = sizeof(p.jobs) / sizeof(p.jobs[0]);
-        return big ? launch_dec_j<J, 1>(p, total_work, s) : launch_dec_j<J, 2>(p, total_work, s);
+        return launch_dec_j<sizeof(p.jobs) / sizeof(p.jobs[0])>(p, total_work, s);
     });
 }
 
