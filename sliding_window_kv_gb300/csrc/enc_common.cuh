@@ -37,10 +37,16 @@ __device__ __forceinline__ float quarter_max(const uint32_t (&sv)[32], int c0, i
     if (mask == 0u)
         return -INFINITY;
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (mask == 0xffffffffu) {  // every column visible: the same maxima without the selects
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float x = (mask >> j) & 1u ? __uint_as_float(sv[j]) : -INFINITY;
-        m4[j & 3] = fmaxf(m4[j & 3], x);
+        for (int j = 0; j < 32; ++j)
+            m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(sv[j]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float x = (mask >> j) & 1u ? __uint_as_float(sv[j]) : -INFINITY;
+            m4[j & 3] = fmaxf(m4[j & 3], x);
+        }
     }
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
@@ -61,16 +67,25 @@ __device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], int c0, i
         return 0.f;
     }
     float l4[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool full = mask == 0xffffffffu;  // every column visible: no selects needed
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
         float pv[8];
+        if (full) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = 8 * qd + e;
-            const float p = ex2(__fmaf_rn(__uint_as_float(sv[j]), scale_log2, neg));
-            pv[e] = (mask >> j) & 1u ? p : 0.f;
-            l4[j & 3] = __fadd_rn(l4[j & 3], pv[e]);
+            for (int e = 0; e < 8; ++e)
+                pv[e] = ex2(__fmaf_rn(__uint_as_float(sv[8 * qd + e]), scale_log2, neg));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = 8 * qd + e;
+                const float p = ex2(__fmaf_rn(__uint_as_float(sv[j]), scale_log2, neg));
+                pv[e] = (mask >> j) & 1u ? p : 0.f;
+            }
         }
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            l4[(8 * qd + e) & 3] = __fadd_rn(l4[(8 * qd + e) & 3], pv[e]);
         const uint4 w = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
                                    pack_bf16(pv[6], pv[7]));
         *reinterpret_cast<uint4*>(sP + (q >> 1) * kTileBytes + sw128_offset(row, (q & 1) * 4 + qd)) = w;
