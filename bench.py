@@ -37,15 +37,15 @@ ENC_H, ENC_D, ENC_W = 20, 64, 750
 DEC_H, DEC_HK, DEC_D, DEC_W = 32, 8, 128, 8192
 
 WORKLOADS = {
-    # configs[1]: the metric's configuration
+    # encoder streaming, 32 layers, one stream, 4416 frames in 50-frame feeds (default line)
     "enc_stream": dict(kind="enc", layers=32, frames=4416, feed=50, streams=1, seed=2, stagger=0),
-    # configs[0]: small correctness case
+    # encoder, one layer, 1000 frames in 100-frame feeds (small case)
     "enc_small": dict(kind="enc", layers=1, frames=1000, feed=100, streams=1, seed=1, stagger=0),
-    # configs[4]: 16 concurrent streams, staggered starts (96*s frames), 512-frame batches
+    # encoder, 16 concurrent streams, staggered starts (96*s frames), 512-frame batches
     "enc_long16": dict(kind="enc", layers=32, frames=15300, feed=512, streams=16, seed=5, stagger=96),
-    # configs[2]: decoder batch 1
+    # decoder, 26 layers, batch 1, KV filled to 8192
     "dec_b1": dict(kind="dec", layers=26, streams=1, fill="full", steps=256, seed=3),
-    # configs[3]: decoder, 64 streams with fills uniform in [1, 8192]
+    # decoder, 26 layers, 64 streams with fills uniform in [1, 8192]
     "dec_b64": dict(kind="dec", layers=26, streams=64, fill="uniform", steps=256, seed=4),
 }
 
