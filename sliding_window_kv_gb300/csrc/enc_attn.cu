@@ -190,28 +190,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             lo = (int)max(-1LL, min(128LL, pq - c.W + 1 - t * 128));
             hi = (int)max(-1LL, min(128LL, pq - t * 128));
         }
-        float mh = -INFINITY;
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-            const int c0 = 64 * half + 32 * qq;
-            uint32_t sv[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + kTmS + c0, sv);
-            tmem_ld_wait();
-            mh = fmaxf(mh, enc::quarter_max(sv, c0, lo, hi));
-        }
+        // both quarters of this half-row in one TMEM round trip, kept for the exp pass
+        uint32_t sa[32], sb[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kTmS + 64 * half, sa);
+        tmem_ld_32x32b_x32(tmem + lane_base + kTmS + 64 * half + 32, sb);
+        tmem_ld_wait();
+        const float mh = fmaxf(enc::quarter_max(sa, 64 * half, lo, hi), enc::quarter_max(sb, 64 * half + 32, lo, hi));
         red_m[half * 128 + r] = mh;
         __syncthreads();
         const float mt = __fmul_rn(fmaxf(red_m[r], red_m[128 + r]), c.scale_log2);  // -inf: row sees nothing
-        float lq[2];
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-            const int c0 = 64 * half + 32 * qq;
-            uint32_t sv[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + kTmS + c0, sv);
-            tmem_ld_wait();
-            lq[qq] = enc::quarter_exp(sv, c0, lo, hi, c.scale_log2, -mt, sP, r);
-        }
-        red_l[half * 128 + r] = __fadd_rn(lq[0], lq[1]);
+        const float la = enc::quarter_exp(sa, 64 * half, lo, hi, c.scale_log2, -mt, sP, r);
+        const float lb = enc::quarter_exp(sb, 64 * half + 32, lo, hi, c.scale_log2, -mt, sP, r);
+        red_l[half * 128 + r] = __fadd_rn(la, lb);
 
         // ---- V of tile t in smem, then O_t = P V
         if (!mbar_wait(bar_v, ph_v))
