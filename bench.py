@@ -591,8 +591,10 @@ def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu):
                         "algorithmic_bytes_per_launch": bytes_per_launch}}
     if want_cpu:
         v, dt, sample = cpu_baseline_dec(spec, 16, cpu_threads())
+        v1, dt1, sample1 = cpu_baseline_dec(spec, 4, 1)
         out["cpu_baseline"] = {"value": v, "unit": "dec steps/s", "cores": cpu_threads(), "kind": "oracle",
-                               "sample": sample}
+                               "sample": sample, "seconds": dt,
+                               "single_thread": {"value": v1, "sample": sample1, "seconds": dt1}}
     w.close()
     return out
 
@@ -710,8 +712,10 @@ def run_vst(args, dist):
 
     if not args.no_cpu and dist.rank == 0:
         v, dt, sample = cpu_baseline_enc(spec, 4 if spec["layers"] >= 4 else spec["layers"], cpu_threads())
+        v1, dt1, sample1 = cpu_baseline_enc(spec, 1, 1)
         line["cpu_baseline"] = {"value": v, "unit": "enc frames/s", "cores": cpu_threads(), "kind": "oracle",
-                                "sample": sample, "seconds": dt}
+                                "sample": sample, "seconds": dt,
+                                "single_thread": {"value": v1, "sample": sample1, "seconds": dt1}}
     if dist.rank == 0:
         print(json.dumps(line))
 

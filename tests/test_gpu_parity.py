@@ -239,6 +239,47 @@ def test_enc_batch_equals_single(dev, enc_module, n_ctx, step):
         c.close()
 
 
+def test_enc_16_streams_512_batches(dev, enc_module):
+    """The 16-stream launch configuration: streams with staggered starts (a first feed of
+    96 s frames), then 512-frame batches through vst_enc_feed_batch (every batch launch is
+    the loop shape over 16 contexts x 20 heads x 4 query tiles, with a compaction before the
+    third). Sampled rows against the oracle; one stream re-fed alone in 50-frame feeds (the
+    split shape) gives the same bits as in the batch."""
+    S, T, B = 16, 1536, 512
+    offsets = [96 * s for s in range(S)]
+    seqs = [_enc_inputs(9, s, offsets[s] + T) for s in range(S)]
+    ctxs = [vst.Ctx(enc_module) for _ in range(S)]
+    for s in range(S):
+        if offsets[s]:
+            o = torch.empty((offsets[s], 20, 64), dtype=torch.bfloat16, device=dev)
+            vst.enc_feed(ctxs[s].handle, *(x[:offsets[s]].to(dev) for x in seqs[s]), o)
+    Q, K, V = (torch.stack([seqs[s][i][offsets[s]:] for s in range(S)]).to(dev) for i in range(3))
+    OUT = torch.empty_like(Q)
+    for t0 in range(0, T, B):
+        o = torch.empty_like(Q[:, t0:t0 + B].contiguous())
+        vst.enc_feed_batch([c.handle for c in ctxs], Q[:, t0:t0 + B].contiguous(), K[:, t0:t0 + B].contiguous(),
+                           V[:, t0:t0 + B].contiguous(), o, B)
+        OUT[:, t0:t0 + B] = o
+    torch.cuda.synchronize()
+    for s in range(S):
+        assert vst.ctx_check(ctxs[s].handle) == vst.OK
+        assert ctxs[s].info().abs_next == offsets[s] + T
+    got = OUT.float().cpu().double().numpy()
+    for s in (0, 5, 15):
+        qb, kb, vb = (synth.bits(x) for x in seqs[s])
+        for i in (0, 1, 511, 512, 1023, 1024, 1535):
+            p = offsets[s] + i
+            j0 = max(0, p - 749)
+            want = oracle.attention_row(qb[p], kb[j0:p + 1], vb[j0:p + 1], p, 750)
+            d = np.abs(got[s, i] - want)
+            assert d.max() <= MAX_TOL, (s, i, d.max())
+    s = 7
+    alone, _ = _feed(enc_module, *seqs[s], [offsets[s]] + [50] * (T // 50) + [T % 50])
+    assert torch.equal(alone[offsets[s]:], OUT[s])
+    for c in ctxs:
+        c.close()
+
+
 # ---------------------------------------------------------------- decoder
 
 def _dec_seq(seed, stream, layer, n_tok, device="cpu", first=0):
