@@ -448,15 +448,17 @@ def kernel_source_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def dram_traffic(kernel: str, units_per_launch: float):
+def dram_traffic(kernel: str, units_per_launch: float, workload: str = ""):
     """DRAM bytes (read + write) per launch from the committed ncu capture, scaled from the
     captured case to this launch by the work units it processes; None when there is no
-    capture or the kernel's source changed since it was taken."""
+    capture or the kernel's source changed since it was taken. A capture of the workload's
+    own launch shape ("kernel@workload") is preferred to the kernel's default one."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
-        d = json.load(open(p)).get(kernel)
+        t = json.load(open(p))
+        d = t.get("%s@%s" % (kernel, workload)) or t.get(kernel)
         if not d or d.get("source_sha") != kernel_source_sha(kernel):
             return None
         return d["dram_bytes_per_unit"] * units_per_launch
@@ -660,7 +662,7 @@ def run_vst(args, dist):
                      "config": workload_config(args.workload, spec),
                      "roofline": {"kernel": "enc_attn_kernel", "bound": "tensor", "achieved": achieved, "peak": tf,
                                   "unit": "TFLOP/s", "frac": achieved / tf,
-                                  "traffic": dram_traffic("enc_attn_kernel", flops_per_launch),
+                                  "traffic": dram_traffic("enc_attn_kernel", flops_per_launch, args.workload),
                                   "peak_source": src + " bf16 burst", "launches": nl,
                                   "avg_launch_us": launch_us, "isolated_launch_us": 1e3 * kms / nl,
                                   "timing": TIMING_NOTE, "algorithmic_flops_per_launch": flops_per_launch},
