@@ -66,31 +66,34 @@ __device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], int c0, i
                 make_uint4(0u, 0u, 0u, 0u);
         return 0.f;
     }
-    float l4[4] = {0.f, 0.f, 0.f, 0.f};
+    // Paired fp32 operations (__ffma2_rn, __fadd2_rn) round each lane exactly as the scalar
+    // operation does; l01 and l23 hold the partial sums (l0, l1) and (l2, l3).
+    float2 l01 = make_float2(0.f, 0.f), l23 = make_float2(0.f, 0.f);
     const bool full = mask == 0xffffffffu;  // every column visible: no selects needed
+    const float2 sc2 = make_float2(scale_log2, scale_log2), ng2 = make_float2(neg, neg);
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
         float pv[8];
-        if (full) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                pv[e] = ex2(__fmaf_rn(__uint_as_float(sv[8 * qd + e]), scale_log2, neg));
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int j = 8 * qd + e;
-                const float p = ex2(__fmaf_rn(__uint_as_float(sv[j]), scale_log2, neg));
-                pv[e] = (mask >> j) & 1u ? p : 0.f;
+        for (int e = 0; e < 8; e += 2) {
+            const int j = 8 * qd + e;
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])), sc2, ng2);
+            pv[e] = ex2(x.x);
+            pv[e + 1] = ex2(x.y);
+            if (!full) {
+                pv[e] = (mask >> j) & 1u ? pv[e] : 0.f;
+                pv[e + 1] = (mask >> (j + 1)) & 1u ? pv[e + 1] : 0.f;
             }
         }
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            l4[(8 * qd + e) & 3] = __fadd_rn(l4[(8 * qd + e) & 3], pv[e]);
+        l01 = __fadd2_rn(l01, make_float2(pv[0], pv[1]));
+        l23 = __fadd2_rn(l23, make_float2(pv[2], pv[3]));
+        l01 = __fadd2_rn(l01, make_float2(pv[4], pv[5]));
+        l23 = __fadd2_rn(l23, make_float2(pv[6], pv[7]));
         const uint4 w = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
                                    pack_bf16(pv[6], pv[7]));
         *reinterpret_cast<uint4*>(sP + (q >> 1) * kTileBytes + sw128_offset(row, (q & 1) * 4 + qd)) = w;
     }
-    return __fadd_rn(__fadd_rn(l4[0], l4[1]), __fadd_rn(l4[2], l4[3]));
+    return __fadd_rn(__fadd_rn(l01.x, l01.y), __fadd_rn(l23.x, l23.y));
 }
 
 // Merge of a tile-local softmax state (mt, lt, ot) into a running state (m, l, o):
@@ -109,9 +112,14 @@ __device__ __forceinline__ FoldCoef fold_coef(float m, float mt)
 template <int N>
 __device__ __forceinline__ void fold_apply(float* o, const float* ot, const FoldCoef& f)
 {
+    static_assert(N % 2 == 0, "dims in pairs");
+    const float2 a2 = make_float2(f.a, f.a), b2 = make_float2(f.b, f.b);
 #pragma unroll
-    for (int d = 0; d < N; ++d)
-        o[d] = __fmaf_rn(o[d], f.a, __fmul_rn(ot[d], f.b));
+    for (int d = 0; d < N; d += 2) {
+        const float2 r = __ffma2_rn(make_float2(o[d], o[d + 1]), a2, __fmul2_rn(make_float2(ot[d], ot[d + 1]), b2));
+        o[d] = r.x;
+        o[d + 1] = r.y;
+    }
 }
 
 __device__ __forceinline__ void fold_finish(float& m, float& l, float lt, const FoldCoef& f)
@@ -177,12 +185,15 @@ template <int N>
 __device__ __forceinline__ void store_out(__nv_bfloat16* orow, const float* o, float l, int d0)
 {
     const float inv = __frcp_rn(l);
+    const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
     for (int c = 0; c < N / 8; ++c) {
         uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16(__fmul_rn(o[8 * c + 2 * e], inv), __fmul_rn(o[8 * c + 2 * e + 1], inv));
+        for (int e = 0; e < 4; ++e) {
+            const float2 y = __fmul2_rn(make_float2(o[8 * c + 2 * e], o[8 * c + 2 * e + 1]), inv2);
+            w[e] = pack_bf16(y.x, y.y);
+        }
         *reinterpret_cast<uint4*>(orow + d0 + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
