@@ -73,7 +73,7 @@ struct EncAttnJob {
     const CUtensorMap* tmap_k;  // over the K ring, dims {D, R, Hk}, box {64, 128, 1}, SW128
     const CUtensorMap* tmap_v;
     float* part_ml;          // split mode scratch: [H][split_tiles][128][2] (m_t, l_t)
-    float* part_o;           // split mode scratch: [H][split_tiles][128][D]
+    float* part_o;           // split mode scratch: [H][split_tiles][4 quarters][128][D / 4]
     unsigned* counters;      // split mode: [H] tiles finished per head
     int* err;
     long long pos0;          // absolute position of row 0
