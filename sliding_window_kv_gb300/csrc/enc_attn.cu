@@ -41,23 +41,33 @@ namespace vst {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kSoftmaxThreads = 256;               // warps 0-7: two threads per query row
+constexpr int kThreads = kSoftmaxThreads + 32;        // warp 8: TMA and MMA issue
 constexpr int kD = 64;
 constexpr int kDh = kD / 2;                            // output dims per thread
 constexpr uint32_t kTileBytes = 128u * 128u;           // 128 rows x 128 B
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;
-constexpr uint32_t kOffV = kOffK + kTileBytes;
-constexpr uint32_t kOffP = kOffV + kTileBytes;         // two 64-key blocks
-constexpr uint32_t kOffRed = kOffP + 2 * kTileBytes;   // float [2][2 halves][128]: row max / sum halves
-constexpr uint32_t kOffBar = kOffRed + 2 * 2 * 128 * 4;
-constexpr uint32_t kSmemBytes = kOffBar + 64 + 1024;   // + slack to align the base to 1024
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTmS = 0;    // S tile: columns [0, 128)
-constexpr uint32_t kTmO = 128;  // O tile: columns [128, 192)
+constexpr uint32_t kOffV = kOffK + kTileBytes;         // two V buffers
+constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;     // two 64-key blocks
+constexpr uint32_t kOffRedM = kOffP + 2 * kTileBytes;  // float [2 tile parities][2 halves][128]
+constexpr uint32_t kOffRedL = kOffRedM + 2 * 2 * 128 * 4;
+constexpr uint32_t kOffBar = kOffRedL + 2 * 2 * 128 * 4;
+constexpr int kNumBars = 11;
+constexpr uint32_t kSmemBytes = kOffBar + 8 * kNumBars + 1024;  // + slack to align the base to 1024
+constexpr uint32_t kTmemCols = 256;  // two 128-column buffers: S_t, then O_t in its first 64 columns
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64, false, true);
+
+// mbarriers (index = bit in the phase and pending masks)
+constexpr int kBarK = 0;      // K tile landed (TMA)
+constexpr int kBarV = 1;      // 1, 2: V buffer landed (TMA)
+constexpr int kBarS = 3;      // 3, 4: S in TMEM buffer ready (MMA commit)
+constexpr int kBarO = 5;      // 5, 6: O in TMEM buffer ready (MMA commit)
+constexpr int kBarFree = 7;   // 7, 8: O in TMEM buffer read by all eight softmax warps
+constexpr int kBarP = 9;      // P written by all eight softmax warps
+constexpr int kBarQ = 10;     // Q' written by all eight softmax warps
 
 }  // namespace
 
@@ -71,8 +81,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const EncAttnJob& job = p.jobs[blockIdx.z];
     const int h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r = 32 * (warp & 3) + lane;  // TMEM lane = query row of this thread
-    const int half = warp >> 2;            // half of the row
     const int row0 = (int)blockIdx.x * 128;
     const int nrows = min(128, c.n_rows - row0);
     const long long p_first = job.pos0 + row0;
@@ -82,188 +90,279 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* sQ = smem + kOffQ;
-    uint8_t* sK = smem + kOffK;
-    uint8_t* sV = smem + kOffV;
     uint8_t* sP = smem + kOffP;
-    float* red_m = reinterpret_cast<float*>(smem + kOffRed);  // [2 halves][128]
-    float* red_l = red_m + 2 * 128;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    const uint32_t bar_k = smem_u32(&bars[0]), bar_v = smem_u32(&bars[1]), bar_m = smem_u32(&bars[2]);
+    float* red_m = reinterpret_cast<float*>(smem + kOffRedM);  // [parity][half][128]
+    float* red_l = reinterpret_cast<float*>(smem + kOffRedL);
+    const uint32_t bar0 = smem_u32(smem + kOffBar);
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
-    // Prologue. The first ring tiles may be requested before the previous kernel in the
-    // stream has finished when the host says that kernel did not touch this ring (early);
-    // everything else waits for it.
-    auto issue_k = [&](long long t) {
-        mbar_arrive_expect_tx(bar_k, kTileBytes);
-        tma_load_3d(smem_u32(sK), job.tmap_k, bar_k, 0, (int)(t * 128 - job.abs_base), h);
-    };
-    auto issue_v = [&](long long t) {
-        mbar_arrive_expect_tx(bar_v, kTileBytes);
-        tma_load_3d(smem_u32(sV), job.tmap_v, bar_v, 0, (int)(t * 128 - job.abs_base), h);
-    };
-    if (tid == 0) {
-        mbar_init(bar_k, 1);
-        mbar_init(bar_v, 1);
-        mbar_init(bar_m, 1);
-        fence_mbar_init();
-        tmap_acquire(job.tmap_k);
-        tmap_acquire(job.tmap_v);
-        if (c.early) {
-            issue_k(t_lo);
-            issue_v(t_lo);
+    if (warp == 8) {
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < kNumBars; ++i)
+                mbar_init(bar(i), i >= kBarFree ? 8u : 1u);
+            fence_mbar_init();
         }
-    }
-    __syncwarp();
-    if (warp == 0) {
+        __syncwarp();
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
         tmem_relinquish();
     }
-    griddep_wait();
-    if (tid == 0 && !c.early) {
-        issue_k(t_lo);
-        issue_v(t_lo);
-    }
-    __syncwarp();
-
-    // ---- this thread's half of query row r, rotated, into sQ
-    const long long pq = p_first + r;
-    const bool row_real = r < nrows;
-    if (row_real) {
-        const __nv_bfloat16* qrow = job.q + ((long long)(row0 + r) * c.H + h) * kD;
-        enc::rotate_quarter(qrow, c.rope + pq * (kD / 2), sQ, r, 2 * half);
-        enc::rotate_quarter(qrow, c.rope + pq * (kD / 2), sQ, r, 2 * half + 1);
-    } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)  // chunks {q, 4 + q} of quarters q = 2 half, 2 half + 1
-            *reinterpret_cast<uint4*>(sQ + sw128_offset(r, (e >> 1) * 4 + 2 * half + (e & 1))) = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();  // Q' (generic stores) before the MMAs read it
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    int aborted = 0;
 
-    float o[kDh];
-#pragma unroll
-    for (int d = 0; d < kDh; ++d)
-        o[d] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
-    uint32_t ph_k = 0, ph_v = 0, ph_m = 0;
-    bool pend_k = tid == 0, pend_v = tid == 0;
-    int fail = 0, aborted = 0;
-
-    for (long long t = t_lo; t <= t_hi; ++t) {
-        // ---- K of tile t in smem, then S = Q K^T
-        if (!mbar_wait(bar_k, ph_k))
-            fail = 1;
-        ph_k ^= 1;
-        if (tid == 0)
-            pend_k = false;
-        tc_fence_before();
-        if (__syncthreads_or(fail)) {
-            aborted = 1;
-            break;
-        }
-        tc_fence_after();
-        if (tid == 0) {
+    if (warp == 8) {
+        // ================= control warp: TMA loads and MMA issue =================
+        // Key tile t uses TMEM buffer and V buffer (t - t_lo) & 1. Order of work for tile t:
+        //   S_t done      -> fetch K_{t+1} (one K buffer)
+        //   PV_{t-1} done -> fetch V_{t+1} into the buffer V_{t-1} used
+        //   K_{t+1} landed, O_{t-1} read by every softmax warp -> S_{t+1} = Q' K_{t+1}^T
+        //   P_t written, V_t landed -> O_t = P_t V_t into the first 64 columns of S_t's buffer
+        // The whole warp runs this code; the elected lane alone issues copies and MMAs.
+        const uint32_t e = elect_one_sync();
+        uint32_t ph = 0, pend = 0;  // pend: copies and MMAs started and not yet seen complete
+        int fail = 0;
+        auto wait = [&](int i) {  // the same answer in every lane
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(i), (ph >> i) & 1u));
+            if (ok) {
+                ph ^= 1u << i;
+                pend &= ~(1u << i);
+            }
+            return ok;
+        };
+        auto issue_k = [&](long long t) {
+            if (e) {
+                mbar_arrive_expect_tx(bar(kBarK), kTileBytes);
+                tma_load_3d(smem_u32(smem + kOffK), job.tmap_k, bar(kBarK), 0, (int)(t * 128 - job.abs_base), h);
+            }
+            pend |= 1u << kBarK;
+        };
+        auto issue_v = [&](long long t) {
+            const int vb = (int)((t - t_lo) & 1);
+            if (e) {
+                mbar_arrive_expect_tx(bar(kBarV + vb), kTileBytes);
+                tma_load_3d(smem_u32(smem + kOffV) + vb * kTileBytes, job.tmap_v, bar(kBarV + vb), 0,
+                            (int)(t * 128 - job.abs_base), h);
+            }
+            pend |= 1u << (kBarV + vb);
+        };
+        auto issue_s = [&](long long t) {
+            const int b = (int)((t - t_lo) & 1);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + kTmS, smem_desc_sw128(smem_u32(sQ) + 32 * kk, 16, 1024),
-                            smem_desc_sw128(smem_u32(sK) + 32 * kk, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-            mma_commit(bar_m);
-        }
-        __syncwarp();
-        if (!mbar_wait(bar_m, ph_m))
-            fail = 1;
-        ph_m ^= 1;
-        tc_fence_after();
-        if (tid == 0 && !fail && t < t_hi) {  // K buffer is free: fetch the next tile's K
-            issue_k(t + 1);
-            pend_k = true;
-        }
-        __syncwarp();
-
-        // ---- tile-local softmax of this thread's half of row r
-        int lo = 1, hi = 0;  // visible columns of row r in this tile; empty unless r is real
-        if (row_real) {
-            lo = (int)max(-1LL, min(128LL, pq - c.W + 1 - t * 128));
-            hi = (int)max(-1LL, min(128LL, pq - t * 128));
-        }
-        // both quarters of this half-row in one TMEM round trip, kept for the exp pass
-        uint32_t sa[32], sb[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + kTmS + 64 * half, sa);
-        tmem_ld_32x32b_x32(tmem + lane_base + kTmS + 64 * half + 32, sb);
-        tmem_ld_wait();
-        const float mh = fmaxf(enc::quarter_max(sa, 64 * half, lo, hi), enc::quarter_max(sb, 64 * half + 32, lo, hi));
-        red_m[half * 128 + r] = mh;
-        __syncthreads();
-        const float mt = __fmul_rn(fmaxf(red_m[r], red_m[128 + r]), c.scale_log2);  // -inf: row sees nothing
-        const float la = enc::quarter_exp(sa, 64 * half, lo, hi, c.scale_log2, -mt, sP, r);
-        const float lb = enc::quarter_exp(sb, 64 * half + 32, lo, hi, c.scale_log2, -mt, sP, r);
-        red_l[half * 128 + r] = __fadd_rn(la, lb);
-
-        // ---- V of tile t in smem, then O_t = P V
-        if (!mbar_wait(bar_v, ph_v))
-            fail = 1;
-        ph_v ^= 1;
-        if (tid == 0)
-            pend_v = false;
-        fence_proxy_async_smem();  // P (generic stores) before the MMA reads it
-        tc_fence_before();
-        if (__syncthreads_or(fail)) {
-            aborted = 1;
-            break;
-        }
-        tc_fence_after();
-        if (tid == 0) {
+                mma_bf16_ss_if(tmem + 128u * b, smem_desc_sw128(smem_u32(sQ) + 32 * kk, 16, 1024),
+                               smem_desc_sw128(smem_u32(smem + kOffK) + 32 * kk, 16, 1024), kIdescS, kk > 0 ? 1u : 0u, e);
+            mma_commit_if(bar(kBarS + b), e);
+            pend |= 1u << (kBarS + b);
+        };
+        auto issue_pv = [&](long long t) {
+            const int b = (int)((t - t_lo) & 1);
+            const uint32_t v = smem_u32(smem + kOffV) + b * kTileBytes;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ss(tmem + kTmO,
-                            smem_desc_sw128(smem_u32(sP) + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024),
-                            smem_desc_sw128(smem_u32(sV) + 2048 * kk, kTileBytes, 1024), kIdescO, kk > 0 ? 1u : 0u);
-            mma_commit(bar_m);
+                mma_bf16_ss_if(tmem + 128u * b,
+                               smem_desc_sw128(smem_u32(sP) + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024),
+                               smem_desc_sw128(v + 2048 * kk, kTileBytes, 1024), kIdescO, kk > 0 ? 1u : 0u, e);
+            mma_commit_if(bar(kBarO + b), e);
+            pend |= 1u << (kBarO + b);
+        };
+        auto issue_first = [&]() {
+            issue_k(t_lo);
+            issue_v(t_lo);
+            if (t_lo < t_hi)
+                issue_v(t_lo + 1);
+        };
+
+        // The first ring tiles may be requested before the previous kernel in the stream has
+        // finished when the host says that kernel did not touch this ring (early).
+        if (e) {
+            tmap_acquire(job.tmap_k);
+            tmap_acquire(job.tmap_v);
         }
-        __syncwarp();
-        const float lt = __fadd_rn(red_l[r], red_l[128 + r]);
-        if (!mbar_wait(bar_m, ph_m))
+        if (c.early)
+            issue_first();
+        griddep_wait();
+        if (!c.early)
+            issue_first();
+        if (!wait(kBarQ) || !wait(kBarK))
             fail = 1;
-        ph_m ^= 1;
-        tc_fence_after();
-        if (tid == 0 && !fail && t < t_hi) {  // V buffer is free: fetch the next tile's V
-            issue_v(t + 1);
-            pend_v = true;
+        else
+            issue_s(t_lo);
+
+        for (long long t = t_lo; !fail && t <= t_hi; ++t) {
+            const int b = (int)((t - t_lo) & 1), nb = b ^ 1;
+            if (t < t_hi) {
+                if (!wait(kBarS + b)) {
+                    fail = 1;
+                    break;
+                }
+                issue_k(t + 1);
+            }
+            if (t > t_lo && t < t_hi) {
+                if (!wait(kBarO + nb)) {
+                    fail = 1;
+                    break;
+                }
+                issue_v(t + 1);
+            }
+            if (t < t_hi) {
+                if (!wait(kBarK) || (t > t_lo && !wait(kBarFree + nb))) {
+                    fail = 1;
+                    break;
+                }
+                tc_fence_after();
+                issue_s(t + 1);
+            }
+            if (!wait(kBarP) || !wait(kBarV + b)) {
+                fail = 1;
+                break;
+            }
+            tc_fence_after();
+            issue_pv(t);
+        }
+        if (fail) {
+            // A bounded wait gave up: record it and let copies and MMAs in flight land.
+            if (e)
+                atomicExch(job.err, kErrTimeout);
+#pragma unroll
+            for (int i = 0; i < kBarFree; ++i)
+                if ((pend >> i) & 1u)
+                    mbar_wait(bar(i), (ph >> i) & 1u);
         }
         __syncwarp();
+        griddep_launch_dependents();
+    } else {
+        // ================= softmax warps: two threads per query row =================
+        // Thread (r, half) owns score columns [64 half, 64 half + 64), output dims
+        // [32 half, 32 half + 32) and RoPE pairs [16 half, 16 half + 16) of query row r.
+        const int r = 32 * (warp & 3) + lane;  // TMEM lane = query row of this thread
+        const int half = warp >> 2;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const long long pq = p_first + r;
+        const bool row_real = r < nrows;
 
-        // ---- O_t of this thread's dims, folded into the running state
-        uint32_t ov[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + kTmO + kDh * half, ov);
-        tmem_ld_wait();
-        if (mt != -INFINITY) {
-            float ot[kDh];
+        griddep_wait();
+        if (row_real) {
+            const __nv_bfloat16* qrow = job.q + ((long long)(row0 + r) * c.H + h) * kD;
+            enc::rotate_quarter(qrow, c.rope + pq * (kD / 2), sQ, r, 2 * half);
+            enc::rotate_quarter(qrow, c.rope + pq * (kD / 2), sQ, r, 2 * half + 1);
+        } else {
 #pragma unroll
-            for (int d = 0; d < kDh; ++d)
-                ot[d] = __uint_as_float(ov[d]);
-            enc::fold_tile<kDh>(m_run, l_run, o, mt, lt, ot);
+            for (int e = 0; e < 4; ++e)  // chunks {q, 4 + q} of quarters q = 2 half, 2 half + 1
+                *reinterpret_cast<uint4*>(sQ + sw128_offset(r, (e >> 1) * 4 + 2 * half + (e & 1))) = make_uint4(0, 0, 0, 0);
         }
-        tc_fence_before();
-    }
+        fence_proxy_async_smem();  // Q' (generic stores) before the MMAs read it
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar(kBarQ));
 
-    griddep_launch_dependents();
-    if (aborted && tid == 0) {
-        // A bounded wait gave up: record it and let copies still in flight land.
-        atomicExch(job.err, kErrTimeout);
-        if (pend_k)
-            mbar_wait(bar_k, ph_k);
-        if (pend_v)
-            mbar_wait(bar_v, ph_v);
+        float o[kDh];
+#pragma unroll
+        for (int d = 0; d < kDh; ++d)
+            o[d] = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;
+        float mt_prev = -INFINITY;  // tile-local max of the previous tile, folded one tile late
+        uint32_t ph = 0;
+        int fail = 0;
+        // o <- fold(o, O_t) for tile t in TMEM buffer b, with m_t = mt and l_t from red_l
+        auto fold_from = [&](int b, float mt) {
+            if (mbar_wait(bar(kBarO + b), (ph >> (kBarO + b)) & 1u))
+                ph ^= 1u << (kBarO + b);
+            else
+                fail = 1;
+            tc_fence_after();
+            const float lt = __fadd_rn(red_l[(b * 2 + 0) * 128 + r], red_l[(b * 2 + 1) * 128 + r]);
+            uint32_t ov[32];
+            tmem_ld_32x32b_x32(tmem + 128u * b + lane_base + kDh * half, ov);
+            tmem_ld_wait();
+            if (mt != -INFINITY) {
+                float ot[kDh];
+#pragma unroll
+                for (int d = 0; d < kDh; ++d)
+                    ot[d] = __uint_as_float(ov[d]);
+                enc::fold_tile<kDh>(m_run, l_run, o, mt, lt, ot);
+            }
+        };
+
+        for (long long t = t_lo; t <= t_hi; ++t) {
+            const int b = (int)((t - t_lo) & 1), nb = b ^ 1;
+            const uint32_t tm_b = tmem + 128u * b + lane_base + 64 * half;
+            if (mbar_wait(bar(kBarS + b), (ph >> (kBarS + b)) & 1u))
+                ph ^= 1u << (kBarS + b);
+            else
+                fail = 1;
+            tc_fence_after();
+
+            // ---- tile-local row max of this thread's half of row r, one quarter at a time
+            int lo = 1, hi = 0;  // visible columns of row r in this tile; empty unless r is real
+            if (row_real) {
+                lo = (int)max(-1LL, min(128LL, pq - c.W + 1 - t * 128));
+                hi = (int)max(-1LL, min(128LL, pq - t * 128));
+            }
+            float mh;
+            {
+                uint32_t sv[32];
+                tmem_ld_32x32b_x32(tm_b, sv);
+                tmem_ld_wait();
+                mh = enc::quarter_max(sv, 64 * half, lo, hi);
+                tmem_ld_32x32b_x32(tm_b + 32, sv);
+                tmem_ld_wait();
+                mh = fmaxf(mh, enc::quarter_max(sv, 64 * half + 32, lo, hi));
+            }
+            red_m[(b * 2 + half) * 128 + r] = mh;
+            if (bar_sync_or(1, kSoftmaxThreads, fail)) {
+                aborted = 1;
+                break;
+            }
+            const float mt = __fmul_rn(fmaxf(red_m[(b * 2) * 128 + r], red_m[(b * 2 + 1) * 128 + r]), c.scale_log2);
+
+            // ---- fold of the previous tile (its PV ran while this tile's max was taken)
+            if (t > t_lo) {
+                fold_from(nb, mt_prev);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(kBarFree + nb));
+            }
+
+            // ---- tile-local exps (P of the previous tile has been consumed: its O is ready)
+            float lh;
+            {
+                uint32_t sv[32];
+                tmem_ld_32x32b_x32(tm_b, sv);
+                tmem_ld_wait();
+                lh = enc::quarter_exp(sv, 64 * half, lo, hi, c.scale_log2, -mt, sP, r);
+                tmem_ld_32x32b_x32(tm_b + 32, sv);
+                tmem_ld_wait();
+                lh = __fadd_rn(lh, enc::quarter_exp(sv, 64 * half + 32, lo, hi, c.scale_log2, -mt, sP, r));
+            }
+            red_l[(b * 2 + half) * 128 + r] = lh;
+            fence_proxy_async_smem();  // P (generic stores) before the MMA reads it
+            tc_fence_before();         // and S_t read before O_t overwrites it
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(kBarP));
+            mt_prev = mt;
+        }
+        // ---- fold of the last tile
+        if (bar_sync_or(1, kSoftmaxThreads, fail))  // also orders red_l of the last tile
+            aborted = 1;
+        if (!aborted) {
+            fold_from((int)((t_hi - t_lo) & 1), mt_prev);
+            if (bar_sync_or(1, kSoftmaxThreads, fail))
+                aborted = 1;
+        }
+        if (aborted && tid == 0)
+            atomicExch(job.err, kErrTimeout);
+        griddep_launch_dependents();
+        if (!aborted && row_real)
+            enc::store_out<kDh>(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, kDh * half);
     }
-    if (!aborted && row_real)
-        enc::store_out<kDh>(job.out + ((long long)(row0 + r) * c.H + h) * kD, o, l_run, kDh * half);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }

@@ -161,6 +161,45 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// One lane of a converged warp: 1 in the elected lane, 0 in the others. The predicated
+// issue helpers below let a whole warp run the issue code together and only the elected
+// lane execute the instruction, which keeps the warp converged (a single lane branching off
+// to issue pays several times more per instruction).
+__device__ __forceinline__ uint32_t elect_one_sync()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred;
+}
+
+// mma_bf16_ss executed only where `pred` is non-zero.
+__device__ __forceinline__ void mma_bf16_ss_if(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate, uint32_t pred)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 e, %5, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(pred)
+        : "memory");
+}
+
+// mma_commit executed only where `pred` is non-zero.
+__device__ __forceinline__ void mma_commit_if(uint32_t bar, uint32_t pred)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "setp.ne.b32 e, %1, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"(pred)
+        : "memory");
+}
+
 // Arrive once on `bar` when all tcgen05 operations issued so far by this thread complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
