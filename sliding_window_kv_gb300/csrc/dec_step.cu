@@ -219,8 +219,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int rr_new = (int)(pos - tau_new * kTile);  // row of the new key in its tile
 
-    // Warp 0: wait for tile i's K, patch the new key in if it is there, and (lane 0) issue
-    // S^T for it into S buffer i & 1. Returns false if the wait gave up.
+    // Warp 0: wait for tile i's K, patch the new key in if it is there, and (the elected lane)
+    // issue S^T for it into S buffer i & 1. Returns false if the wait gave up.
+    const uint32_t elect = warp == 0 ? elect_one_sync() : 0u;
     auto prepare_and_issue_s = [&](int i) -> bool {
         bool ok = mbar_wait(bar_k, parity(i));
         if (ok && has_new && tau_lo + i == tau_new && lane < 16) {
@@ -231,15 +232,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncwarp();
         ok = __all_sync(0xFFFFFFFFu, ok);
-        if (ok && lane == 0) {
+        if (ok) {  // the whole warp, converged; the elected lane issues
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t ad = smem_desc_sw128(smem_u32(sK) + (kk >> 2) * kBox + 32 * (kk & 3), 16, 1024);
                 const uint64_t bd = smem_desc_sw128(smem_u32(sQ) + (kk >> 2) * 2048 + 32 * (kk & 3), 16, 1024);
-                mma_bf16_ss(tmem + 16 * (i & 1), ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+                mma_bf16_ss_if(tmem + 16 * (i & 1), ad, bd, kIdescS, kk > 0 ? 1u : 0u, elect);
             }
-            mma_commit(bar_s(i & 1));
+            mma_commit_if(bar_s(i & 1), elect);
         }
         return ok;
     };
@@ -296,14 +297,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         tc_fence_after();
         const float lt = __fadd_rn(__fadd_rn(red_l[hh * 4], red_l[hh * 4 + 1]), __fadd_rn(red_l[hh * 4 + 2], red_l[hh * 4 + 3]));
-        if (tid == 0) {
+        if (warp == 0) {  // converged after the barrier; the elected lane issues
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t ad = smem_desc_sw128(smem_u32(sV) + 2048 * kk, kBox, 1024);
                 const uint64_t bd = smem_desc_sw128(smem_u32(sP) + (kk >> 2) * 2048 + 32 * (kk & 3), 16, 1024);
-                mma_bf16_ss(tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
+                mma_bf16_ss_if(tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u, elect);
             }
-            mma_commit(bar_o);
+            mma_commit_if(bar_o, elect);
         }
         if (!mbar_wait(bar_o, ph_o))
             fail = 1;

@@ -144,26 +144,27 @@ __device__ __forceinline__ void unstage_row(const Cta& s, bool is_k)
     *reinterpret_cast<uint4*>(dst + sw128_offset(s.r, ch1)) = *reinterpret_cast<const uint4*>(src + sw128_offset(s.r, ch1));
 }
 
-__device__ __forceinline__ void issue_s_mma(const Cta& s)
+// Issued by the whole of warp 0 (converged); the elected lane `e` executes the MMAs.
+__device__ __forceinline__ void issue_s_mma(const Cta& s, uint32_t e)
 {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
         const uint64_t ad = smem_desc_sw128(smem_u32(s.sQ) + 32 * kk, 16, 1024);
         const uint64_t bd = smem_desc_sw128(smem_u32(s.sK) + 32 * kk, 16, 1024);
-        mma_bf16_ss(s.tmem + kTmS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+        mma_bf16_ss_if(s.tmem + kTmS, ad, bd, kIdescS, kk > 0 ? 1u : 0u, e);
     }
-    mma_commit(s.bar_m);
+    mma_commit_if(s.bar_m, e);
 }
 
-__device__ __forceinline__ void issue_o_mma(const Cta& s)
+__device__ __forceinline__ void issue_o_mma(const Cta& s, uint32_t e)
 {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         const uint64_t ad = smem_desc_sw128(smem_u32(s.sP) + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024);
         const uint64_t bd = smem_desc_sw128(smem_u32(s.sV) + 2048 * kk, kTileBytes, 1024);
-        mma_bf16_ss(s.tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
+        mma_bf16_ss_if(s.tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u, e);
     }
-    mma_commit(s.bar_m);
+    mma_commit_if(s.bar_m, e);
 }
 
 }  // namespace
@@ -256,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t ph_k = 0, ph_v = 0, ph_m = 0;
     bool pend_k = s.tid == 0, pend_v = s.tid == 0;
+    const uint32_t elect = s.warp == 0 ? elect_one_sync() : 0u;  // lane of warp 0 that issues MMAs
     int fail = 0, aborted = 0;
 
     for (long long t = t_begin; t <= t_end; ++t) {
@@ -281,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
         tc_fence_after();
-        if (s.tid == 0)
-            issue_s_mma(s);
+        if (s.warp == 0)
+            issue_s_mma(s, elect);
         if (!mbar_wait(s.bar_m, ph_m))
             fail = 1;
         ph_m ^= 1;
@@ -331,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
         tc_fence_after();
-        if (s.tid == 0)
-            issue_o_mma(s);
+        if (s.warp == 0)
+            issue_o_mma(s, elect);
         const float lt = __fadd_rn(__fadd_rn(s.red_l[r], s.red_l[128 + r]), __fadd_rn(s.red_l[256 + r], s.red_l[384 + r]));
         if (!mbar_wait(s.bar_m, ph_m))
             fail = 1;
