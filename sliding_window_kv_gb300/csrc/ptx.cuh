@@ -77,6 +77,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 // Named barrier over `count` threads (a multiple of 32) with an OR of `pred` across them.
 __device__ __forceinline__ int bar_sync_or(int id, int count, int pred)
 {
+    __syncwarp();  // .aligned: the whole warp executes it together
     int r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
@@ -123,6 +124,7 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
 // Executed by one whole warp.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
+    __syncwarp();  // .aligned: the whole warp executes it together
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                  "r"(ncols)
                  : "memory");
@@ -130,11 +132,13 @@ __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 
 __device__ __forceinline__ void tmem_relinquish()
 {
+    __syncwarp();  // .aligned: the whole warp executes it together
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 {
+    __syncwarp();  // .aligned: the whole warp executes it together
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                  : "memory");
 }
@@ -211,6 +215,7 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 // Each thread of the warp reads 32 consecutive fp32 columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
 {
+    __syncwarp();  // .aligned: the whole warp executes it together
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -226,6 +231,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 // Each thread of the warp reads 16 consecutive fp32 columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
 {
+    __syncwarp();  // .aligned: the whole warp executes it together
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
@@ -238,6 +244,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 // Each thread of the warp reads 4 consecutive fp32 columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[4])
 {
+    __syncwarp();  // .aligned: the whole warp executes it together
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(taddr));
@@ -245,6 +252,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[
 
 __device__ __forceinline__ uint32_t tmem_ld_32x32b_x1(uint32_t taddr)
 {
+    __syncwarp();  // .aligned: the whole warp executes it together
     uint32_t r;
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
     return r;
@@ -252,6 +260,7 @@ __device__ __forceinline__ uint32_t tmem_ld_32x32b_x1(uint32_t taddr)
 
 __device__ __forceinline__ void tmem_ld_wait()
 {
+    __syncwarp();  // .aligned: the whole warp executes it together
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
