@@ -77,6 +77,7 @@ __device__ __forceinline__ float warp_sum(float x)
 // Barrier over the 4 warps (128 threads) of one head group.
 __device__ __forceinline__ void head_sync(int hh)
 {
+    __syncwarp();  // .aligned: the whole warp executes it together
     asm volatile("bar.sync %0, 128;" ::"r"(1 + hh) : "memory");
 }
 

@@ -53,7 +53,7 @@ constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;     // two 64-key blocks
 constexpr uint32_t kOffRedM = kOffP + 2 * kTileBytes;  // float [2 tile parities][2 halves][128]
 constexpr uint32_t kOffRedL = kOffRedM + 2 * 2 * 128 * 4;
 constexpr uint32_t kOffBar = kOffRedL + 2 * 2 * 128 * 4;
-constexpr int kNumBars = 11;
+constexpr int kNumBars = 12;
 constexpr uint32_t kSmemBytes = kOffBar + 8 * kNumBars + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 256;  // two 128-column buffers: S_t, then O_t in its first 64 columns
 
@@ -66,8 +66,8 @@ constexpr int kBarV = 1;      // 1, 2: V buffer landed (TMA)
 constexpr int kBarS = 3;      // 3, 4: S in TMEM buffer ready (MMA commit)
 constexpr int kBarO = 5;      // 5, 6: O in TMEM buffer ready (MMA commit)
 constexpr int kBarFree = 7;   // 7, 8: O in TMEM buffer read by all eight softmax warps
-constexpr int kBarP = 9;      // P written by all eight softmax warps
-constexpr int kBarQ = 10;     // Q' written by all eight softmax warps
+constexpr int kBarP = 9;      // 9, 10: P keys [64 half, 64 half + 64) written by the four warps of that half
+constexpr int kBarQ = 11;     // Q' written by all eight softmax warps
 
 }  // namespace
 
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
 #pragma unroll
             for (int i = 0; i < kNumBars; ++i)
-                mbar_init(bar(i), i >= kBarFree ? 8u : 1u);
+                mbar_init(bar(i), i == kBarP || i == kBarP + 1 ? 4u : i >= kBarFree ? 8u : 1u);
             fence_mbar_init();
         }
         __syncwarp();
@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         //   S_t done      -> fetch K_{t+1} (one K buffer)
         //   PV_{t-1} done -> fetch V_{t+1} into the buffer V_{t-1} used
         //   K_{t+1} landed, O_{t-1} read by every softmax warp -> S_{t+1} = Q' K_{t+1}^T
-        //   P_t written, V_t landed -> O_t = P_t V_t into the first 64 columns of S_t's buffer
+        //   V_t landed, P_t keys [0, 64) written -> first four K steps of O_t = P_t V_t, into the
+        //   first 64 columns of S_t's buffer; P_t keys [64, 128) written -> the last four
         // The whole warp runs this code; the elected lane alone issues copies and MMAs.
         const uint32_t e = elect_one_sync();
         uint32_t ph = 0, pend = 0;  // pend: copies and MMAs started and not yet seen complete
@@ -157,16 +158,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             mma_commit_if(bar(kBarS + b), e);
             pend |= 1u << (kBarS + b);
         };
-        auto issue_pv = [&](long long t) {
+        auto issue_pv = [&](long long t, int kh) {  // K steps [4 kh, 4 kh + 4): keys [64 kh, 64 kh + 64)
             const int b = (int)((t - t_lo) & 1);
             const uint32_t v = smem_u32(smem + kOffV) + b * kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16_ss_if(tmem + 128u * b,
-                               smem_desc_sw128(smem_u32(sP) + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024),
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int kk = 4 * kh + k4;
+                mma_bf16_ss_if(tmem + 128u * b, smem_desc_sw128(smem_u32(sP) + kh * kTileBytes + 32 * k4, 16, 1024),
                                smem_desc_sw128(v + 2048 * kk, kTileBytes, 1024), kIdescO, kk > 0 ? 1u : 0u, e);
-            mma_commit_if(bar(kBarO + b), e);
-            pend |= 1u << (kBarO + b);
+            }
+            if (kh == 1) {
+                mma_commit_if(bar(kBarO + b), e);
+                pend |= 1u << (kBarO + b);
+            }
         };
         auto issue_first = [&]() {
             issue_k(t_lo);
@@ -215,12 +219,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc_fence_after();
                 issue_s(t + 1);
             }
-            if (!wait(kBarP) || !wait(kBarV + b)) {
+            if (!wait(kBarV + b) || !wait(kBarP)) {
                 fail = 1;
                 break;
             }
             tc_fence_after();
-            issue_pv(t);
+            issue_pv(t, 0);
+            if (!wait(kBarP + 1)) {
+                fail = 1;
+                break;
+            }
+            tc_fence_after();
+            issue_pv(t, 1);
         }
         if (fail) {
             // A bounded wait gave up: record it and let copies and MMAs in flight land.
@@ -239,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // [32 half, 32 half + 32) and RoPE pairs [16 half, 16 half + 16) of query row r.
         const int r = 32 * (warp & 3) + lane;  // TMEM lane = query row of this thread
         const int half = warp >> 2;
+        const int pair_bar = 1 + (warp & 3);   // named barrier of warps w and w + 4 (the same rows)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const long long pq = p_first + r;
         const bool row_real = r < nrows;
@@ -312,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 mh = fmaxf(mh, enc::quarter_max(sv, 64 * half + 32, lo, hi));
             }
             red_m[(b * 2 + half) * 128 + r] = mh;
-            if (bar_sync_or(1, kSoftmaxThreads, fail)) {
+            if (bar_sync_or(pair_bar, 64, fail)) {
                 aborted = 1;
                 break;
             }
@@ -343,18 +354,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc_fence_before();         // and S_t read before O_t overwrites it
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar(kBarP));
+                mbar_arrive(bar(kBarP + half));
             mt_prev = mt;
         }
         // ---- fold of the last tile
-        if (bar_sync_or(1, kSoftmaxThreads, fail))  // also orders red_l of the last tile
+        if (bar_sync_or(pair_bar, 64, fail))  // also orders red_l of the last tile
             aborted = 1;
         if (!aborted) {
             fold_from((int)((t_hi - t_lo) & 1), mt_prev);
-            if (bar_sync_or(1, kSoftmaxThreads, fail))
+            if (bar_sync_or(pair_bar, 64, fail))
                 aborted = 1;
         }
-        if (aborted && tid == 0)
+        if (aborted && lane == 0)
             atomicExch(job.err, kErrTimeout);
         griddep_launch_dependents();
         if (!aborted && row_real)

@@ -4,7 +4,7 @@
 // 32-column quarters in the same order, so every shape produces the same bits.
 //
 // Row softmax of one 128-key tile, for a row whose visible columns are [lo, hi]:
-//   quarter max    max over the quarter's visible columns (4 interleaved partial maxima)
+//   quarter max    max over the quarter's visible columns (exact in any order)
 //   row max        max of the 4 quarter maxima (exact in any order), m_t = max * log2e/sqrt(D)
 //   quarter sum    p = 2^(s * log2e/sqrt(D) - m_t) over the quarter (0 where not visible),
 //                  accumulated into 4 interleaved partial sums, combined (l0+l1)+(l2+l3)
@@ -30,25 +30,45 @@ __device__ __forceinline__ uint32_t visible_mask(int c0, int lo, int hi)
     return below_b & ~below_a;
 }
 
+// Three-input maximum (one instruction); exact, so any grouping gives the same value.
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Max over the 32 values of x: four interleaved partial maxima of eight values each.
+__device__ __forceinline__ float max32(const float (&x)[32])
+{
+    float m4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float a = max3(x[k], x[k + 4], x[k + 8]);
+        const float b = max3(a, x[k + 12], x[k + 16]);
+        const float d = max3(b, x[k + 20], x[k + 24]);
+        m4[k] = fmaxf(d, x[k + 28]);
+    }
+    return fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
+}
+
 // Max over the visible columns of the quarter [c0, c0 + 32) held in sv.
 __device__ __forceinline__ float quarter_max(const uint32_t (&sv)[32], int c0, int lo, int hi)
 {
     const uint32_t mask = visible_mask(c0, lo, hi);
     if (mask == 0u)
         return -INFINITY;
-    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    if (mask == 0xffffffffu) {  // every column visible: the same maxima without the selects
+    float x[32];
+    if (mask == 0xffffffffu) {  // every column visible: the same maximum without the selects
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(sv[j]));
+            x[j] = __uint_as_float(sv[j]);
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float x = (mask >> j) & 1u ? __uint_as_float(sv[j]) : -INFINITY;
-            m4[j & 3] = fmaxf(m4[j & 3], x);
-        }
+        for (int j = 0; j < 32; ++j)
+            x[j] = (mask >> j) & 1u ? __uint_as_float(sv[j]) : -INFINITY;
     }
-    return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    return max32(x);
 }
 
 // Probabilities of the quarter [c0, c0 + 32) of row `row` (neg = -m_t): written as bf16
