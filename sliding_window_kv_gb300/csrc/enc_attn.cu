@@ -47,9 +47,9 @@ constexpr int kD = 64;
 constexpr int kDh = kD / 2;                            // output dims per thread
 constexpr uint32_t kTileBytes = 128u * 128u;           // 128 rows x 128 B
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;
-constexpr uint32_t kOffV = kOffK + kTileBytes;         // two V buffers
-constexpr uint32_t kOffP = kOffV + 2 * kTileBytes;     // two 64-key blocks
+constexpr uint32_t kOffK = kOffQ + kTileBytes;         // two K buffers
+constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;
+constexpr uint32_t kOffP = kOffV + kTileBytes;         // two 64-key blocks
 constexpr uint32_t kOffRedM = kOffP + 2 * kTileBytes;  // float [2 tile parities][2 halves][128]
 constexpr uint32_t kOffRedL = kOffRedM + 2 * 2 * 128 * 4;
 constexpr uint32_t kOffBar = kOffRedL + 2 * 2 * 128 * 4;
@@ -61,8 +61,8 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64, false, true);
 
 // mbarriers (index = bit in the phase and pending masks)
-constexpr int kBarK = 0;      // K tile landed (TMA)
-constexpr int kBarV = 1;      // 1, 2: V buffer landed (TMA)
+constexpr int kBarK = 0;      // 0, 1: K buffer landed (TMA)
+constexpr int kBarV = 2;      // V tile landed (TMA)
 constexpr int kBarS = 3;      // 3, 4: S in TMEM buffer ready (MMA commit)
 constexpr int kBarO = 5;      // 5, 6: O in TMEM buffer ready (MMA commit)
 constexpr int kBarFree = 7;   // 7, 8: O in TMEM buffer read by all eight softmax warps
@@ -115,12 +115,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == 8) {
         // ================= control warp: TMA loads and MMA issue =================
-        // Key tile t uses TMEM buffer and V buffer (t - t_lo) & 1. Order of work for tile t:
-        //   S_t done      -> fetch K_{t+1} (one K buffer)
-        //   PV_{t-1} done -> fetch V_{t+1} into the buffer V_{t-1} used
+        // Key tile t uses TMEM buffer and K buffer (t - t_lo) & 1; V has one buffer. For tile t:
+        //   S_t done -> fetch K_{t+2} into the buffer K_t used
         //   K_{t+1} landed, O_{t-1} read by every softmax warp -> S_{t+1} = Q' K_{t+1}^T
         //   V_t landed, P_t keys [0, 64) written -> first four K steps of O_t = P_t V_t, into the
         //   first 64 columns of S_t's buffer; P_t keys [64, 128) written -> the last four
+        //   O_t done -> fetch V_{t+1}
         // The whole warp runs this code; the elected lane alone issues copies and MMAs.
         const uint32_t e = elect_one_sync();
         uint32_t ph = 0, pend = 0;  // pend: copies and MMAs started and not yet seen complete
@@ -134,33 +134,34 @@ __global__ void __launch_bounds__(kThreads, 2)
             return ok;
         };
         auto issue_k = [&](long long t) {
+            const int kb = (int)((t - t_lo) & 1);
             if (e) {
-                mbar_arrive_expect_tx(bar(kBarK), kTileBytes);
-                tma_load_3d(smem_u32(smem + kOffK), job.tmap_k, bar(kBarK), 0, (int)(t * 128 - job.abs_base), h);
-            }
-            pend |= 1u << kBarK;
-        };
-        auto issue_v = [&](long long t) {
-            const int vb = (int)((t - t_lo) & 1);
-            if (e) {
-                mbar_arrive_expect_tx(bar(kBarV + vb), kTileBytes);
-                tma_load_3d(smem_u32(smem + kOffV) + vb * kTileBytes, job.tmap_v, bar(kBarV + vb), 0,
+                mbar_arrive_expect_tx(bar(kBarK + kb), kTileBytes);
+                tma_load_3d(smem_u32(smem + kOffK) + kb * kTileBytes, job.tmap_k, bar(kBarK + kb), 0,
                             (int)(t * 128 - job.abs_base), h);
             }
-            pend |= 1u << (kBarV + vb);
+            pend |= 1u << (kBarK + kb);
+        };
+        auto issue_v = [&](long long t) {
+            if (e) {
+                mbar_arrive_expect_tx(bar(kBarV), kTileBytes);
+                tma_load_3d(smem_u32(smem + kOffV), job.tmap_v, bar(kBarV), 0, (int)(t * 128 - job.abs_base), h);
+            }
+            pend |= 1u << kBarV;
         };
         auto issue_s = [&](long long t) {
             const int b = (int)((t - t_lo) & 1);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16_ss_if(tmem + 128u * b, smem_desc_sw128(smem_u32(sQ) + 32 * kk, 16, 1024),
-                               smem_desc_sw128(smem_u32(smem + kOffK) + 32 * kk, 16, 1024), kIdescS, kk > 0 ? 1u : 0u, e);
+                               smem_desc_sw128(smem_u32(smem + kOffK) + b * kTileBytes + 32 * kk, 16, 1024), kIdescS,
+                               kk > 0 ? 1u : 0u, e);
             mma_commit_if(bar(kBarS + b), e);
             pend |= 1u << (kBarS + b);
         };
         auto issue_pv = [&](long long t, int kh) {  // K steps [4 kh, 4 kh + 4): keys [64 kh, 64 kh + 64)
             const int b = (int)((t - t_lo) & 1);
-            const uint32_t v = smem_u32(smem + kOffV) + b * kTileBytes;
+            const uint32_t v = smem_u32(smem + kOffV);
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
                 const int kk = 4 * kh + k4;
@@ -174,9 +175,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         };
         auto issue_first = [&]() {
             issue_k(t_lo);
-            issue_v(t_lo);
             if (t_lo < t_hi)
-                issue_v(t_lo + 1);
+                issue_k(t_lo + 1);
+            issue_v(t_lo);
         };
 
         // The first ring tiles may be requested before the previous kernel in the stream has
@@ -197,29 +198,22 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         for (long long t = t_lo; !fail && t <= t_hi; ++t) {
             const int b = (int)((t - t_lo) & 1), nb = b ^ 1;
-            if (t < t_hi) {
+            if (t + 2 <= t_hi) {
                 if (!wait(kBarS + b)) {
                     fail = 1;
                     break;
                 }
-                issue_k(t + 1);
-            }
-            if (t > t_lo && t < t_hi) {
-                if (!wait(kBarO + nb)) {
-                    fail = 1;
-                    break;
-                }
-                issue_v(t + 1);
+                issue_k(t + 2);
             }
             if (t < t_hi) {
-                if (!wait(kBarK) || (t > t_lo && !wait(kBarFree + nb))) {
+                if (!wait(kBarK + nb) || (t > t_lo && !wait(kBarFree + nb))) {
                     fail = 1;
                     break;
                 }
                 tc_fence_after();
                 issue_s(t + 1);
             }
-            if (!wait(kBarV + b) || !wait(kBarP)) {
+            if (!wait(kBarV) || !wait(kBarP)) {
                 fail = 1;
                 break;
             }
@@ -231,6 +225,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             tc_fence_after();
             issue_pv(t, 1);
+            if (t < t_hi) {
+                if (!wait(kBarO + b)) {
+                    fail = 1;
+                    break;
+                }
+                issue_v(t + 1);
+            }
         }
         if (fail) {
             // A bounded wait gave up: record it and let copies and MMAs in flight land.
@@ -312,15 +313,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                 lo = (int)max(-1LL, min(128LL, pq - c.W + 1 - t * 128));
                 hi = (int)max(-1LL, min(128LL, pq - t * 128));
             }
+            const uint32_t mask0 = enc::visible_mask(64 * half, lo, hi), mask1 = enc::visible_mask(64 * half + 32, lo, hi);
             float mh;
             {
                 uint32_t sv[32];
                 tmem_ld_32x32b_x32(tm_b, sv);
                 tmem_ld_wait();
-                mh = enc::quarter_max(sv, 64 * half, lo, hi);
+                mh = enc::quarter_max(sv, mask0);
                 tmem_ld_32x32b_x32(tm_b + 32, sv);
                 tmem_ld_wait();
-                mh = fmaxf(mh, enc::quarter_max(sv, 64 * half + 32, lo, hi));
+                mh = fmaxf(mh, enc::quarter_max(sv, mask1));
             }
             red_m[(b * 2 + half) * 128 + r] = mh;
             if (bar_sync_or(pair_bar, 64, fail)) {
@@ -344,10 +346,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint32_t sv[32];
                 tmem_ld_32x32b_x32(tm_b, sv);
                 tmem_ld_wait();
-                lh = enc::quarter_exp(sv, 64 * half, lo, hi, c.scale_log2, -mt, sP, r);
+                lh = enc::quarter_exp(sv, mask0, 2 * half, c.scale_log2, -mt, sP, r);
                 tmem_ld_32x32b_x32(tm_b + 32, sv);
                 tmem_ld_wait();
-                lh = __fadd_rn(lh, enc::quarter_exp(sv, 64 * half + 32, lo, hi, c.scale_log2, -mt, sP, r));
+                lh = __fadd_rn(lh, enc::quarter_exp(sv, mask1, 2 * half + 1, c.scale_log2, -mt, sP, r));
             }
             red_l[(b * 2 + half) * 128 + r] = lh;
             fence_proxy_async_smem();  // P (generic stores) before the MMA reads it
