@@ -436,8 +436,9 @@ TIMING_NOTE = ("avg_launch_us: timed region / launches, split between kernels by
                "shares; isolated_launch_us: events around each launch (no overlap with neighbours)")
 
 # sources of each profiled kernel id (the encoder attention id covers all its launch shapes)
-KERNEL_SOURCES = {"enc_attn_kernel": ("enc_attn.cu", "enc_attn_split.cu", "enc_common.cuh"),
-                  "dec_step_kernel": ("dec_step.cu",), "compact_kernel": ("compact.cu",)}
+_COMMON_SOURCES = ("ptx.cuh", "common.cuh", "vst_internal.h")
+KERNEL_SOURCES = {"enc_attn_kernel": ("enc_attn.cu", "enc_attn_split.cu", "enc_common.cuh") + _COMMON_SOURCES,
+                  "dec_step_kernel": ("dec_step.cu",) + _COMMON_SOURCES, "compact_kernel": ("compact.cu",) + _COMMON_SOURCES}
 
 
 def kernel_source_sha(kernel: str) -> str:
