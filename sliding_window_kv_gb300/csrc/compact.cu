@@ -5,10 +5,18 @@
 // length; slot 0 then holds absolute frame abs_base + (n_kv - 750).
 //
 // The move ring[s] <- ring[src + s], s in [0, keep), overlaps itself whenever src < keep.
-// One CTA owns one (context, K|V plane, KV head) plane: every thread first loads its
-// share of the source rows into registers, the CTA synchronises, and only then does any
-// thread store. Planes are disjoint, so no two CTAs touch the same bytes.
+// When some job's move does, one CTA owns each (context, K|V plane, KV head) plane: every
+// thread first loads its share of the source rows into registers, the CTA synchronises, and
+// only then does any thread store. When no job's move overlaps (src >= keep, the usual
+// case), each plane is split by rows over `split` CTAs: source and destination rows are then
+// disjoint, so no CTA can overwrite rows that another still reads. Planes are disjoint, so
+// no two planes share bytes either.
+//
+// Launched with programmatic dependent launch: the copy waits for the previous kernel in the
+// stream (which may still read this ring) and lets the next one start its prologue at once;
+// every kernel of the library waits for its predecessor before touching a ring.
 #include "common.cuh"
+#include "ptx.cuh"
 #include "vst_internal.h"
 
 namespace vst {
@@ -21,13 +29,20 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
 {
     const CompactCommon& c = p.c;
     const CompactJob& job = p.jobs[blockIdx.y];
-    const int plane = blockIdx.x;  // 0 .. 2*Hk-1: K heads then V heads
+    griddep_wait();
+    griddep_launch_dependents();
+    const int plane = blockIdx.x / c.split;  // 0 .. 2*Hk-1: K heads then V heads
+    const int part = blockIdx.x % c.split;
     const int head = plane % c.Hk;
+    const int rows_per = (c.keep + c.split - 1) / c.split;
+    const int row_lo = part * rows_per, row_hi = min(c.keep, row_lo + rows_per);
+    if (row_lo >= row_hi)
+        return;
     __nv_bfloat16* ring = plane < c.Hk ? job.k_ring : job.v_ring;
     const long long row_elems = c.D;
-    uint4* dst = reinterpret_cast<uint4*>(ring + (long long)head * c.R * row_elems);
-    const uint4* src = reinterpret_cast<const uint4*>(ring + ((long long)head * c.R + job.src_row) * row_elems);
-    const int n_vec = (int)(c.keep * row_elems * 2 / 16);
+    uint4* dst = reinterpret_cast<uint4*>(ring + ((long long)head * c.R + row_lo) * row_elems);
+    const uint4* src = reinterpret_cast<const uint4*>(ring + ((long long)head * c.R + job.src_row + row_lo) * row_elems);
+    const int n_vec = (int)((row_hi - row_lo) * row_elems * 2 / 16);
 
     uint4 r[kCompactVecPerThread];
 #pragma unroll
@@ -45,16 +60,20 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
     }
 }
 
-cudaError_t launch_compact(const CompactCommon& c, const CompactJob* jobs, int n_jobs, cudaStream_t s)
+cudaError_t launch_compact(const CompactCommon& c0, const CompactJob* jobs, int n_jobs, cudaStream_t s)
 {
     if (n_jobs == 0)
         return cudaSuccess;
-    if ((long long)c.keep * c.D * 2 > 16LL * kCompactThreads * kCompactVecPerThread)
+    if ((long long)c0.keep * c0.D * 2 > 16LL * kCompactThreads * kCompactVecPerThread)
         return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)(2 * c.Hk), (unsigned)n_jobs);
+    CompactCommon c = c0;
+    c.split = kCompactSplit;
+    for (int i = 0; i < n_jobs; ++i)
+        if (jobs[i].src_row < c.keep)
+            c.split = 1;  // the move overlaps itself: one CTA reads a whole plane before writing
+    const dim3 grid((unsigned)(2 * c.Hk * c.split), (unsigned)n_jobs);
     return with_params(c, jobs, n_jobs, [&](const auto& p) {
-        compact_kernel<sizeof(p.jobs) / sizeof(p.jobs[0])><<<grid, kCompactThreads, 0, s>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(compact_kernel<sizeof(p.jobs) / sizeof(p.jobs[0])>, grid, dim3(kCompactThreads), 0, s, p);
     });
 }
 

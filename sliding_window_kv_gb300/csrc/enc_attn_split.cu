@@ -306,11 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sv[32];
         tmem_ld_32x32b_x32(s.tmem + s.lane_base + kTmS + c0, sv);
         tmem_ld_wait();
-        s.red_m[s.q * 128 + r] = quarter_max(sv, c0, lo, hi);
+        const uint32_t vmask = enc::visible_mask(c0, lo, hi);
+        s.red_m[s.q * 128 + r] = quarter_max(sv, vmask);
         __syncthreads();
         const float mraw = fmaxf(fmaxf(s.red_m[r], s.red_m[128 + r]), fmaxf(s.red_m[256 + r], s.red_m[384 + r]));
         const float mt = __fmul_rn(mraw, c.scale_log2);  // -inf when the row sees nothing here
-        s.red_l[s.q * 128 + r] = quarter_exp(sv, c0, lo, hi, c.scale_log2, -mt, s.sP, r);
+        s.red_l[s.q * 128 + r] = quarter_exp(sv, vmask, s.q, c.scale_log2, -mt, s.sP, r);
 
         // ---- V of tile t in smem (new rows patched in), then O_t = P V
         if (!mbar_wait(s.bar_v, ph_v))

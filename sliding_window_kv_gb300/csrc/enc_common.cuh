@@ -52,14 +52,15 @@ __device__ __forceinline__ float max32(const float (&x)[32])
     return fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
 }
 
-// Max over the visible columns of the quarter [c0, c0 + 32) held in sv.
-__device__ __forceinline__ float quarter_max(const uint32_t (&sv)[32], int c0, int lo, int hi)
+// Max over the visible columns (bit j of `mask` for column j) of a quarter held in sv.
+// Called by whole warps: the branch between the all-visible path and the per-column selects
+// is taken for the whole warp at once (the selects give the same value when every bit is set).
+__device__ __forceinline__ float quarter_max(const uint32_t (&sv)[32], uint32_t mask)
 {
-    const uint32_t mask = visible_mask(c0, lo, hi);
-    if (mask == 0u)
+    if (__all_sync(0xffffffffu, mask == 0u))
         return -INFINITY;
     float x[32];
-    if (mask == 0xffffffffu) {  // every column visible: the same maximum without the selects
+    if (__all_sync(0xffffffffu, mask == 0xffffffffu)) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             x[j] = __uint_as_float(sv[j]);
@@ -71,15 +72,14 @@ __device__ __forceinline__ float quarter_max(const uint32_t (&sv)[32], int c0, i
     return max32(x);
 }
 
-// Probabilities of the quarter [c0, c0 + 32) of row `row` (neg = -m_t): written as bf16
-// into the K-major P operand (two 64-key blocks, 128-B swizzle); returns the quarter sum.
-// Columns are taken in ascending order, eight at a time; a hidden column is 0.
-__device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], int c0, int lo, int hi, float scale_log2,
+// Probabilities of quarter q (columns [32 q, 32 q + 32)) of row `row` (neg = -m_t), visible
+// columns in `mask`: written as bf16 into the K-major P operand (two 64-key blocks, 128-B
+// swizzle); returns the quarter sum. Columns are taken in ascending order, eight at a time;
+// a hidden column is 0. Called by whole warps (the branches are taken warp by warp).
+__device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], uint32_t mask, int q, float scale_log2,
                                              float neg, uint8_t* sP, int row)
 {
-    const uint32_t mask = visible_mask(c0, lo, hi);
-    const int q = c0 >> 5;
-    if (mask == 0u) {  // nothing visible: P = 0 and the sum is 0, as below, without the exps
+    if (__all_sync(0xffffffffu, mask == 0u)) {  // nothing visible: P = 0 and the sum is 0, as below
 #pragma unroll
         for (int qd = 0; qd < 4; ++qd)
             *reinterpret_cast<uint4*>(sP + (q >> 1) * kTileBytes + sw128_offset(row, (q & 1) * 4 + qd)) =
@@ -89,7 +89,7 @@ __device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], int c0, i
     // Paired fp32 operations (__ffma2_rn, __fadd2_rn) round each lane exactly as the scalar
     // operation does; l01 and l23 hold the partial sums (l0, l1) and (l2, l3).
     float2 l01 = make_float2(0.f, 0.f), l23 = make_float2(0.f, 0.f);
-    const bool full = mask == 0xffffffffu;  // every column visible: no selects needed
+    const bool full = __all_sync(0xffffffffu, mask == 0xffffffffu);  // no selects needed (whole warp)
     const float2 sc2 = make_float2(scale_log2, scale_log2), ng2 = make_float2(neg, neg);
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {

@@ -10,6 +10,7 @@
 namespace vst {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kSuspendHintNs = 1000000u;     // 1 ms: longest hardware suspension per attempt
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
@@ -42,15 +43,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// One bounded attempt: the thread may be suspended in hardware until the phase completes or
+// kSuspendHintNs passes, so a waiting warp takes no issue slots from the warps that work.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }

@@ -61,7 +61,9 @@ struct CompactJob {
 
 struct CompactCommon {
     int Hk, R, D, keep;
+    int split;  // CTAs per (K|V, head) plane; set by the launcher
 };
+constexpr int kCompactSplit = 2;  // CTAs per plane when no job's move overlaps itself
 
 struct EncAttnJob {
     const __nv_bfloat16* q;  // [n_rows][H][D] input rows of this batch
