@@ -182,6 +182,24 @@ VST_API vst_status vst_dec_step(vst_ctx* const* ctxs, int32_t n_streams, const v
  * Arguments, layouts, ownership and errors are those of vst_dec_step. */
 VST_API vst_status vst_dec_step_noalloc(vst_ctx* const* ctxs, int32_t n_streams, const void* q,
                                         const void* k, const void* v, void* out, void* stream);
+/* Decoder prefill: n tokens of one decoder ctx at positions pos .. pos + n - 1, pos being
+ * its abs_next. This is the prompt the stream driver prefills once before stepping
+ * ("Voxtral Realtime -- incremental streaming implementation plan", SHIPPED / Mechanism and
+ * the stream_feed hook; 39 tokens there, any n here). Output row i is, bit for bit, what
+ * the i-th of n successive vst_dec_step calls (one token each) returns: token i's K
+ * (rotated) and V go to ring slot p_i % R and its query attends keys
+ * [max(0, p_i - W + 1), p_i].
+ * q [n][H][D], k/v [n][Hk][D], out [n][H][D]: bf16 device pointers, 16-byte aligned.
+ * Tokens go in chunks of up to 64 per attention launch, each chunk's rows appended to the
+ * ring first. So a chunk stays below position R (nothing evicted yet) or spans at most
+ * R - W + 1 tokens: one token per launch once a ring with R = W is full; a ring a little
+ * larger than the window keeps chunks of 64 everywhere.
+ * The first call allocates the ctx's prefill scratch: split partials for 64 tokens, about
+ * 18 MB for the pages' decoder (cudaMalloc, blocking). vst_ctx_destroy frees it.
+ * Errors: VST_E_INVAL for bad arguments or positions past max_position (nothing
+ * enqueued); VST_E_NOMEM if the scratch cannot be allocated; otherwise as vst_dec_step. */
+VST_API vst_status vst_dec_prefill(vst_ctx* c, const void* q, const void* k, const void* v, int32_t n,
+                                   void* out, void* stream);
 /* Append n tokens of K/V (no attention) at positions abs_next .. abs_next + n - 1 of one
  * decoder ctx: k/v [n][Hk][D]. Used to fill a cache. */
 VST_API vst_status vst_dec_append(vst_ctx* c, const void* k, const void* v, int32_t n, void* stream);

@@ -24,7 +24,8 @@
 // V as soon as O^T is done; S^T alternates between two TMEM buffers.
 // The query heads are rotated in the prologue; if the split holds pos, the new key is
 // rotated too, patched into its tile row in shared memory, and stored (K', V) to ring slot
-// pos % R by this CTA. Each CTA writes its split's (m, l, o) per head; the last CTA of
+// pos % R by this CTA. A prefill chunk (several tokens of one stream, one job each) has its
+// rows appended to the ring before the launch, so there every key comes from the ring. Each CTA writes its split's (m, l, o) per head; the last CTA of
 // (stream, g) folds the splits in ascending order and writes the output. Tiles and splits
 // are fixed by absolute position, so a stream's output is the same bits alone or in a
 // batch, with either pipeline, and whatever the ring size.
@@ -141,7 +142,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const long long tau_hi = min(sig * kTilesPerSplit + kTilesPerSplit - 1, pos / kTile);
     const int n_tiles = (int)(tau_hi - tau_lo + 1);
     const long long tau_new = pos / kTile;  // tile holding this step's key
-    const bool has_new = tau_new >= tau_lo && tau_new <= tau_hi;
+    // This CTA rotates, patches in and stores the step's key unless the row is already in
+    // the ring (a prefill chunk, appended before the launch).
+    const bool has_new = !c.appended && tau_new >= tau_lo && tau_new <= tau_hi;
 
     uint8_t* const sK = smem;             // K tile: two 64-dim boxes
     uint8_t* const sV = smem + 2 * kBox;  // V tile

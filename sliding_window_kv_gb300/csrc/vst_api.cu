@@ -7,6 +7,7 @@
 // [0, n_kv) = absolute frames [abs_base, abs_base + n_kv); a feed is pushed in batches of
 // at most max_batch frames; a batch that would not fit first triggers a compaction that
 // keeps the last W rows. All of it is known on the host, so no call ever waits for the GPU.
+#include <algorithm>
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -46,6 +47,8 @@ struct vst_ctx {
     int64_t n_kv, abs_base, abs_next, n_compactions;
     int failed;
     CUtensorMap host_maps[2];
+    uint8_t* pf_mem;  // decoder prefill scratch (library-owned, allocated on first use)
+    size_t pf_bytes;
 };
 
 namespace {
@@ -500,7 +503,8 @@ vst_status vst_ctx_reset(vst_ctx* c, void* stream)
     DeviceGuard g(c->m->device);
     c->n_kv = c->abs_base = c->abs_next = c->n_compactions = 0;
     c->failed = 0;
-    if (clear_ctx(c, as_stream(stream)) != cudaSuccess) {
+    if (clear_ctx(c, as_stream(stream)) != cudaSuccess ||
+        (c->pf_mem && cudaMemsetAsync(c->pf_mem, 0, c->pf_bytes, as_stream(stream)) != cudaSuccess)) {
         c->failed = 1;
         return VST_E_CUDA;
     }
@@ -511,9 +515,12 @@ vst_status vst_ctx_destroy(vst_ctx* c)
 {
     if (!c)
         return VST_E_INVAL;
-    if (c->owns) {
+    {
         DeviceGuard g(c->m->device);
-        cudaFree(c->mem);
+        if (c->owns)
+            cudaFree(c->mem);
+        if (c->pf_mem)
+            cudaFree(c->pf_mem);
     }
     delete c;
     return VST_OK;
@@ -778,6 +785,92 @@ vst_status vst_dec_step(vst_ctx* const* ctxs, int32_t n_streams, const void* q, 
             return fail_all(ctxs, n_streams);
         for (int i = 0; i < nj; ++i)
             ctxs[c0 + i]->abs_next += 1;
+    }
+    return VST_OK;
+}
+
+vst_status vst_dec_prefill(vst_ctx* c, const void* q, const void* k, const void* v, int32_t n, void* out,
+                           void* stream)
+{
+    vst_ctx* cs[1] = {c};
+    vst_status st = check_ctxs(cs, 1, VST_DEC);
+    if (st != VST_OK)
+        return st;
+    if (n < 0)
+        return VST_E_INVAL;
+    if (n == 0)
+        return VST_OK;
+    if (!q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return VST_E_INVAL;
+    const vst_module* m = c->m;
+    const vst_config& cfg = m->cfg;
+    if (c->abs_next + n > cfg.max_position)
+        return VST_E_INVAL;
+    DeviceGuard g(m->device);
+    if (!g.ok)
+        return fail_all(cs, 1);
+    const int H = cfg.n_heads, Hk = cfg.n_kv_heads, D = cfg.head_dim;
+    const long long R = cfg.ring_slots, W = cfg.window;
+    // per token of a chunk: m, l [H][S][2] and o [H][S][D] floats, then Hk merge counters
+    const size_t ml_bytes = align256((size_t)H * m->splits * 2 * sizeof(float));
+    const size_t o_bytes = align256((size_t)H * m->splits * D * sizeof(float));
+    const size_t cnt_bytes = align256((size_t)Hk * sizeof(unsigned));
+    const size_t per_token = ml_bytes + o_bytes + cnt_bytes;
+    if (!c->pf_mem) {
+        const size_t bytes = (size_t)kPrefillChunk * per_token;
+        void* mem = nullptr;
+        if (cudaMalloc(&mem, bytes) != cudaSuccess)
+            return VST_E_NOMEM;
+        if (cudaMemset(mem, 0, bytes) != cudaSuccess) {  // the merge counters start at zero
+            cudaFree(mem);
+            return VST_E_CUDA;
+        }
+        c->pf_mem = static_cast<uint8_t*>(mem);
+        c->pf_bytes = bytes;
+    }
+    cudaStream_t s = as_stream(stream);
+    const auto* qb = static_cast<const __nv_bfloat16*>(q);
+    const auto* kb = static_cast<const __nv_bfloat16*>(k);
+    const auto* vb = static_cast<const __nv_bfloat16*>(v);
+    auto* ob = static_cast<__nv_bfloat16*>(out);
+    const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    DecJob jobs[kPrefillChunk];
+    for (int32_t off = 0; off < n;) {
+        const long long pos0 = c->abs_next;
+        // Chunk length. The chunk's rows are appended first, then each token attends from the
+        // ring. Token j's row evicts key p_j - R, which an earlier token i of the chunk still
+        // sees when p_j - R >= p_i - W + 1. So a chunk either stays below position R (nothing
+        // is evicted) or spans at most R - W + 1 tokens; with R = W that is one token.
+        long long len = n - off < kPrefillChunk ? n - off : kPrefillChunk;
+        if (pos0 + len > R) {
+            const long long lim = std::max(R - W + 1, R - pos0);
+            len = std::max(1LL, std::min(len, lim));
+        }
+        const AppendCommon ac{m->rope, (int)len, Hk, D, (int)R, 1};
+        const AppendJob aj{kb + (long long)off * Hk * D, vb + (long long)off * Hk * D, c->k_ring, c->v_ring, pos0, 0};
+        record_touch(s, cs, 1);
+        if (tracked(VST_K_ROPE_APPEND, s, [&] { return launch_rope_append(ac, &aj, 1, s); }) != cudaSuccess)
+            return fail_all(cs, 1);
+        int work = 0;
+        for (int i = 0; i < (int)len; ++i) {
+            const long long pos = pos0 + i;
+            const long long lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
+            const int sig0 = (int)(lo / kDecSplit);
+            const int nsp = (int)(pos / kDecSplit) - sig0 + 1;
+            uint8_t* base = c->pf_mem + (size_t)i * per_token;
+            const long long t = off + i;
+            jobs[i] = DecJob{qb + t * H * D, kb + t * Hk * D, vb + t * Hk * D, ob + t * H * D, c->k_ring, c->v_ring,
+                             c->tmap_k, c->tmap_v, reinterpret_cast<float*>(base),
+                             reinterpret_cast<float*>(base + ml_bytes), reinterpret_cast<unsigned*>(base + ml_bytes + o_bytes),
+                             c->err, pos, sig0, nsp, work, 0};
+            work += nsp;
+        }
+        DecCommon dc{m->rope, (int)len, Hk, (int)R, (int)W, m->splits, 0, scale_log2, 1};
+        dc.early = record_touch(s, cs, 1);  // 0: the append just wrote this ring
+        if (tracked(VST_K_DEC_STEP, s, [&] { return launch_dec_step(dc, jobs, (int)len, work, s); }) != cudaSuccess)
+            return fail_all(cs, 1);
+        c->abs_next += len;
+        off += (int32_t)len;
     }
     return VST_OK;
 }

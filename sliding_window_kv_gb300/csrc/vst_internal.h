@@ -34,6 +34,7 @@ constexpr int kEncTileM = 128;
 constexpr int kEncTileN = 128;
 
 constexpr int kMaxJobs = 64;  // contexts per launch
+constexpr int kPrefillChunk = kMaxJobs;  // decoder prefill: tokens per attention launch (one job each)
 
 // Error codes written into the ctx error word by kernels.
 constexpr int kErrTimeout = 1;
@@ -118,6 +119,7 @@ struct DecCommon {
     int n_jobs, Hk, R, W, S;
     int early;               // 1: ring loads may start before the previous kernel completes
     float scale_log2;
+    int appended;            // 1: every job's K'/V row is already in the ring (prefill chunks)
 };
 
 // Kernel parameters: the common block plus up to J jobs, passed by value. Launchers pick

@@ -46,7 +46,7 @@ K_ROPE_APPEND, K_COMPACT, K_ENC_ATTN, K_DEC_STEP, K_COUNT = 0, 1, 2, 3, 4
 EXPORTS = ["vst_config_default", "vst_module_create", "vst_module_destroy", "vst_module_config",
            "vst_ctx_bytes", "vst_ctx_create", "vst_ctx_reset", "vst_ctx_destroy", "vst_ctx_info_get",
            "vst_ctx_check", "vst_enc_feed", "vst_enc_feed_batch", "vst_ctx_compact", "vst_enc_plan",
-           "vst_dec_step", "vst_dec_step_noalloc", "vst_dec_append", "vst_prof_enable", "vst_prof_read", "vst_launch_count",
+           "vst_dec_step", "vst_dec_step_noalloc", "vst_dec_prefill", "vst_dec_append", "vst_prof_enable", "vst_prof_read", "vst_launch_count",
            "vst_kernel_name", "vst_status_str", "vst_version"]
 
 _lib = None
@@ -79,6 +79,7 @@ def lib():
                               ctypes.POINTER(I32), ctypes.POINTER(I64), ctypes.POINTER(I64)], I32),
             "vst_dec_step": ([PP, I32, P, P, P, P, P], I32),
             "vst_dec_step_noalloc": ([PP, I32, P, P, P, P, P], I32),
+            "vst_dec_prefill": ([P, P, P, P, I32, P, P], I32),
             "vst_dec_append": ([P, P, P, I32, P], I32),
             "vst_prof_enable": ([I32], I32),
             "vst_prof_read": ([ctypes.POINTER(ProfStat), I32], I32),
@@ -222,6 +223,12 @@ def dec_step_noalloc(ctxs, q, k, v, out, stream=None):
     h, keep = _handles(ctxs)
     _check(lib().vst_dec_step_noalloc(h, len(ctxs), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream)),
            "vst_dec_step_noalloc")
+
+
+def dec_prefill(c: int, q, k, v, out, n: int | None = None, stream=None):
+    """vst_dec_prefill: n tokens of one decoder ctx, q/out [n][H][D], k/v [n][Hk][D]."""
+    n = q.shape[0] if n is None else n
+    _check(lib().vst_dec_prefill(c, _ptr(q), _ptr(k), _ptr(v), n, _ptr(out), _stream(stream)), "vst_dec_prefill")
 
 
 def dec_append(c: int, k, v, n: int | None = None, stream=None):
