@@ -47,6 +47,10 @@ WORKLOADS = {
     "dec_b1": dict(kind="dec", layers=26, streams=1, fill="full", steps=256, seed=3),
     # decoder, 26 layers, 64 streams with fills uniform in [1, 8192]
     "dec_b64": dict(kind="dec", layers=26, streams=64, fill="uniform", steps=256, seed=4),
+    # decoder prefill, 26 layers, one stream: the 39-token prompt on an empty cache
+    "dec_prefill39": dict(kind="prefill", layers=26, tokens=39, seed=6),
+    # decoder prefill, 26 layers, one stream: a 512-token prompt on an empty cache
+    "dec_prefill512": dict(kind="prefill", layers=26, tokens=512, seed=7),
 }
 
 
@@ -368,6 +372,46 @@ class DecWorkload:
         self.module.close()
 
 
+class PrefillWorkload:
+    """26 decoder layers of one stream, each prefilling `tokens` prompt tokens on an empty
+    cache (vst_dec_prefill per layer). The ring is cleared once before the captured run, and
+    a replay redoes the same positions."""
+
+    def __init__(self, spec, dev, rank=0):
+        import torch
+        from sliding_window_kv_gb300 import synth, vst
+        self.vst = vst
+        self.L, self.n = spec["layers"], spec["tokens"]
+        seed = spec["seed"] + 1000 * rank
+        self.module = vst.Module(vst.DEC)
+        self.ctxs = [vst.Ctx(self.module) for _ in range(self.L)]
+        self.Q = [synth.frames(synth.tensor_key(seed, 0, l, 0), 0, self.n, DEC_H, DEC_D, dev) for l in range(self.L)]
+        self.K = [synth.frames(synth.tensor_key(seed, 0, l, 1), 0, self.n, DEC_HK, DEC_D, dev) for l in range(self.L)]
+        self.V = [synth.frames(synth.tensor_key(seed, 0, l, 2), 0, self.n, DEC_HK, DEC_D, dev) for l in range(self.L)]
+        self.O = [torch.empty_like(q) for q in self.Q]
+
+    def reset(self, stream):
+        for c in self.ctxs:
+            self.vst.ctx_reset(c.handle, stream)
+
+    def run(self, stream):
+        for l in range(self.L):
+            self.vst.dec_prefill(self.ctxs[l].handle, self.Q[l], self.K[l], self.V[l], self.O[l], self.n, stream)
+
+    def kv_bytes(self):
+        """Algorithmic bytes of kernel (c) for one run: what n one-token steps read (K and V
+        of every visible key, min(p+1, W) keys x Hk x D x 2 B x 2, plus each token's q, k,
+        v and out)."""
+        per_key = DEC_HK * DEC_D * 2 * 2
+        io = (DEC_H * DEC_D * 2) * 2 + DEC_HK * DEC_D * 2 * 2
+        return self.L * sum(min(p + 1, DEC_W) * per_key + io for p in range(self.n))
+
+    def close(self):
+        for c in self.ctxs:
+            c.close()
+        self.module.close()
+
+
 # ---------------------------------------------------------------- timing helpers
 
 def capture(fn, stream):
@@ -602,6 +646,41 @@ def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu):
     return out
 
 
+def bench_prefill(spec, dev, stream, dist, steps, warmup, peaks):
+    import torch
+    from sliding_window_kv_gb300 import vst
+    w = PrefillWorkload(spec, dev, dist.rank)
+    w.run(stream)  # eager: allocates each ctx's prefill scratch, configures the kernels
+    w.reset(stream)
+    torch.cuda.synchronize()
+    n0 = vst.launch_count()
+    g = capture(w.run, stream)
+    launches = vst.launch_count() - n0
+    for _ in range(max(1, warmup)):
+        g.replay()
+    ms = dist.max(time_graph(g, stream, steps, dist)) / steps  # per run of the 26 layers
+    tok_per_s = dist.world * w.n / (ms / 1e3)
+    w.reset(stream)
+    prof = profiled_kernels(w.run, stream)
+    nl, kms = prof["dec_step_kernel"]
+    bytes_per_launch = w.kv_bytes() / max(1, nl)
+    launch_us = region_launch_us(prof, "dec_step_kernel", ms)
+    achieved = bytes_per_launch / (launch_us / 1e6) / 1e9
+    hbm, _, _, src = peaks
+    out = {"value": tok_per_s, "unit": "prompt tokens/s",
+           "config": {"workload": "dec_prefill_%dL_gqa32-8x128_W8192_1stream_%dtok" % (w.L, w.n), "layers": w.L,
+                      "tokens": w.n, "seed": spec["seed"], "l2": "prompt K/V fit in L2 (no flush between replays)"},
+           "ms_per_step": ms, "gpu_launches": launches,
+           "roofline": {"kernel": "dec_step_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm,
+                        "unit": "GB/s", "frac": achieved / hbm,
+                        "traffic": dram_traffic("dec_step_kernel", bytes_per_launch),
+                        "peak_source": src, "launches": nl, "avg_launch_us": launch_us,
+                        "isolated_launch_us": 1e3 * kms / nl, "timing": TIMING_NOTE,
+                        "algorithmic_bytes_per_launch": bytes_per_launch}}
+    w.close()
+    return out
+
+
 def run_vst(args, dist):
     import torch
     from sliding_window_kv_gb300 import vst
@@ -621,6 +700,17 @@ def run_vst(args, dist):
     line = {"metric": METRIC, "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded counter-hash bf16 ~N(0,1))", "impl": "vst"}
+
+    if spec["kind"] == "prefill":
+        with torch.cuda.stream(stream):
+            sampler.start()
+            d = bench_prefill(spec, dev, stream, dist, args.steps, args.warmup, peaks)
+            clocks = sampler.stop()
+        line.update({"value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"], "config": d["config"],
+                     "roofline": d["roofline"], "gpu_launches": d["gpu_launches"], "clocks": clocks})
+        if dist.rank == 0:
+            print(json.dumps(line))
+        return
 
     if spec["kind"] == "dec":
         with torch.cuda.stream(stream):
@@ -712,6 +802,11 @@ def run_vst(args, dist):
                           not args.no_cpu and dist.rank == 0)
             d["clocks"] = sampler2.stop()
             line["dec"] = d
+            sampler3 = ClockSampler(dist.local_rank)
+            sampler3.start()
+            d = bench_prefill(dict(WORKLOADS["dec_prefill39"]), dev, stream, dist, args.steps, args.warmup, peaks)
+            d["clocks"] = sampler3.stop()
+            line["prefill"] = d
 
     if not args.no_cpu and dist.rank == 0:
         v, dt, sample = cpu_baseline_enc(spec, 4 if spec["layers"] >= 4 else spec["layers"], cpu_threads())
