@@ -55,9 +55,10 @@ def _bind(lib):
     lib.vst_oracle_rope.argtypes = [P, I, D, LL, P]
     lib.vst_oracle_rope_rows.argtypes = [P, LL, I, I, D, LL, P]
     lib.vst_oracle_attend.argtypes = [P, P, P, LL, I, I, I, LL, LL, LL, P]
+    lib.vst_oracle_attend_lr.argtypes = [P, P, P, LL, I, I, I, LL, LL, LL, LL, P]
     lib.vst_oracle_ring_feed.argtypes = [ctypes.POINTER(_RingState), LL, LL, LL, LL]
     for f in ("vst_oracle_bf16_to_double_n", "vst_oracle_rope", "vst_oracle_rope_rows",
-              "vst_oracle_attend", "vst_oracle_ring_feed"):
+              "vst_oracle_attend", "vst_oracle_attend_lr", "vst_oracle_ring_feed"):
         getattr(lib, f).restype = None
     return lib
 
@@ -137,6 +138,46 @@ def attend(qr: np.ndarray, kr: np.ndarray, v: np.ndarray, window: int,
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(lambda s: run(*s), spans))
     return out
+
+
+def attend_lr(qr: np.ndarray, kr: np.ndarray, v: np.ndarray, left: int, right: int,
+              rows: tuple[int, int] | None = None, threads: int = 1) -> np.ndarray:
+    """Sliding attention with a left window and a right lookahead: row i sees key j of the
+    clip iff 0 <= i - j < left or 0 < j - i < right. Arguments as `attend`."""
+    qr = np.ascontiguousarray(qr, dtype=np.float64)
+    kr = np.ascontiguousarray(kr, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    T, H, D = qr.shape
+    Hk = kr.shape[1]
+    if kr.shape != (T, Hk, D) or v.shape != (T, Hk, D) or H % Hk or left < 1 or right < 0:
+        raise ValueError("shape or mask mismatch")
+    r0, r1 = rows if rows is not None else (0, T)
+    out = np.empty((r1 - r0, H, D), dtype=np.float64)
+    lib = _load()
+
+    def run(a, b):
+        sub = out[a - r0:b - r0]
+        lib.vst_oracle_attend_lr(_ptr(qr), _ptr(kr), _ptr(v), T, H, Hk, D, int(left), int(right), a, b,
+                                 sub.ctypes.data_as(ctypes.c_void_p))
+
+    if threads <= 1 or r1 - r0 < 2 * threads:
+        run(r0, r1)
+    else:
+        step = -(-(r1 - r0) // (4 * threads))
+        spans = [(a, min(a + step, r1)) for a in range(r0, r1, step)]
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda s: run(*s), spans))
+    return out
+
+
+def attention_lr(q_bits, k_bits, v_bits, left: int, right: int, pos0: int = 0, theta: float = THETA,
+                 rows: tuple[int, int] | None = None, threads: int = 1) -> np.ndarray:
+    """Whole-clip oracle with a (left, right) mask: RoPE at absolute positions pos0 + t,
+    then `attend_lr`. q [T][H][D], k/v [T][Hk][D] as bf16 bit patterns."""
+    qr = rope_rows(q_bits, pos0, theta)
+    kr = rope_rows(k_bits, pos0, theta)
+    vv = bf16_to_double(v_bits)
+    return attend_lr(qr, kr, vv, left, right, rows, threads)
 
 
 def attention(q_bits, k_bits, v_bits, window: int, pos0: int = 0, theta: float = THETA,

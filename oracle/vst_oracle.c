@@ -93,6 +93,49 @@ void vst_oracle_rope_rows(const uint16_t* x, long long n_rows, int n_heads, int 
         }
 }
 
+/* One output row i (all H heads) over the keys j in [j0, j1] of a clip, offline definition:
+ * out[h] = sum_j softmax_j(qr[i][h] . kr[j][g] / sqrt(D)) v[j][g], KV head g = h / (H / Hk),
+ * the maximum score subtracted before exp. Layouts as vst_oracle_attend. */
+static void attend_span(const double* qr, const double* kr, const double* v, int H, int Hk, int D,
+                        long long i, long long j0, long long j1, double* out_row)
+{
+    int group = H / Hk;
+    double scale = 1.0 / sqrt((double)D);
+    for (int h = 0; h < H; ++h) {
+        int g = h / group;
+        const double* qi = qr + (i * H + h) * (long long)D;
+        double* o = out_row + (long long)h * D;
+        /* scores and their maximum */
+        double m = -INFINITY;
+        for (long long j = j0; j <= j1; ++j) {
+            const double* kj = kr + (j * Hk + g) * (long long)D;
+            double s = 0.0;
+            for (int d = 0; d < D; ++d)
+                s += qi[d] * kj[d];
+            s *= scale;
+            if (s > m)
+                m = s;
+        }
+        /* softmax-weighted sum of values */
+        double z = 0.0;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        for (long long j = j0; j <= j1; ++j) {
+            const double* kj = kr + (j * Hk + g) * (long long)D;
+            const double* vj = v + (j * Hk + g) * (long long)D;
+            double s = 0.0;
+            for (int d = 0; d < D; ++d)
+                s += qi[d] * kj[d];
+            double w = exp(s * scale - m);
+            z += w;
+            for (int d = 0; d < D; ++d)
+                o[d] += w * vj[d];
+        }
+        for (int d = 0; d < D; ++d)
+            o[d] /= z;
+    }
+}
+
 /* Windowed-causal attention, offline definition, for rows i in [row_begin, row_end) of a
  * clip of T rows (row t = absolute position base + t; only differences matter here, RoPE
  * is already applied by the caller).
@@ -105,45 +148,31 @@ void vst_oracle_attend(const double* qr, const double* kr, const double* v, long
                        int H, int Hk, int D, long long W, long long row_begin, long long row_end,
                        double* out)
 {
-    int group = H / Hk;
-    double scale = 1.0 / sqrt((double)D);
     for (long long i = row_begin; i < row_end && i < T; ++i) {
         long long j0 = i - W + 1;
         if (j0 < 0)
             j0 = 0;
-        for (int h = 0; h < H; ++h) {
-            int g = h / group;
-            const double* qi = qr + (i * H + h) * (long long)D;
-            double* o = out + ((i - row_begin) * H + h) * (long long)D;
-            /* scores and their maximum */
-            double m = -INFINITY;
-            for (long long j = j0; j <= i; ++j) {
-                const double* kj = kr + (j * Hk + g) * (long long)D;
-                double s = 0.0;
-                for (int d = 0; d < D; ++d)
-                    s += qi[d] * kj[d];
-                s *= scale;
-                if (s > m)
-                    m = s;
-            }
-            /* softmax-weighted sum of values */
-            double z = 0.0;
-            for (int d = 0; d < D; ++d)
-                o[d] = 0.0;
-            for (long long j = j0; j <= i; ++j) {
-                const double* kj = kr + (j * Hk + g) * (long long)D;
-                const double* vj = v + (j * Hk + g) * (long long)D;
-                double s = 0.0;
-                for (int d = 0; d < D; ++d)
-                    s += qi[d] * kj[d];
-                double w = exp(s * scale - m);
-                z += w;
-                for (int d = 0; d < D; ++d)
-                    o[d] += w * vj[d];
-            }
-            for (int d = 0; d < D; ++d)
-                o[d] /= z;
-        }
+        attend_span(qr, kr, v, H, Hk, D, i, j0, i, out + (i - row_begin) * H * (long long)D);
+    }
+}
+
+/* Sliding attention with a left window and a right lookahead, offline definition ("Moonshine
+ * streaming forward map", Encoder table, per-layer sliding-window mask row): query i sees key
+ * j of the same clip iff 0 <= i - j < L or 0 < j - i < R, for j in [0, T). So the visible
+ * keys are [i - L + 1, i + R - 1], clipped to the clip; L = W, R = 0 is the windowed-causal
+ * mask of vst_oracle_attend. Arguments as vst_oracle_attend. */
+void vst_oracle_attend_lr(const double* qr, const double* kr, const double* v, long long T,
+                          int H, int Hk, int D, long long L, long long R, long long row_begin,
+                          long long row_end, double* out)
+{
+    for (long long i = row_begin; i < row_end && i < T; ++i) {
+        long long lo = i - L + 1;
+        long long hi = R > 0 ? i + R - 1 : i;
+        if (lo < 0)
+            lo = 0;
+        if (hi > T - 1)
+            hi = T - 1;
+        attend_span(qr, kr, v, H, Hk, D, i, lo, hi, out + (i - row_begin) * H * (long long)D);
     }
 }
 

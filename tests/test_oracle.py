@@ -298,10 +298,84 @@ def check_chunking_not_observable():
         assert np.array_equal(np.concatenate(out), whole)
 
 
+# ---- (left, right) mask: "Moonshine streaming forward map", Encoder table, per-layer
+# sliding-window mask row: mask[q, k] = 0 iff (q - k in [0, L)) or (k - q in (0, R)).
+
+def _bruteforce_lr(qb, kb, vb, L, R, pos0=0):
+    """Full T x T score matrix with the pages' (L, R) mask written out, softmax by definition."""
+    q = oracle.bf16_to_double(qb)
+    k = oracle.bf16_to_double(kb)
+    v = oracle.bf16_to_double(vb)
+    T, H, D = q.shape
+    Hk = k.shape[1]
+    pos = np.arange(T) + pos0
+    qr = _rope_complex(q, pos[:, None])
+    kr = _rope_complex(k, pos[:, None])
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    allowed = ((i - j >= 0) & (i - j < L)) | ((j - i > 0) & (j - i < R))
+    out = np.zeros((T, H, D))
+    for h in range(H):
+        g = h // (H // Hk)
+        S = qr[:, h] @ kr[:, g].T / math.sqrt(D)
+        S = np.where(allowed, S, -np.inf)
+        P = np.exp(S - S.max(axis=1, keepdims=True))
+        P /= P.sum(axis=1, keepdims=True)
+        out[:, h] = P @ v[:, g]
+    return out
+
+
+def check_lr_bruteforce_tiny():
+    for (T, H, Hk, D, L, R, pos0) in [(9, 2, 2, 8, 3, 2, 0), (12, 4, 2, 8, 16, 4, 5), (11, 2, 1, 16, 1, 3, 0),
+                                      (10, 2, 2, 8, 4, 0, 7), (7, 2, 2, 8, 2, 9, 0)]:
+        qb, kb, vb = (_randn_bits(s, seed) for s, seed in (((T, H, D), 110), ((T, Hk, D), 111), ((T, Hk, D), 112)))
+        got = oracle.attention_lr(qb, kb, vb, L, R, pos0=pos0)
+        want = _bruteforce_lr(qb, kb, vb, L, R, pos0=pos0)
+        assert np.allclose(got, want, atol=1e-12, rtol=0), (T, L, R)
+
+
+def check_lr_bidirectional_is_sdpa():
+    """L and R past the clip: every row sees the whole clip, which is torch's unmasked SDPA."""
+    T, H, D = 30, 2, 16
+    qb, kb, vb = (_randn_bits((T, H, D), s) for s in (120, 121, 122))
+    got = oracle.attention_lr(qb, kb, vb, T + 3, T + 3)
+    pos = np.arange(T)[:, None]
+    qr = torch.from_numpy(_rope_complex(oracle.bf16_to_double(qb), pos)).permute(1, 0, 2)
+    kr = torch.from_numpy(_rope_complex(oracle.bf16_to_double(kb), pos)).permute(1, 0, 2)
+    vv = torch.from_numpy(oracle.bf16_to_double(vb)).permute(1, 0, 2)
+    want = torch.nn.functional.scaled_dot_product_attention(qr, kr, vv)
+    assert np.allclose(got, want.permute(1, 0, 2).numpy(), atol=1e-12, rtol=0)
+
+
+def check_lr_zero_query_span_mean():
+    """q = 0: row i is the plain mean of v over [max(0, i-L+1), min(T-1, i+R-1)], which pins
+    both edges of the span (R = 0 and R = 1 both mean no lookahead)."""
+    T, H, D = 60, 2, 4
+    vb = _randn_bits((T, H, D), 130)
+    kb = _randn_bits((T, H, D), 131)
+    qb = np.zeros((T, H, D), dtype=np.uint16)
+    v = oracle.bf16_to_double(vb)
+    for L, R in ((16, 4), (16, 0), (16, 1), (1, 1), (5, 7)):
+        out = oracle.attention_lr(qb, kb, vb, L, R)
+        for i in (0, 1, 3, 15, 16, 30, 56, 57, 58, 59):
+            j0, j1 = max(0, i - L + 1), min(T - 1, i + max(R - 1, 0))
+            assert np.allclose(out[i], v[j0:j1 + 1].mean(axis=0), atol=1e-13), (L, R, i)
+
+
+def check_lr_causal_case_is_windowed_attention():
+    """R = 0 is the windowed-causal mask with W = L: the same bits as `attention`."""
+    T, H, D = 80, 2, 64
+    qb, kb, vb = (_randn_bits((T, H, D), s) for s in (140, 141, 142))
+    for L in (1, 7, 80, 200):
+        assert np.array_equal(oracle.attention_lr(qb, kb, vb, L, 0), oracle.attention(qb, kb, vb, window=L))
+
+
 ATTENTION_CHECKS = [check_bruteforce_tiny, check_long_window_is_causal_sdpa,
                     check_window_one_returns_v, check_zero_query_gives_window_mean,
                     check_decoder_window_8192, check_gqa_groups, check_position_shift_invariance,
-                    check_window_locality, check_chunking_not_observable]
+                    check_window_locality, check_chunking_not_observable, check_lr_bruteforce_tiny,
+                    check_lr_bidirectional_is_sdpa, check_lr_zero_query_span_mean,
+                    check_lr_causal_case_is_windowed_attention]
 
 
 @pytest.mark.parametrize("check", ATTENTION_CHECKS)
@@ -396,6 +470,9 @@ MUTANTS = {
     "ring_trigger": ("if (st->n_kv + b > ring_slots) {", "if (st->n_kv + b >= ring_slots) {"),
     "ring_keep": ("st->abs_base += st->n_kv - kept;", "st->abs_base += st->n_kv - kept + 1;"),
     "bf16_shift": ("((uint32_t)b) << 16;", "((uint32_t)b) << 15;"),
+    "lr_right_edge": ("long long hi = R > 0 ? i + R - 1 : i;", "long long hi = R > 0 ? i + R : i;"),
+    "lr_left_edge": ("long long lo = i - L + 1;", "long long lo = i - L;"),
+    "lr_clip_end": ("            hi = T - 1;", "            hi = T - 2;"),
 }
 
 
