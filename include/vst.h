@@ -92,6 +92,7 @@ VST_API vst_status vst_config_default(int32_t kind, vst_config* cfg);
 
 typedef struct vst_module vst_module; /* immutable: config + RoPE table on one device */
 typedef struct vst_ctx vst_ctx;       /* one (stream, layer) cache */
+typedef struct vst_offline vst_offline; /* scratch for batched whole-clip encoder attention */
 
 /* Build the module on the current CUDA device: validates cfg, computes the RoPE cos/sin
  * table on the host in double precision (angle p * theta^(-2i/D)), rounds it to fp32 and
@@ -153,6 +154,34 @@ VST_API vst_status vst_ctx_compact(vst_ctx* c, void* stream);
 VST_API vst_status vst_enc_plan(const vst_config* cfg, int64_t n_kv, int64_t abs_base, int32_t n_new,
                         int32_t* batch, int32_t* compact, int32_t max_steps, int32_t* n_steps,
                         int64_t* n_kv_out, int64_t* abs_base_out);
+
+/* ---- batched offline encoder over whole clips ---------------------------------------------
+ * The pages' batch path ("Voxtral Realtime" family doc, Capability Validation, Batch row,
+ * item (1)): clips right-padded to one length T and stacked, one shared position range and
+ * mask, each caller slicing its clip's real rows. Causal masks never let padding reach a
+ * real row. Optionally with a right lookahead: the (left L, right R) sliding mask of
+ * "Moonshine streaming forward map", Encoder table, per-layer sliding-window mask row.
+ * Frame i of a clip sees frame j of the same clip iff 0 <= i - j < L or 0 < j - i < R.
+ * With L = W and R = 0, row i is bit for bit what streaming the clip through
+ * vst_enc_feed gives for frame i (same tiles, same order of folds).
+ *
+ * A plan holds the scratch for B clips of T frames: K' and V of each clip, [H][T][D] bf16,
+ * plus one error word and two tensor maps per clip. vst_offline_bytes gives its size
+ * (0 for a decoder module or B, T < 1). dev_mem: caller-owned device memory of at least
+ * that size, 256-byte aligned, or NULL for library-owned memory. Creation uploads the
+ * tensor maps (blocking). */
+VST_API size_t vst_offline_bytes(const vst_module* m, int32_t B, int32_t T);
+VST_API vst_status vst_offline_create(const vst_module* m, int32_t B, int32_t T, void* dev_mem, size_t bytes,
+                                      vst_offline** out);
+VST_API vst_status vst_offline_destroy(vst_offline* p);
+/* q, k, v, out: [B][T][H][D] bf16 device pointers, 16-byte aligned (Hk = H for the
+ * encoder). left >= 1, right >= 0. Two launches per 64 clips: RoPE of K into the scratch,
+ * then the loop-shape attention over all query tiles. Asynchronous on `stream`; positions
+ * run 0 .. T-1 in every clip. VST_E_INVAL on bad arguments (nothing enqueued). */
+VST_API vst_status vst_enc_offline(vst_offline* p, const void* q, const void* k, const void* v, int32_t left,
+                                   int32_t right, void* out, void* stream);
+/* Synchronise `stream`; VST_E_TIMEOUT (and clear it) if a bounded wait in a kernel gave up. */
+VST_API vst_status vst_offline_check(vst_offline* p, void* stream);
 
 /* ---- decoder step path (family doc, Streaming row, item (5)) ---------------------------
  * One token per stream: for each of n_streams contexts (one module, distinct), token s is

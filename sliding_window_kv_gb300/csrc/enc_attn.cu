@@ -9,6 +9,10 @@
 // multi-query prefill against <= 750 cached keys. Frame i attends to [i-749, i]
 // ("RECOMMENDED implementation").
 //
+// With a right lookahead (offline clips, "Moonshine streaming forward map", Encoder table,
+// per-layer sliding-window mask row), frame i also sees [i+1, i+right] of the batch; right
+// is 0 on the streaming path.
+//
 // Keys are visited in tiles of 128 ABSOLUTE positions [128t, 128t+128), loaded whole by
 // TMA from ring slots 128t - abs_base (rows outside the ring read as zero): the batch's own
 // rows were rotated and appended to the ring by kernel (a) (rope_append.cu) just before
@@ -84,8 +88,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int row0 = (int)blockIdx.x * 128;
     const int nrows = min(128, c.n_rows - row0);
     const long long p_first = job.pos0 + row0;
+    const long long key_last = job.pos0 + c.n_rows - 1;  // last key of the batch
     const long long t_lo = max(0LL, p_first - c.W + 1) / 128;
-    const long long t_hi = (p_first + nrows - 1) / 128;
+    const long long t_hi = min(p_first + nrows - 1 + c.right, key_last) / 128;
 
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             int lo = 1, hi = 0;  // visible columns of row r in this tile; empty unless r is real
             if (row_real) {
                 lo = (int)max(-1LL, min(128LL, pq - c.W + 1 - t * 128));
-                hi = (int)max(-1LL, min(128LL, pq - t * 128));
+                hi = (int)max(-1LL, min(128LL, min(pq + c.right, key_last) - t * 128));
             }
             const uint32_t mask0 = enc::visible_mask(64 * half, lo, hi), mask1 = enc::visible_mask(64 * half + 32, lo, hi);
             float mh;
@@ -403,7 +408,7 @@ cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int 
 {
     if (n_jobs == 0 || c.n_rows == 0)
         return cudaSuccess;
-    if (c.split || !c.appended)
+    if (c.split || !c.appended || c.right < 0)
         return cudaErrorInvalidValue;  // split shape: launch_enc_attn_split; rows appended first
     return with_params(c, jobs, n_jobs, [&](const auto& p) {
         return launch_enc_attn_j<sizeof(p.jobs) / sizeof(p.jobs[0])>(p, n_jobs, grid_x, s);

@@ -472,6 +472,8 @@ cudaError_t launch_enc_attn_split(const EncAttnCommon& c, const EncAttnJob* jobs
 {
     if (n_jobs == 0 || c.n_rows == 0)
         return cudaSuccess;
+    if (c.right != 0)
+        return cudaErrorInvalidValue;  // the split shape serves the streaming (causal) mask only
     return with_params(c, jobs, n_jobs, [&](const auto& p) {
         return launch_enc_attn_split_j<sizeof(p.jobs) / sizeof(p.jobs[0])>(p, n_jobs, grid_x, s);
     });

@@ -51,6 +51,20 @@ struct vst_ctx {
     size_t pf_bytes;
 };
 
+// Offline plan: scratch for B whole clips of T frames ([B][H][T][D] K' and V), the error
+// word and one pair of tensor maps per clip, in caller-provided or library-owned memory.
+struct vst_offline {
+    const vst_module* m;
+    uint8_t* mem;
+    bool owns;
+    size_t bytes;
+    int32_t B, T;
+    CUtensorMap* maps;  // device: [B][2] (K', V)
+    int* err;
+    __nv_bfloat16* k_scr;
+    __nv_bfloat16* v_scr;
+};
+
 namespace {
 
 struct Layout {
@@ -785,6 +799,153 @@ vst_status vst_dec_step(vst_ctx* const* ctxs, int32_t n_streams, const void* q, 
             return fail_all(ctxs, n_streams);
         for (int i = 0; i < nj; ++i)
             ctxs[c0 + i]->abs_next += 1;
+    }
+    return VST_OK;
+}
+
+// ---- batched offline encoder over whole clips ------------------------------------------
+
+size_t vst_offline_bytes(const vst_module* m, int32_t B, int32_t T)
+{
+    if (!m || m->cfg.kind != VST_ENC || B < 1 || T < 1)
+        return 0;
+    const vst_config& c = m->cfg;
+    const size_t scr = align256((size_t)B * c.n_kv_heads * T * c.head_dim * sizeof(__nv_bfloat16));
+    return align256((size_t)B * 2 * sizeof(CUtensorMap)) + 256 + 2 * scr;
+}
+
+vst_status vst_offline_create(const vst_module* m, int32_t B, int32_t T, void* dev_mem, size_t bytes,
+                              vst_offline** out)
+{
+    if (!out)
+        return VST_E_INVAL;
+    *out = nullptr;
+    if (!m || m->cfg.kind != VST_ENC || B < 1 || T < 1 || T > m->cfg.max_position)
+        return VST_E_INVAL;
+    const vst_config& cfg = m->cfg;
+    const size_t need = vst_offline_bytes(m, B, T);
+    if (dev_mem && (bytes < need || ((uintptr_t)dev_mem & 255u)))
+        return VST_E_INVAL;
+    DeviceGuard g(m->device);
+    if (!g.ok)
+        return VST_E_CUDA;
+    vst_offline* p = new (std::nothrow) vst_offline();
+    if (!p)
+        return VST_E_NOMEM;
+    p->m = m;
+    p->B = B;
+    p->T = T;
+    p->bytes = need;
+    if (dev_mem) {
+        p->mem = static_cast<uint8_t*>(dev_mem);
+        p->owns = false;
+    } else {
+        void* mem = nullptr;
+        if (cudaMalloc(&mem, need) != cudaSuccess) {
+            delete p;
+            return VST_E_NOMEM;
+        }
+        p->mem = static_cast<uint8_t*>(mem);
+        p->owns = true;
+    }
+    const size_t maps_bytes = align256((size_t)B * 2 * sizeof(CUtensorMap));
+    const size_t scr = align256((size_t)B * cfg.n_kv_heads * T * cfg.head_dim * sizeof(__nv_bfloat16));
+    p->maps = reinterpret_cast<CUtensorMap*>(p->mem);
+    p->err = reinterpret_cast<int*>(p->mem + maps_bytes);
+    p->k_scr = reinterpret_cast<__nv_bfloat16*>(p->mem + maps_bytes + 256);
+    p->v_scr = reinterpret_cast<__nv_bfloat16*>(p->mem + maps_bytes + 256 + scr);
+    // clip b's K' and V: [H][T][D] each, maps over them as over a ring of T slots
+    vst_config mc = cfg;
+    mc.ring_slots = T;
+    std::vector<CUtensorMap> host(2 * (size_t)B);
+    bool ok = true;
+    const size_t per_clip = (size_t)cfg.n_kv_heads * T * cfg.head_dim;
+    for (int b = 0; b < B && ok; ++b)
+        ok = make_ring_map(&host[2 * b], p->k_scr + b * per_clip, mc) &&
+             make_ring_map(&host[2 * b + 1], p->v_scr + b * per_clip, mc);
+    if (!ok || cudaMemcpy(p->maps, host.data(), host.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(p->err, 0, 256) != cudaSuccess) {
+        if (p->owns)
+            cudaFree(p->mem);
+        delete p;
+        return ok ? VST_E_CUDA : VST_E_UNSUPPORTED;
+    }
+    *out = p;
+    return VST_OK;
+}
+
+vst_status vst_offline_destroy(vst_offline* p)
+{
+    if (!p)
+        return VST_E_INVAL;
+    if (p->owns) {
+        DeviceGuard g(p->m->device);
+        cudaFree(p->mem);
+    }
+    delete p;
+    return VST_OK;
+}
+
+vst_status vst_enc_offline(vst_offline* p, const void* q, const void* k, const void* v, int32_t left, int32_t right,
+                           void* out, void* stream)
+{
+    if (!p || !q || !k || !v || !out || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return VST_E_INVAL;
+    if (left < 1 || right < 0)
+        return VST_E_INVAL;
+    const vst_module* m = p->m;
+    const vst_config& cfg = m->cfg;
+    DeviceGuard g(m->device);
+    if (!g.ok)
+        return VST_E_CUDA;
+    cudaStream_t s = as_stream(stream);
+    const int H = cfg.n_heads, Hk = cfg.n_kv_heads, D = cfg.head_dim;
+    const int32_t T = p->T;
+    const auto* qb = static_cast<const __nv_bfloat16*>(q);
+    const auto* kb = static_cast<const __nv_bfloat16*>(k);
+    const auto* vb = static_cast<const __nv_bfloat16*>(v);
+    auto* ob = static_cast<__nv_bfloat16*>(out);
+    const size_t per_clip = (size_t)Hk * T * D;
+    for (int32_t b0 = 0; b0 < p->B; b0 += kMaxJobs) {
+        const int nj = p->B - b0 < kMaxJobs ? p->B - b0 : kMaxJobs;
+        // K' (rotated at positions 0 .. T-1) and V of each clip into its [H][T][D] scratch
+        const AppendCommon ac{m->rope, T, Hk, D, T, 0};
+        AppendJob aj[kMaxJobs];
+        EncAttnJob ej[kMaxJobs];
+        for (int i = 0; i < nj; ++i) {
+            const long long row = (long long)(b0 + i) * T;
+            __nv_bfloat16* ks = p->k_scr + (b0 + i) * per_clip;
+            __nv_bfloat16* vs = p->v_scr + (b0 + i) * per_clip;
+            aj[i] = AppendJob{kb + row * Hk * D, vb + row * Hk * D, ks, vs, 0, 0};
+            ej[i] = EncAttnJob{qb + row * H * D, kb + row * Hk * D, vb + row * Hk * D, ob + row * H * D, ks, vs,
+                               p->maps + 2 * (b0 + i), p->maps + 2 * (b0 + i) + 1, nullptr, nullptr, nullptr, p->err,
+                               0, 0, 0};
+        }
+        if (tracked(VST_K_ROPE_APPEND, s, [&] { return launch_rope_append(ac, aj, nj, s); }) != cudaSuccess)
+            return VST_E_CUDA;
+        // one loop-shape launch over every query tile of every clip; mask [i - left + 1, i + right - 1]
+        EncAttnCommon ec{m->rope, T, H, left, T, 0, 0, 0, 1, (float)(1.4426950408889634 / std::sqrt((double)D)),
+                         right > 0 ? right - 1 : 0};
+        const int grid_x = (T + kEncTileN - 1) / kEncTileN;
+        if (tracked(VST_K_ENC_ATTN, s, [&] { return launch_enc_attn(ec, ej, nj, grid_x, s); }) != cudaSuccess)
+            return VST_E_CUDA;
+    }
+    return VST_OK;
+}
+
+vst_status vst_offline_check(vst_offline* p, void* stream)
+{
+    if (!p)
+        return VST_E_INVAL;
+    DeviceGuard g(p->m->device);
+    int err = 0;
+    cudaStream_t s = as_stream(stream);
+    if (cudaMemcpyAsync(&err, p->err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return VST_E_CUDA;
+    if (err != 0) {
+        cudaMemsetAsync(p->err, 0, sizeof(int), s);
+        return VST_E_TIMEOUT;
     }
     return VST_OK;
 }

@@ -92,6 +92,7 @@ struct EncAttnCommon {
     int early;               // 1: ring loads may start before the previous kernel completes
     int appended;            // 1: the batch's K'/V rows are already in the ring (loop shape)
     float scale_log2;        // log2(e) / sqrt(D)
+    int right;               // keys after the query that the mask shows (loop shape; 0: causal)
 };
 
 struct DecJob {

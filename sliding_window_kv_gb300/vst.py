@@ -46,6 +46,7 @@ K_ROPE_APPEND, K_COMPACT, K_ENC_ATTN, K_DEC_STEP, K_COUNT = 0, 1, 2, 3, 4
 EXPORTS = ["vst_config_default", "vst_module_create", "vst_module_destroy", "vst_module_config",
            "vst_ctx_bytes", "vst_ctx_create", "vst_ctx_reset", "vst_ctx_destroy", "vst_ctx_info_get",
            "vst_ctx_check", "vst_enc_feed", "vst_enc_feed_batch", "vst_ctx_compact", "vst_enc_plan",
+           "vst_offline_bytes", "vst_offline_create", "vst_offline_destroy", "vst_enc_offline", "vst_offline_check",
            "vst_dec_step", "vst_dec_step_noalloc", "vst_dec_prefill", "vst_dec_append", "vst_prof_enable", "vst_prof_read", "vst_launch_count",
            "vst_kernel_name", "vst_status_str", "vst_version"]
 
@@ -80,6 +81,11 @@ def lib():
             "vst_dec_step": ([PP, I32, P, P, P, P, P], I32),
             "vst_dec_step_noalloc": ([PP, I32, P, P, P, P, P], I32),
             "vst_dec_prefill": ([P, P, P, P, I32, P, P], I32),
+            "vst_offline_bytes": ([P, I32, I32], SZ),
+            "vst_offline_create": ([P, I32, I32, P, SZ, PP], I32),
+            "vst_offline_destroy": ([P], I32),
+            "vst_enc_offline": ([P, P, P, P, I32, I32, P, P], I32),
+            "vst_offline_check": ([P, P], I32),
             "vst_dec_append": ([P, P, P, I32, P], I32),
             "vst_prof_enable": ([I32], I32),
             "vst_prof_read": ([ctypes.POINTER(ProfStat), I32], I32),
@@ -229,6 +235,32 @@ def dec_prefill(c: int, q, k, v, out, n: int | None = None, stream=None):
     """vst_dec_prefill: n tokens of one decoder ctx, q/out [n][H][D], k/v [n][Hk][D]."""
     n = q.shape[0] if n is None else n
     _check(lib().vst_dec_prefill(c, _ptr(q), _ptr(k), _ptr(v), n, _ptr(out), _stream(stream)), "vst_dec_prefill")
+
+
+class Offline:
+    """Owning wrapper: vst_offline_create / vst_offline_destroy (library-owned scratch)."""
+
+    def __init__(self, module: "Module", B: int, T: int):
+        out = ctypes.c_void_p()
+        _check(lib().vst_offline_create(module.handle, B, T, None, 0, ctypes.byref(out)), "vst_offline_create")
+        self.handle, self.B, self.T = out.value, B, T
+
+    def run(self, q, k, v, out, left: int, right: int = 0, stream=None):
+        """vst_enc_offline: q, k, v, out [B][T][H][D]."""
+        _check(lib().vst_enc_offline(self.handle, _ptr(q), _ptr(k), _ptr(v), left, right, _ptr(out),
+                                     _stream(stream)), "vst_enc_offline")
+
+    def check(self, stream=None) -> int:
+        return lib().vst_offline_check(self.handle, _stream(stream))
+
+    def close(self):
+        if self.handle:
+            lib().vst_offline_destroy(self.handle)
+            self.handle = None
+
+
+def offline_bytes(module_handle: int, B: int, T: int) -> int:
+    return lib().vst_offline_bytes(module_handle, B, T)
 
 
 def dec_append(c: int, k, v, n: int | None = None, stream=None):
