@@ -47,6 +47,10 @@ WORKLOADS = {
     "dec_b1": dict(kind="dec", layers=26, streams=1, fill="full", steps=256, seed=3),
     # decoder, 26 layers, 64 streams with fills uniform in [1, 8192]
     "dec_b64": dict(kind="dec", layers=26, streams=64, fill="uniform", steps=256, seed=4),
+    # offline encoder, 32 layers, 4 whole clips of 4416 frames, the streaming mask (750, 0)
+    "enc_offline4": dict(kind="offline", layers=32, clips=4, frames=4416, left=750, right=0, seed=8),
+    # the same with a 4-frame right lookahead (the pages' (left, right) sliding mask)
+    "enc_offline4_la": dict(kind="offline", layers=32, clips=4, frames=4416, left=750, right=4, seed=8),
     # decoder prefill, 26 layers, one stream: the 39-token prompt on an empty cache
     "dec_prefill39": dict(kind="prefill", layers=26, tokens=39, seed=6),
     # decoder prefill, 26 layers, one stream: a 512-token prompt on an empty cache
@@ -412,6 +416,41 @@ class PrefillWorkload:
         self.module.close()
 
 
+class OfflineWorkload:
+    """32 encoder layers over B whole clips of T frames (vst_enc_offline per layer, one plan
+    shared by the layers). Inputs of layer l are [B][T][H][D] buffers."""
+
+    def __init__(self, spec, dev, rank=0):
+        import torch
+        from sliding_window_kv_gb300 import synth, vst
+        self.vst = vst
+        self.L, self.B, self.T = spec["layers"], spec["clips"], spec["frames"]
+        self.left, self.right = spec["left"], spec["right"]
+        seed = spec["seed"] + 1000 * rank
+        self.module = vst.Module(vst.ENC)
+        self.plan = vst.Offline(self.module, self.B, self.T)
+        mk = lambda l, i: torch.stack([synth.frames(synth.tensor_key(seed, b, l, i), 0, self.T, ENC_H, ENC_D, dev)
+                                       for b in range(self.B)])
+        self.Q = [mk(l, 0) for l in range(self.L)]
+        self.K = [mk(l, 1) for l in range(self.L)]
+        self.V = [mk(l, 2) for l in range(self.L)]
+        self.O = [torch.empty_like(q) for q in self.Q]
+
+    def run(self, stream):
+        for l in range(self.L):
+            self.plan.run(self.Q[l], self.K[l], self.V[l], self.O[l], self.left, self.right, stream)
+
+    def flops_per_launch(self):
+        """4·D FLOP per visible (query, key) pair per head, for one layer of all clips."""
+        T, L, R = self.T, self.left, max(self.right - 1, 0)
+        pairs = sum(min(i, L - 1) + 1 + min(R, T - 1 - i) for i in range(T))
+        return 4.0 * ENC_D * pairs * ENC_H * self.B
+
+    def close(self):
+        self.plan.close()
+        self.module.close()
+
+
 # ---------------------------------------------------------------- timing helpers
 
 def capture(fn, stream):
@@ -493,17 +532,18 @@ def kernel_source_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def dram_traffic(kernel: str, units_per_launch: float, workload: str = ""):
+def dram_traffic(kernel: str, units_per_launch: float, workload: str = "", fallback: bool = True):
     """DRAM bytes (read + write) per launch from the committed ncu capture, scaled from the
     captured case to this launch by the work units it processes; None when there is no
     capture or the kernel's source changed since it was taken. A capture of the workload's
-    own launch shape ("kernel@workload") is preferred to the kernel's default one."""
+    own launch shape ("kernel@workload") is preferred to the kernel's default one, which is
+    used only when `fallback` (the same launch shape)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         t = json.load(open(p))
-        d = t.get("%s@%s" % (kernel, workload)) or t.get(kernel)
+        d = t.get("%s@%s" % (kernel, workload)) or (t.get(kernel) if fallback else None)
         if not d or d.get("source_sha") != kernel_source_sha(kernel):
             return None
         return d["dram_bytes_per_unit"] * units_per_launch
@@ -646,6 +686,42 @@ def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu):
     return out
 
 
+def bench_offline(spec, dev, stream, dist, steps, warmup, peaks):
+    import torch
+    from sliding_window_kv_gb300 import vst
+    w = OfflineWorkload(spec, dev, dist.rank)
+    w.run(stream)  # eager warm-up (configures the kernels)
+    torch.cuda.synchronize()
+    n0 = vst.launch_count()
+    g = capture(w.run, stream)
+    launches = vst.launch_count() - n0
+    for _ in range(max(1, warmup)):
+        g.replay()
+    ms = dist.max(time_graph(g, stream, steps, dist)) / steps  # per pass of all layers
+    frames_per_s = dist.world * w.B * w.T / (ms / 1e3)
+    prof = profiled_kernels(w.run, stream)
+    nl, kms = prof["enc_attn_kernel"]
+    flops = w.flops_per_launch()
+    launch_us = region_launch_us(prof, "enc_attn_kernel", ms)
+    achieved = flops / (launch_us / 1e6) / 1e12
+    _, tflops, _, src = peaks
+    out = {"value": frames_per_s, "unit": "enc frames/s",
+           "config": {"workload": "enc_offline_%dL_20x64_%dclips_%dframes_left%d_right%d" % (w.L, w.B, w.T, w.left, w.right),
+                      "layers": w.L, "clips": w.B, "frames_per_clip": w.T, "left": w.left, "right": w.right,
+                      "seed": spec["seed"], "l2": "inputs larger than L2 (no flush)"},
+           "ms_per_step": ms, "gpu_launches": launches,
+           "roofline": {"kernel": "enc_attn_kernel", "bound": "tensor", "achieved": achieved, "peak": tflops,
+                        "unit": "TFLOP/s", "frac": achieved / tflops,
+                        "traffic": dram_traffic("enc_attn_kernel", flops, "enc_offline%d" % w.B + ("_la" if w.right else ""),
+                                                fallback=False),
+                        "peak_source": src, "launches": nl, "avg_launch_us": launch_us,
+                        "isolated_launch_us": 1e3 * kms / nl, "timing": TIMING_NOTE,
+                        "algorithmic_flops_per_launch": flops},
+           "kernels": {k: {"launches": v[0], "total_ms": v[1]} for k, v in prof.items()}}
+    w.close()
+    return out
+
+
 def bench_prefill(spec, dev, stream, dist, steps, warmup, peaks):
     import torch
     from sliding_window_kv_gb300 import vst
@@ -673,7 +749,7 @@ def bench_prefill(spec, dev, stream, dist, steps, warmup, peaks):
            "ms_per_step": ms, "gpu_launches": launches,
            "roofline": {"kernel": "dec_step_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm,
                         "unit": "GB/s", "frac": achieved / hbm,
-                        "traffic": dram_traffic("dec_step_kernel", bytes_per_launch),
+                        "traffic": dram_traffic("dec_step_kernel", bytes_per_launch, "dec_prefill%d" % w.n, fallback=False),
                         "peak_source": src, "launches": nl, "avg_launch_us": launch_us,
                         "isolated_launch_us": 1e3 * kms / nl, "timing": TIMING_NOTE,
                         "algorithmic_bytes_per_launch": bytes_per_launch}}
@@ -700,6 +776,18 @@ def run_vst(args, dist):
     line = {"metric": METRIC, "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded counter-hash bf16 ~N(0,1))", "impl": "vst"}
+
+    if spec["kind"] == "offline":
+        with torch.cuda.stream(stream):
+            sampler.start()
+            d = bench_offline(spec, dev, stream, dist, args.steps, args.warmup, peaks)
+            clocks = sampler.stop()
+        line.update({"value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"], "config": d["config"],
+                     "roofline": d["roofline"], "gpu_launches": d["gpu_launches"], "kernels": d["kernels"],
+                     "clocks": clocks})
+        if dist.rank == 0:
+            print(json.dumps(line))
+        return
 
     if spec["kind"] == "prefill":
         with torch.cuda.stream(stream):
