@@ -18,10 +18,11 @@
 //   O^T = V^T P^T    tcgen05.mma M=128 dims, N=16, K=128 keys; A = V tile read as
 //                    MN-major (dims contiguous), B = P^T (K-major); TMEM
 //   fold             thread (head h, dim d) folds (m_t, l_t, O_t[h][d]) into registers.
-// Pipeline: one K/V stage per CTA and two CTAs per SM, so that one CTA's prologue and
-// merge overlap another's streaming (also across launches: the next launch's CTAs share
-// the SM while this one finishes). The next K is fetched as soon as S^T is done, the next
-// V as soon as O^T is done; S^T alternates between two TMEM buffers.
+// Pipeline: one K buffer and two V buffers per CTA and two CTAs per SM, so that one CTA's
+// prologue and merge overlap another's streaming (also across launches: the next launch's
+// CTAs share the SM while this one finishes). The next K is fetched as soon as S^T is
+// done; V runs two tiles ahead (V of tile i + 2 as soon as O^T of tile i is done); S^T
+// alternates between two TMEM buffers.
 // The query heads are rotated in the prologue; if the split holds pos, the new key is
 // rotated too, patched into its tile row in shared memory, and stored (K', V) to ring slot
 // pos % R by this CTA. A prefill chunk (several tokens of one stream, one job each) has its
@@ -43,16 +44,19 @@ constexpr int kG = 4;                       // query heads per KV head
 constexpr int kTile = kDecTile;             // keys per tile
 constexpr int kTilesPerSplit = kDecSplit / kTile;
 constexpr uint32_t kBox = 128u * 128u;      // 128 keys x 64 dims x 2 B
-constexpr uint32_t kStage = 4 * kBox;       // K lo, K hi, V lo, V hi
+constexpr uint32_t kStage = 6 * kBox;       // K lo, K hi, then two V buffers (lo, hi)
 constexpr uint32_t kTmemCols = 64;          // S^T buffers at [0,16) and [16,32); O^T at [32,48)
 constexpr uint32_t kTmO = 32;
+// Split partials loaded per round of the last CTA's fold: 17, the splits of a full 8192
+// window, so that one round trip fetches them all.
+constexpr int kMergeGroup = 17;
 
 struct Layout {
     static constexpr uint32_t kOffQ = kStage;           // Q' [16 rows][128 dims]: 2 blocks of 2 KB
     static constexpr uint32_t kOffP = kOffQ + 4096;     // P^T [16 rows][128 keys]: 2 blocks of 2 KB
     static constexpr uint32_t kOffNew = kOffP + 4096;   // new K' row, new V row (bf16 x 128 each)
     static constexpr uint32_t kOffRed = kOffNew + 512;  // float [2][4 heads][4 warps]; merge coefficients
-    static constexpr uint32_t kOffBar = kOffRed + 4 * 32 * 3 * 4;  // 5 mbarriers
+    static constexpr uint32_t kOffBar = kOffRed + 4 * 32 * 3 * 4;  // 6 mbarriers
     static constexpr uint32_t kSmemBytes = kOffBar + 128 + 1024;
 };
 
@@ -118,8 +122,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     float* red_m = reinterpret_cast<float*>(smem + L::kOffRed);  // [4 heads][4 warps]
     float* red_l = red_m + 16;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-    // bars: K landed, V landed, S^T done [2], O^T done
-    const uint32_t bar_k = smem_u32(&bars[0]), bar_v = smem_u32(&bars[1]);
+    // bars: K landed, V buffer 0 landed, S^T done [2], O^T done, V buffer 1 landed
+    const uint32_t bar_k = smem_u32(&bars[0]);
+    auto bar_v = [&](int i) { return smem_u32(&bars[(i & 1) ? 5 : 1]); };  // V of tile i
     auto bar_s = [&](int b) { return smem_u32(&bars[2 + b]); };
     const uint32_t bar_o = smem_u32(&bars[4]);
 
@@ -146,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the ring (a prefill chunk, appended before the launch).
     const bool has_new = !c.appended && tau_new >= tau_lo && tau_new <= tau_hi;
 
-    uint8_t* const sK = smem;             // K tile: two 64-dim boxes
-    uint8_t* const sV = smem + 2 * kBox;  // V tile
+    uint8_t* const sK = smem;  // K tile: two 64-dim boxes
+    auto sV = [&](int i) { return smem + (2 + 2 * (i & 1)) * kBox; };  // V of tile i: two buffers
     auto parity = [&](int i) { return (uint32_t)(i & 1); };
     auto slot_of = [&](int i) { return (int)(((tau_lo + i) * kTile) % c.R); };
     auto issue_k = [&](int i) {
@@ -157,21 +162,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_3d(dst + kBox, job.tmap_k, bar_k, 64, slot_of(i), g);
     };
     auto issue_v = [&](int i) {
-        const uint32_t dst = smem_u32(sV);
-        mbar_arrive_expect_tx(bar_v, 2 * kBox);
-        tma_load_3d(dst, job.tmap_v, bar_v, 0, slot_of(i), g);
-        tma_load_3d(dst + kBox, job.tmap_v, bar_v, 64, slot_of(i), g);
+        const uint32_t dst = smem_u32(sV(i));
+        mbar_arrive_expect_tx(bar_v(i), 2 * kBox);
+        tma_load_3d(dst, job.tmap_v, bar_v(i), 0, slot_of(i), g);
+        tma_load_3d(dst + kBox, job.tmap_v, bar_v(i), 64, slot_of(i), g);
     };
     auto issue_first = [&]() {  // every split has at least one tile
         issue_k(0);
         issue_v(0);
+        if (n_tiles > 1)
+            issue_v(1);
     };
 
     // Prologue. The first ring tiles may be requested before the previous kernel in the
     // stream has finished when the host says that kernel did not touch this ring (early);
     // everything else waits for it.
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b)
+        for (int b = 0; b < 6; ++b)
             mbar_init(smem_u32(&bars[b]), 1);
         fence_mbar_init();
         tmap_acquire(job.tmap_k);
@@ -286,11 +293,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             red_l[hh * 4 + (warp & 3)] = ws;
 
         // ---- V of tile i (new value patched in), then O^T = V^T P^T
-        if (!mbar_wait(bar_v, parity(i)))
+        if (!mbar_wait(bar_v(i), (uint32_t)((i >> 1) & 1)))
             fail = 1;
         if (!fail && has_new && tau_lo + i == tau_new && tid < 16) {
             const uint4 vw = reinterpret_cast<const uint4*>(snew + kD)[tid];
-            *reinterpret_cast<uint4*>(sV + (tid >> 3) * kBox + sw128_offset(rr_new, tid & 7)) = vw;
+            *reinterpret_cast<uint4*>(sV(i) + (tid >> 3) * kBox + sw128_offset(rr_new, tid & 7)) = vw;
             *reinterpret_cast<uint4*>(job.v_ring + ((long long)g * c.R + pos % c.R) * kD + 8 * tid) = vw;
         }
         fence_proxy_async_smem();
@@ -304,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (warp == 0) {  // converged after the barrier; the elected lane issues
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t ad = smem_desc_sw128(smem_u32(sV) + 2048 * kk, kBox, 1024);
+                const uint64_t ad = smem_desc_sw128(smem_u32(sV(i)) + 2048 * kk, kBox, 1024);
                 const uint64_t bd = smem_desc_sw128(smem_u32(sP) + (kk >> 2) * 2048 + 32 * (kk & 3), 16, 1024);
                 mma_bf16_ss_if(tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u, elect);
             }
@@ -314,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             fail = 1;
         ph_o ^= 1;
         tc_fence_after();
-        if (tid == 0 && !fail && i + 1 < n_tiles)
-            issue_v(i + 1);  // the V buffer is free once O^T of tile i is done
+        if (tid == 0 && !fail && i + 2 < n_tiles)
+            issue_v(i + 2);  // tile i's V buffer is free once O^T of tile i is done
         const uint32_t ov = tmem_ld_32x32b_x1(tmem + lane_base + kTmO + hh);
         tmem_ld_wait();
         fold1(m, l, o, mt, lt, __uint_as_float(ov));
@@ -329,7 +336,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             // land, release TMEM and leave.
             atomicExch(job.err, kErrTimeout);
             mbar_wait(bar_k, 0);
-            mbar_wait(bar_v, 0);
+            mbar_wait(bar_v(0), 0);
+            mbar_wait(bar_v(1), 0);
         }
     } else {
         // ---- this split's partial; the last CTA of (stream, g) folds all splits in order.
@@ -354,12 +362,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             // exact prefix max), and every thread replays the same FMA chain for its dim.
             const int ns = job.n_splits;
             float* coef = red_m;  // [4 heads][32 splits][a, b, l_u]: reuses the reduction area
-            // this dim's partials of the first 16 splits: in flight while the coefficients
+            // this dim's partials of the first kMergeGroup splits: in flight while the coefficients
             // are computed
             const float* po = job.part_o + (long long)hq * c.S * kD + row;
-            float ov0[16];
+            float ov0[kMergeGroup];
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
+            for (int u = 0; u < kMergeGroup; ++u)
                 ov0[u] = u < ns ? __ldcg(po + (long long)u * kD) : 0.f;
             if ((warp & 3) == 0) {
                 float2 mlv = make_float2(-INFINITY, 0.f);
@@ -382,13 +390,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             head_sync(hh);
             const float* cf = coef + hh * 32 * 3;
             float oo = 0.f, ll = 0.f;
-            for (int u0 = 0; u0 < ns; u0 += 16) {
-                float ov[16];
+            for (int u0 = 0; u0 < ns; u0 += kMergeGroup) {
+                float ov[kMergeGroup];
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
+                for (int u = 0; u < kMergeGroup; ++u)
                     ov[u] = u0 == 0 ? ov0[u] : (u0 + u < ns ? __ldcg(po + (long long)(u0 + u) * kD) : 0.f);
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
+                for (int u = 0; u < kMergeGroup; ++u) {
                     if (u0 + u < ns) {
                         const float a = cf[(u0 + u) * 3], b = cf[(u0 + u) * 3 + 1], lu = cf[(u0 + u) * 3 + 2];
                         ll = __fmaf_rn(ll, a, __fmul_rn(lu, b));
