@@ -57,7 +57,7 @@ constexpr uint32_t kOffP = kOffV + kTileBytes;         // two 64-key blocks
 constexpr uint32_t kOffRedM = kOffP + 2 * kTileBytes;  // float [2 tile parities][2 halves][128]
 constexpr uint32_t kOffRedL = kOffRedM + 2 * 2 * 128 * 4;
 constexpr uint32_t kOffBar = kOffRedL + 2 * 2 * 128 * 4;
-constexpr int kNumBars = 12;
+constexpr int kNumBars = 13;
 constexpr uint32_t kSmemBytes = kOffBar + 8 * kNumBars + 1024;  // + slack to align the base to 1024
 constexpr uint32_t kTmemCols = 256;  // two 128-column buffers: S_t, then O_t in its first 64 columns
 
@@ -72,6 +72,8 @@ constexpr int kBarO = 5;      // 5, 6: O in TMEM buffer ready (MMA commit)
 constexpr int kBarFree = 7;   // 7, 8: O in TMEM buffer read by all eight softmax warps
 constexpr int kBarP = 9;      // 9, 10: P keys [64 half, 64 half + 64) written by the four warps of that half
 constexpr int kBarQ = 11;     // Q' written by all eight softmax warps
+constexpr int kBarQin = 12;   // raw queries and their (cos, sin) rows landed (TMA)
+constexpr uint32_t kQinBytes = kTileBytes + 128u * kD * 4u;  // 128 query rows + 128 table rows
 
 }  // namespace
 
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
 #pragma unroll
             for (int i = 0; i < kNumBars; ++i)
-                mbar_init(bar(i), i == kBarP || i == kBarP + 1 ? 4u : i >= kBarFree ? 8u : 1u);
+                mbar_init(bar(i), i == kBarP || i == kBarP + 1 ? 4u : (i >= kBarFree && i <= kBarQ) ? 8u : 1u);
             fence_mbar_init();
         }
         __syncwarp();
@@ -186,14 +188,22 @@ __global__ void __launch_bounds__(kThreads, 2)
         };
 
         // The first ring tiles may be requested before the previous kernel in the stream has
-        // finished when the host says that kernel did not touch this ring (early).
+        // finished when the host says that kernel did not touch this ring (early). The rows of
+        // the constant (cos, sin) table go at once (into P, unused until the first exps), the
+        // queries once the previous kernel is done.
         if (e) {
             tmap_acquire(job.tmap_k);
             tmap_acquire(job.tmap_v);
+            tmap_acquire(c.tmap_rope);
+            mbar_arrive_expect_tx(bar(kBarQin), kQinBytes);
+            tma_load_2d(smem_u32(sP), c.tmap_rope, bar(kBarQin), 0, (int)p_first);
         }
+        pend |= 1u << kBarQin;  // waited by the softmax warps; here only after a failure
         if (c.early)
             issue_first();
         griddep_wait();
+        if (e)
+            tma_load_4d(smem_u32(sQ), &c.tmap_q, bar(kBarQin), 0, h, row0, job.q_z);
         if (!c.early)
             issue_first();
         if (!wait(kBarQ) || !wait(kBarK))
@@ -246,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int i = 0; i < kBarFree; ++i)
                 if ((pend >> i) & 1u)
                     mbar_wait(bar(i), (ph >> i) & 1u);
+            mbar_wait(bar(kBarQin), 0);
         }
         __syncwarp();
         griddep_launch_dependents();
@@ -261,14 +272,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool row_real = r < nrows;
 
         griddep_wait();
-        if (row_real) {
-            const __nv_bfloat16* qrow = job.q + ((long long)(row0 + r) * c.H + h) * kD;
-            enc::rotate_quarter(qrow, c.rope + pq * (kD / 2), sQ, r, 2 * half);
-            enc::rotate_quarter(qrow, c.rope + pq * (kD / 2), sQ, r, 2 * half + 1);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)  // chunks {q, 4 + q} of quarters q = 2 half, 2 half + 1
-                *reinterpret_cast<uint4*>(sQ + sw128_offset(r, (e >> 1) * 4 + 2 * half + (e & 1))) = make_uint4(0, 0, 0, 0);
+        // Raw query row r (zero past the batch) and its (cos, sin) row landed by TMA: rotate
+        // this thread's two quarters in place.
+        int qfail = mbar_wait(bar(kBarQin), 0) ? 0 : 1;
+        if (!qfail) {
+            const float2* cs = reinterpret_cast<const float2*>(sP + r * (kD * 4));
+            enc::rotate_quarter_in_place(sQ, cs, r, 2 * half);
+            enc::rotate_quarter_in_place(sQ, cs, r, 2 * half + 1);
         }
         fence_proxy_async_smem();  // Q' (generic stores) before the MMAs read it
         __syncwarp();
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         float m_run = -INFINITY, l_run = 0.f;
         float mt_prev = -INFINITY;  // tile-local max of the previous tile, folded one tile late
         uint32_t ph = 0;
-        int fail = 0;
+        int fail = qfail;
         // o <- fold(o, O_t) for tile t in TMEM buffer b, with m_t = mt and l_t from red_l
         auto fold_from = [&](int b, float mt) {
             if (mbar_wait(bar(kBarO + b), (ph >> (kBarO + b)) & 1u))

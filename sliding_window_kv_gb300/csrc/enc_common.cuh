@@ -173,6 +173,30 @@ __device__ __forceinline__ void fold_tile_if(bool seen, float& m, float& l, floa
     m = seen ? f.mn : m;
 }
 
+// NEOX rotation of pairs [8q, 8q+8) of a 64-value head row: a holds elements [8q, 8q+8),
+// b elements [32+8q, 32+8q+8) (bf16), cs the row's 32 (cos, sin) pairs; ya, yb the results.
+__device__ __forceinline__ void rotate_chunks(const uint4 a, const uint4 b, const float2* cs, int q, uint4& ya,
+                                              uint4& yb)
+{
+    const float4* cs4 = reinterpret_cast<const float4*>(cs + 8 * q);  // 8 (cos, sin) pairs, 16-B aligned
+    const float4 c01 = cs4[0], c23 = cs4[1], c45 = cs4[2], c67 = cs4[3];
+    const float2 cw[8] = {{c01.x, c01.y}, {c01.z, c01.w}, {c23.x, c23.y}, {c23.z, c23.w},
+                          {c45.x, c45.y}, {c45.z, c45.w}, {c67.x, c67.y}, {c67.z, c67.w}};
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+    uint32_t ra[4], rb[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float y1a, y2a, y1b, y2b;
+        rope_pair(bf16lo(aw[w]), bf16lo(bw[w]), cw[2 * w], y1a, y2a);
+        rope_pair(bf16hi(aw[w]), bf16hi(bw[w]), cw[2 * w + 1], y1b, y2b);
+        ra[w] = pack_bf16(y1a, y1b);
+        rb[w] = pack_bf16(y2a, y2b);
+    }
+    ya = make_uint4(ra[0], ra[1], ra[2], ra[3]);
+    yb = make_uint4(rb[0], rb[1], rb[2], rb[3]);
+}
+
 // Rotate pairs [8q, 8q+8) of a 64-value head row (NEOX: element i pairs with i + 32) at the
 // angle table row cs, and write them as chunks q and 4 + q of a swizzled 128-byte row.
 __device__ __forceinline__ void rotate_quarter(const __nv_bfloat16* src, const float2* cs, uint8_t* tile, int row,
@@ -180,23 +204,21 @@ __device__ __forceinline__ void rotate_quarter(const __nv_bfloat16* src, const f
 {
     const uint4 a = *reinterpret_cast<const uint4*>(src + 8 * q);
     const uint4 b = *reinterpret_cast<const uint4*>(src + 32 + 8 * q);
-    const float4* cs4 = reinterpret_cast<const float4*>(cs + 8 * q);  // 8 (cos, sin) pairs, 16-B aligned
-    const float4 c01 = cs4[0], c23 = cs4[1], c45 = cs4[2], c67 = cs4[3];
-    const float2 cw[8] = {{c01.x, c01.y}, {c01.z, c01.w}, {c23.x, c23.y}, {c23.z, c23.w},
-                          {c45.x, c45.y}, {c45.z, c45.w}, {c67.x, c67.y}, {c67.z, c67.w}};
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-    uint32_t ya[4], yb[4];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        float y1a, y2a, y1b, y2b;
-        rope_pair(bf16lo(aw[w]), bf16lo(bw[w]), cw[2 * w], y1a, y2a);
-        rope_pair(bf16hi(aw[w]), bf16hi(bw[w]), cw[2 * w + 1], y1b, y2b);
-        ya[w] = pack_bf16(y1a, y1b);
-        yb[w] = pack_bf16(y2a, y2b);
-    }
-    *reinterpret_cast<uint4*>(tile + sw128_offset(row, q)) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-    *reinterpret_cast<uint4*>(tile + sw128_offset(row, 4 + q)) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+    uint4 ya, yb;
+    rotate_chunks(a, b, cs, q, ya, yb);
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, q)) = ya;
+    *reinterpret_cast<uint4*>(tile + sw128_offset(row, 4 + q)) = yb;
+}
+
+// The same rotation in place, for a row already in the swizzled tile (landed there by TMA).
+__device__ __forceinline__ void rotate_quarter_in_place(uint8_t* tile, const float2* cs, int row, int q)
+{
+    uint4* pa = reinterpret_cast<uint4*>(tile + sw128_offset(row, q));
+    uint4* pb = reinterpret_cast<uint4*>(tile + sw128_offset(row, 4 + q));
+    uint4 ya, yb;
+    rotate_chunks(*pa, *pb, cs, q, ya, yb);
+    *pa = ya;
+    *pb = yb;
 }
 
 // Store N consecutive output dims starting at dim d0 of an output row: o * (1 / l) as bf16

@@ -29,6 +29,7 @@ struct vst_module {
     int n_sms;     // SMs of the device (launch-shape choice)
     float2* rope;  // device [max_position][D/2]
     int splits;    // scratch slots per head: decoder splits per step / encoder key tiles
+    CUtensorMap* rope_map;  // device: tensor map over the rope table (128-row boxes)
 };
 
 struct vst_ctx {
@@ -183,6 +184,23 @@ bool make_ring_map(CUtensorMap* map, void* base, const vst_config& c)
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Tensor map over a launch's queries for the loop shape: rows of D bf16 at `base`, laid out
+// [jobs][row stride `job_rows`][H][D]; dims {D, H, rows, jobs}, box {D, 1, 128, 1}, 128-B
+// swizzle (the Q' operand layout), zero fill past the rows.
+bool make_query_map(CUtensorMap* map, const void* base, int D, int H, int rows, int jobs, long long job_rows)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)jobs};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)job_rows * H * D * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)D, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // ---- launch accounting and optional per-kernel event timing
 std::atomic<long long> g_launches{0};
@@ -435,6 +453,27 @@ vst_status vst_module_create(const vst_config* cfg, vst_module** out)
         delete m;
         return VST_E_CUDA;
     }
+    // the encoder's loop shape fetches 128 rows of the table at a time by TMA
+    if (cfg->kind == VST_ENC) {
+        CUtensorMap host;
+        auto fn = encode_fn();
+        const cuuint64_t dims[2] = {(cuuint64_t)cfg->head_dim, (cuuint64_t)cfg->max_position};
+        const cuuint64_t strides[1] = {(cuuint64_t)cfg->head_dim * sizeof(float)};
+        const cuuint32_t box[2] = {(cuuint32_t)cfg->head_dim, 128};
+        const cuuint32_t estr[2] = {1, 1};
+        void* dmap = nullptr;
+        if (!fn || fn(&host, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, m->rope, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            cudaMalloc(&dmap, sizeof(CUtensorMap)) != cudaSuccess ||
+            cudaMemcpy(dmap, &host, sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaFree(dmap);
+            cudaFree(m->rope);
+            delete m;
+            return VST_E_UNSUPPORTED;
+        }
+        m->rope_map = static_cast<CUtensorMap*>(dmap);
+    }
     *out = m;
     return VST_OK;
 }
@@ -445,6 +484,7 @@ vst_status vst_module_destroy(vst_module* m)
         return VST_E_INVAL;
     DeviceGuard g(m->device);
     cudaFree(m->rope);
+    cudaFree(m->rope_map);
     delete m;
     return VST_OK;
 }
@@ -637,8 +677,9 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
     auto* ob = static_cast<__nv_bfloat16*>(out);
 
     const CompactCommon cc{Hk, cfg.ring_slots, D, cfg.window};
-    const EncAttnCommon ec{m->rope, 0, H, cfg.window, cfg.ring_slots, 0, m->splits, 0, 0,
-                           (float)(1.4426950408889634 / std::sqrt((double)D))};
+    EncAttnCommon ec{m->rope, 0, H, cfg.window, cfg.ring_slots, 0, m->splits, 0, 0,
+                     (float)(1.4426950408889634 / std::sqrt((double)D))};
+    ec.tmap_rope = m->rope_map;
     CompactJob cj[kMaxJobs];
     const vst_ctx* cctx[kMaxJobs];
     EncAttnJob ej[kMaxJobs];
@@ -677,7 +718,7 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
                 const long long row = (long long)(c0 + i) * n_new + off;
                 ej[i] = EncAttnJob{qb + row * H * D, kb + row * Hk * D, vb + row * Hk * D, ob + row * H * D,
                                    c->k_ring, c->v_ring, c->tmap_k, c->tmap_v, c->part_ml, c->part_o,
-                                   c->counters, c->err, c->abs_next, c->abs_base, c->n_kv};
+                                   c->counters, c->err, c->abs_next, c->abs_base, c->n_kv, i};
                 if (split) {
                     const long long lo = c->abs_next - cfg.window + 1 > 0 ? c->abs_next - cfg.window + 1 : 0;
                     const int tiles = (int)((c->abs_next + b - 1) / kEncTileN - lo / kEncTileN + 1);
@@ -709,6 +750,8 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
             e2.n_rows = b;
             e2.split = per_cta;
             e2.appended = split ? 0 : 1;
+            if (!split && !make_query_map(&e2.tmap_q, qb + ((long long)c0 * n_new + off) * H * D, D, H, b, nj, n_new))
+                return fail_all(ctxs, n_ctx);
             e2.early = record_touch(s, ctxs + c0, nj);
             if (tracked(VST_K_ENC_ATTN, s, [&] {
                     return split ? launch_enc_attn_split(e2, ej, nj, grid_x, s) : launch_enc_attn(e2, ej, nj, grid_x, s);
@@ -919,13 +962,15 @@ vst_status vst_enc_offline(vst_offline* p, const void* q, const void* k, const v
             aj[i] = AppendJob{kb + row * Hk * D, vb + row * Hk * D, ks, vs, 0, 0};
             ej[i] = EncAttnJob{qb + row * H * D, kb + row * Hk * D, vb + row * Hk * D, ob + row * H * D, ks, vs,
                                p->maps + 2 * (b0 + i), p->maps + 2 * (b0 + i) + 1, nullptr, nullptr, nullptr, p->err,
-                               0, 0, 0};
+                               0, 0, 0, i};
         }
         if (tracked(VST_K_ROPE_APPEND, s, [&] { return launch_rope_append(ac, aj, nj, s); }) != cudaSuccess)
             return VST_E_CUDA;
         // one loop-shape launch over every query tile of every clip; mask [i - left + 1, i + right - 1]
         EncAttnCommon ec{m->rope, T, H, left, T, 0, 0, 0, 1, (float)(1.4426950408889634 / std::sqrt((double)D)),
-                         right > 0 ? right - 1 : 0};
+                         right > 0 ? right - 1 : 0, m->rope_map};
+        if (!make_query_map(&ec.tmap_q, qb + (long long)b0 * T * H * D, D, H, T, nj, T))
+            return VST_E_UNSUPPORTED;
         const int grid_x = (T + kEncTileN - 1) / kEncTileN;
         if (tracked(VST_K_ENC_ATTN, s, [&] { return launch_enc_attn(ec, ej, nj, grid_x, s); }) != cudaSuccess)
             return VST_E_CUDA;

@@ -82,6 +82,7 @@ struct EncAttnJob {
     long long pos0;          // absolute position of row 0
     long long abs_base;      // absolute position held by ring slot 0
     long long slot0;         // ring slot of row 0 (n_kv before the batch)
+    int q_z;                 // loop shape: this job's index in tmap_q's outer dimension
 };
 
 struct EncAttnCommon {
@@ -93,6 +94,8 @@ struct EncAttnCommon {
     int appended;            // 1: the batch's K'/V rows are already in the ring (loop shape)
     float scale_log2;        // log2(e) / sqrt(D)
     int right;               // keys after the query that the mask shows (loop shape; 0: causal)
+    const CUtensorMap* tmap_rope;  // loop shape: over the (cos, sin) table, fp32 {D, positions}, box {D, 128}
+    CUtensorMap tmap_q;      // loop shape: over this launch's queries {D, H, rows, jobs}, box {D, 1, 128, 1}, SW128
 };
 
 struct DecJob {
