@@ -10,6 +10,7 @@
 // elements of the second half (the NEOX pairs), so every load and store is a 16-byte
 // vector and the (cos, sin) table row is read once per pair.
 #include "common.cuh"
+#include "ptx.cuh"
 #include "vst_internal.h"
 
 namespace vst {
@@ -19,6 +20,10 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const __grid_constant_
 {
     const AppendCommon& c = p.c;
     const AppendJob& job = p.jobs[blockIdx.y];
+    // Programmatic dependent launch: the previous kernel may still read the rows this one
+    // overwrites, so wait for it; the next kernel waits for this one before it reads them.
+    griddep_wait();
+    griddep_launch_dependents();
     const int half = c.D / 2;
     const int per_vec = half / 8;  // threads per head vector
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -68,8 +73,7 @@ cudaError_t launch_rope_append(const AppendCommon& c, const AppendJob* jobs, int
     const int threads = 256;
     const dim3 grid((unsigned)((total + threads - 1) / threads), (unsigned)n_jobs);
     return with_params(c, jobs, n_jobs, [&](const auto& p) {
-        rope_append_kernel<sizeof(p.jobs) / sizeof(p.jobs[0])><<<grid, threads, 0, s>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(rope_append_kernel<sizeof(p.jobs) / sizeof(p.jobs[0])>, grid, dim3(threads), 0, s, p);
     });
 }
 
