@@ -65,7 +65,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="vst", choices=["vst", "reference"])
     ap.add_argument("--workload", default="enc_stream", choices=sorted(WORKLOADS))
-    ap.add_argument("--no-dec", action="store_true", help="skip the decoder object of the default line")
+    ap.add_argument("--no-dec", action="store_true",
+                    help="skip the secondary objects of the default line (decoder, prefill, offline encoder)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dec-steps", type=int, default=256, help="decoder steps (decoder workloads and dec object)")
@@ -895,6 +896,11 @@ def run_vst(args, dist):
             d = bench_prefill(dict(WORKLOADS["dec_prefill39"]), dev, stream, dist, args.steps, args.warmup, peaks)
             d["clocks"] = sampler3.stop()
             line["prefill"] = d
+            sampler4 = ClockSampler(dist.local_rank)
+            sampler4.start()
+            d = bench_offline(dict(WORKLOADS["enc_offline4"]), dev, stream, dist, args.steps, args.warmup, peaks)
+            d["clocks"] = sampler4.stop()
+            line["offline"] = d
 
     if not args.no_cpu and dist.rank == 0:
         v, dt, sample = cpu_baseline_enc(spec, 4 if spec["layers"] >= 4 else spec["layers"], cpu_threads())
