@@ -425,3 +425,60 @@ def test_interleaved_contexts_bit_exact(dev, enc_module, dec_module):
     for s in range(3):
         assert torch.equal(got[s], alone[s]), s
         dctx[s].close()
+
+
+def test_all_paths_interleaved_bit_exact(dev, enc_module, dec_module):
+    """Every kernel of the library is chained by programmatic dependent launch, so a launch
+    may start while the previous one, on another context or another path, still runs.
+    Streaming feeds (both launch shapes, with a compaction), decoder steps, prefill chunks
+    and offline passes issued round-robin on one CUDA stream, with the offline plan reused
+    from one pass to the next, must give the same bits as each run alone."""
+    T = 1700
+    q, k, v = _enc_inputs(61, 0, T)
+    enc_alone = _feed(enc_module, q, k, v, [512, 50, 512, 50, 512, 64])[0]
+    off_in = [_enc_inputs(62 + i, 0, 600) for i in range(3)]
+    plan = vst.Offline(enc_module, 1, 600)
+    off_alone = []
+    for i in range(3):
+        o = torch.empty((1, 600, 20, 64), dtype=torch.bfloat16, device=dev)
+        plan.run(*(x[None].to(dev) for x in off_in[i]), o, 750 if i != 1 else 16, 0 if i != 1 else 4)
+        off_alone.append(o)
+    fill = 8150
+    dq, dk, dv = _dec_seq(63, 0, 0, fill + 100)
+    dec_alone = _run_dec(dec_module, dq, dk, dv, fill=fill, steps=100)
+    torch.cuda.synchronize()
+
+    ectx = vst.Ctx(enc_module)
+    dctx = vst.Ctx(dec_module)
+    vst.dec_append(dctx.handle, dk[:fill].to(dev), dv[:fill].to(dev))
+    eq, ek, ev = q.to(dev), k.to(dev), v.to(dev)
+    qd, kd, vd = dq.to(dev), dk.to(dev), dv.to(dev)
+    enc_out = torch.empty_like(eq)
+    dec_out = torch.empty((100, 32, 128), dtype=torch.bfloat16, device=dev)
+    off_out = [torch.empty((1, 600, 20, 64), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    t = 0
+    dsteps = [("step", 1), ("prefill", 39), ("step", 1), ("prefill", 59)]
+    d = 0
+    for i, n in enumerate([512, 50, 512, 50, 512, 64]):
+        vst.enc_feed(ectx.handle, eq[t:t + n], ek[t:t + n], ev[t:t + n], enc_out[t:t + n])
+        t += n
+        if i < len(dsteps):
+            kind, m = dsteps[i]
+            a = fill + d
+            if kind == "step":
+                vst.dec_step([dctx.handle], qd[a:a + 1], kd[a:a + 1], vd[a:a + 1], dec_out[d:d + 1])
+            else:
+                vst.dec_prefill(dctx.handle, qd[a:a + m], kd[a:a + m], vd[a:a + m], dec_out[d:d + m])
+            d += m
+        if i < 3:
+            plan.run(*(x[None].to(dev) for x in off_in[i]), off_out[i], 750 if i != 1 else 16, 0 if i != 1 else 4)
+    torch.cuda.synchronize()
+    assert vst.ctx_check(ectx.handle) == vst.OK and vst.ctx_check(dctx.handle) == vst.OK
+    assert plan.check() == vst.OK
+    assert torch.equal(enc_out, enc_alone)
+    assert d == 100 and torch.equal(dec_out, dec_alone)
+    for i in range(3):
+        assert torch.equal(off_out[i], off_alone[i]), i
+    ectx.close()
+    dctx.close()
+    plan.close()
