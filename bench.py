@@ -255,37 +255,6 @@ class EncWorkload:
                 else:
                     vst.enc_feed_batch([c.handle for c in self.ctxs[l]], q, k, v, o, n, stream)
 
-    def c_calls(self, stream):
-        """run_step as a list of C-ABI calls with their arguments resolved to plain integers
-        (handles, device pointers, the stream): what a C caller of the library issues."""
-        import ctypes
-        vst = self.vst
-        L = vst.lib()
-        sp = vst._stream(stream)
-        calls = []
-        for l in range(self.L):
-            for c in self.ctxs[l]:
-                calls.append((L.vst_ctx_reset, (c.handle, sp)))
-        for l in range(self.L):
-            pv = self.pviews[l]
-            for s in range(self.S):
-                if self.pre[s]:
-                    calls.append((L.vst_enc_feed, (self.ctxs[l][s].handle, pv[0][s].data_ptr(), pv[1][s].data_ptr(),
-                                                   pv[2][s].data_ptr(), self.pre[s], pv[3][s].data_ptr(), sp)))
-        self._handle_arrays = []
-        for f, (t, n) in enumerate(self.sched):
-            for l in range(self.L):
-                q, k, v, o = (self.views[l][i][f] for i in range(4))
-                if self.S == 1:
-                    calls.append((L.vst_enc_feed, (self.ctxs[l][0].handle, q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                                   n, o.data_ptr(), sp)))
-                else:
-                    arr = (ctypes.c_void_p * self.S)(*[c.handle for c in self.ctxs[l]])
-                    self._handle_arrays.append(arr)
-                    calls.append((L.vst_enc_feed_batch, (arr, self.S, q.data_ptr(), k.data_ptr(), v.data_ptr(), n,
-                                                         o.data_ptr(), sp)))
-        return calls
-
     def e2e_setup(self, stream):
         """End-to-end step as a streaming client runs it: the inputs of each feed (every
         layer's q, k, v) sit in one pinned host block and go to the GPU in one copy on a copy
@@ -378,33 +347,6 @@ class EncWorkload:
             with torch.cuda.stream(st["back"]):
                 st["hout"][f].copy_(st["dout"][f], non_blocking=True)
         stream.wait_stream(st["back"])
-
-    def host_buffers(self):
-        """Pinned host copies of the step's inputs and room for its outputs (for e2e)."""
-        import torch
-        npre = sum(self.pre)
-        hin = [[self.buf[l][i].cpu().pin_memory() for i in range(3)] for l in range(self.L)]
-        hin_pre = [[self.pbuf[l][i].cpu().pin_memory() for i in range(3)] for l in range(self.L)] if npre else None
-        hout = [torch.empty(self.buf[l][3].shape, dtype=torch.bfloat16, pin_memory=True) for l in range(self.L)]
-        hout_pre = [torch.empty(self.pbuf[l][3].shape, dtype=torch.bfloat16, pin_memory=True)
-                    for l in range(self.L)] if npre else None
-        return hin, hin_pre, hout, hout_pre
-
-    def e2e_step(self, bufs, stream, calls):
-        hin, hin_pre, hout, hout_pre = bufs
-        for l in range(self.L):
-            for i in range(3):
-                self.buf[l][i].copy_(hin[l][i], non_blocking=True)
-                if hin_pre:
-                    self.pbuf[l][i].copy_(hin_pre[l][i], non_blocking=True)
-        for fn, args in calls:
-            st = fn(*args)
-            if st != 0:
-                raise RuntimeError("%s failed: %d" % (fn.__name__, st))
-        for l in range(self.L):
-            hout[l].copy_(self.buf[l][3], non_blocking=True)
-            if hout_pre:
-                hout_pre[l].copy_(self.pbuf[l][3], non_blocking=True)
 
     def attn_flops(self):
         """Algorithmic FLOPs of kernel (b) per step: 4*D per visible (query, key) pair, per
