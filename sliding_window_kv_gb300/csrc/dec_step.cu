@@ -341,18 +341,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // ---- this split's partial; the last CTA of (stream, g) folds all splits in order.
-        // The CTA barrier orders every thread's partial before thread 0's releasing counter
-        // update; the last CTA's thread 0 acquires before the barrier that releases its readers.
+        // The CTA barrier orders every thread's partial before thread 0's counter update
+        // (acquire-release), which also makes the other CTAs' partials visible to the last CTA.
         const int hq = g * kG + hh;
         job.part_o[((long long)hq * c.S + sl) * kD + row] = o;
         if ((warp & 3) == 0 && lane == 0)
             *reinterpret_cast<float2*>(job.part_ml + ((long long)hq * c.S + sl) * 2) = make_float2(m, l);
         __syncthreads();
         if (tid == 0) {
-            const unsigned prev = atom_add_release_gpu(job.counters + g, 1u);
+            const unsigned prev = atom_add_acq_rel_gpu(job.counters + g, 1u);
             s_last = prev == (unsigned)(job.n_splits - 1);
-            if (s_last)
-                fence_acquire_gpu();
         }
         __syncthreads();
         if (s_last) {

@@ -390,15 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // the last CTA of (job, head) folds all tiles in ascending order. The
-        // CTA barrier orders every thread's partial before thread 0's releasing counter
-        // update (cumulative), and the last CTA's thread 0 acquires before the barrier that
-        // releases its readers.
+        // CTA barrier orders every thread's partial before thread 0's counter update
+        // (acquire-release, cumulative); the barrier after it passes what the last CTA's
+        // thread 0 acquired on to its readers.
         __syncthreads();
         if (s.tid == 0) {
-            const unsigned prev = atom_add_release_gpu(job.counters + h, 1u);
+            const unsigned prev = atom_add_acq_rel_gpu(job.counters + h, 1u);
             s_last = prev == (unsigned)((t_hi - t_lo) / c.split);  // CTAs of this (job, head) - 1
-            if (s_last)
-                fence_acquire_gpu();
         }
         __syncthreads();
         if (s_last) {

@@ -95,21 +95,16 @@ __device__ __forceinline__ int bar_sync_or(int id, int count, int pred)
 
 // ---------------------------------------------------------------- cross-CTA handoff
 
-// Atomic add at GPU scope with release semantics: the writes this thread has made or
-// observed (those of its CTA, once ordered before it by a CTA barrier) are visible to any
-// thread that observes the new count and then acquires. Returns the old count.
-__device__ __forceinline__ unsigned atom_add_release_gpu(unsigned* p, unsigned v)
+// Atomic add at GPU scope with acquire-release semantics, returning the old count: the
+// writes this thread has made or observed (those of its CTA, once ordered before it by a CTA
+// barrier) are visible to any thread that observes the new count and then acquires, and the
+// writes released before the counts this thread observes are visible to it (and, through a
+// following CTA barrier, to its CTA), so the last of several CTAs needs no separate fence.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v)
 {
     unsigned old;
-    asm volatile("atom.add.release.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
-}
-
-// Acquire at GPU scope: writes released before the counts this thread observed are visible
-// to it (and, through a following CTA barrier, to its CTA).
-__device__ __forceinline__ void fence_acquire_gpu()
-{
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMA
