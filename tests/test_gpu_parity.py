@@ -196,6 +196,53 @@ def test_enc_ring_after_compaction_bit_exact(dev, enc_module):
     ctx.close()
 
 
+def test_enc_batch_compaction_ring_bytes(dev, enc_module):
+    """A batched feed of several query tiles on which some contexts compact and some do not.
+    Three contexts fed together: fill 1100 + 300 (the move overlaps itself and the batch
+    lands inside the old source rows), fill 1530 + 300 (disjoint move, batch inside the old
+    source rows) and fill 200 + 300 (no compaction). Ring bytes, ring state and outputs equal
+    those of each context compacted explicitly and then fed alone, and rows match the
+    oracle."""
+    fills, b = [1100, 1530, 200], 300
+    seqs = [_enc_inputs(13, s, fills[s] + b) for s in range(3)]
+
+    def prefilled(s):
+        ctx = TorchCtx(enc_module, dev)
+        o = torch.empty((fills[s], 20, 64), dtype=torch.bfloat16, device=dev)
+        vst.enc_feed(ctx.handle, *(x[:fills[s]].to(dev) for x in seqs[s]), o)
+        return ctx
+
+    fused = [prefilled(s) for s in range(3)]
+    Q, K, V = (torch.stack([seqs[s][i][fills[s]:] for s in range(3)]).to(dev) for i in range(3))
+    OUT = torch.empty_like(Q)
+    vst.enc_feed_batch([c.handle for c in fused], Q, K, V, OUT, b)
+    torch.cuda.synchronize()
+    got = OUT.float().cpu().double().numpy()
+    for s in range(3):
+        ref = prefilled(s)
+        if fills[s] + b > 1536:
+            vst.ctx_compact(ref.handle)
+        out = torch.empty((b, 20, 64), dtype=torch.bfloat16, device=dev)
+        vst.enc_feed(ref.handle, *(x[fills[s]:].to(dev) for x in seqs[s]), out)
+        torch.cuda.synchronize()
+        assert vst.ctx_check(fused[s].handle) == vst.OK and vst.ctx_check(ref.handle) == vst.OK
+        a, r = fused[s].info(), ref.info()
+        assert (a.n_kv, a.abs_base, a.abs_next, a.n_compactions) == (r.n_kv, r.abs_base, r.abs_next, r.n_compactions)
+        assert torch.equal(fused[s].k_ring, ref.k_ring), s
+        assert torch.equal(fused[s].v_ring, ref.v_ring), s
+        assert torch.equal(OUT[s], out), s
+        qb, kb, vb = (synth.bits(x) for x in seqs[s])
+        for i in (0, 127, 128, b - 1):
+            p = fills[s] + i
+            j0 = max(0, p - 749)
+            want = oracle.attention_row(qb[p], kb[j0:p + 1], vb[j0:p + 1], p, 750)
+            d = np.abs(got[s, i] - want)
+            assert d.max() <= MAX_TOL, (s, i, d.max())
+        ref.close()
+    for c in fused:
+        c.close()
+
+
 @pytest.mark.parametrize("n_ctx,step", [(4, 300), (8, 100)])
 def test_enc_batch_equals_single(dev, enc_module, n_ctx, step):
     """Streams with staggered starts fed together through vst_enc_feed_batch give the same
