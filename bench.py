@@ -101,9 +101,26 @@ class Dist:
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
+    def job_rate(self, units_per_rank: float, ms_local: float):
+        """Whole-job throughput of the replicas: every rank processed `units_per_rank` units in
+        its own `ms_local`, and the job took as long as the slowest rank. Returns (units per
+        second over all ranks, the slowest rank's ms)."""
+        ms = self.max(ms_local)
+        return self.world * units_per_rank / (ms / 1e3), ms
+
     def close(self):
         if self.pg:
             self.pg.destroy_process_group()
+
+
+def want_cpu_baseline(args, dist) -> bool:
+    """The oracle's CPU baseline is timed once, on a single-GPU run's only rank."""
+    return not args.no_cpu and dist.world == 1 and dist.rank == 0
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Seed of a replica's inputs: each rank streams its own synthetic data (weak scaling)."""
+    return seed + 1000 * rank
 
 
 def _cuda_ok():
@@ -201,7 +218,7 @@ class EncWorkload:
         self.module = vst.Module(vst.ENC)
         self.ctxs = [[vst.Ctx(self.module) for _ in range(self.S)] for _ in range(self.L)]
         self.sched = enc_feed_schedule(self.frames, self.feed)
-        seed = spec["seed"] + 1000 * rank
+        seed = rank_seed(spec["seed"], rank)
         HD = ENC_H * ENC_D
         self.buf = []      # [layer][role] flat bf16 buffers (q, k, v, out)
         self.views = []    # [layer][role][feed] -> [S][n][H][D] views
@@ -392,7 +409,7 @@ class DecWorkload:
         from sliding_window_kv_gb300 import synth, vst
         self.vst = vst
         self.L, self.S, self.steps = spec["layers"], spec["streams"], n_steps
-        seed = spec["seed"] + 1000 * rank
+        seed = rank_seed(spec["seed"], rank)
         if spec["fill"] == "full":
             self.fills = [DEC_W] * self.S
         else:
@@ -456,7 +473,7 @@ class PrefillWorkload:
         from sliding_window_kv_gb300 import synth, vst
         self.vst = vst
         self.L, self.n = spec["layers"], spec["tokens"]
-        seed = spec["seed"] + 1000 * rank
+        seed = rank_seed(spec["seed"], rank)
         self.module = vst.Module(vst.DEC)
         self.ctxs = [vst.Ctx(self.module) for _ in range(self.L)]
         self.Q = [synth.frames(synth.tensor_key(seed, 0, l, 0), 0, self.n, DEC_H, DEC_D, dev) for l in range(self.L)]
@@ -496,7 +513,7 @@ class OfflineWorkload:
         self.vst = vst
         self.L, self.B, self.T = spec["layers"], spec["clips"], spec["frames"]
         self.left, self.right = spec["left"], spec["right"]
-        seed = spec["seed"] + 1000 * rank
+        seed = rank_seed(spec["seed"], rank)
         self.module = vst.Module(vst.ENC)
         self.plan = vst.Offline(self.module, self.B, self.T)
         mk = lambda l, i: torch.stack([synth.frames(synth.tensor_key(seed, b, l, i), 0, self.T, ENC_H, ENC_D, dev)
@@ -728,9 +745,7 @@ def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu):
     launches = vst.launch_count() - n0
     for _ in range(max(1, warmup)):
         g.replay()
-    ms = time_graph(g, stream, 1, dist)
-    ms = dist.max(ms)
-    steps_per_s = dist.world * w.steps / (ms / 1e3)
+    steps_per_s, ms = dist.job_rate(w.steps, time_graph(g, stream, 1, dist))
     start_pos = w.positions()
     prof = profiled_kernels(w.run_steps, stream)
     nl, kms = prof["dec_step_kernel"]
@@ -767,8 +782,8 @@ def bench_offline(spec, dev, stream, dist, steps, warmup, peaks):
     launches = vst.launch_count() - n0
     for _ in range(max(1, warmup)):
         g.replay()
-    ms = dist.max(time_graph(g, stream, steps, dist)) / steps  # per pass of all layers
-    frames_per_s = dist.world * w.B * w.T / (ms / 1e3)
+    frames_per_s, ms = dist.job_rate(w.B * w.T * steps, time_graph(g, stream, steps, dist))
+    ms /= steps  # per pass of all layers
     prof = profiled_kernels(w.run, stream)
     nl, kms = prof["enc_attn_kernel"]
     flops = w.flops_per_launch()
@@ -804,8 +819,8 @@ def bench_prefill(spec, dev, stream, dist, steps, warmup, peaks):
     launches = vst.launch_count() - n0
     for _ in range(max(1, warmup)):
         g.replay()
-    ms = dist.max(time_graph(g, stream, steps, dist)) / steps  # per run of the 26 layers
-    tok_per_s = dist.world * w.n / (ms / 1e3)
+    tok_per_s, ms = dist.job_rate(w.n * steps, time_graph(g, stream, steps, dist))
+    ms /= steps  # per run of the 26 layers
     w.reset(stream)
     prof = profiled_kernels(w.run, stream)
     nl, kms = prof["dec_step_kernel"]
@@ -873,7 +888,7 @@ def run_vst(args, dist):
     if spec["kind"] == "dec":
         with torch.cuda.stream(stream):
             sampler.start()
-            d = bench_dec(spec, dev, stream, dist, spec["steps"], args.warmup, peaks, not args.no_cpu and dist.rank == 0)
+            d = bench_dec(spec, dev, stream, dist, spec["steps"], args.warmup, peaks, want_cpu_baseline(args, dist))
             clocks = sampler.stop()
         line.update({"value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"], "config": d["config"],
                      "roofline": d["roofline"], "gpu_launches": d["gpu_launches"], "clocks": clocks})
@@ -894,9 +909,7 @@ def run_vst(args, dist):
             g.replay()
         torch.cuda.synchronize()
         sampler.start()
-        ms = time_graph(g, stream, args.steps, dist)
-        ms = dist.max(ms)
-        value = dist.world * w.frames_per_step * args.steps / (ms / 1e3)
+        value, ms = dist.job_rate(w.frames_per_step * args.steps, time_graph(g, stream, args.steps, dist))
         prof = profiled_kernels(w.run_step, stream)
         clocks = sampler.stop()
         del g
@@ -943,8 +956,8 @@ def run_vst(args, dist):
             torch.cuda.synchronize()
             wall = time.perf_counter() - t0
             dist.barrier()
-            ems = dist.max(a.elapsed_time(b))
-            line["e2e"] = {"value": dist.world * w.frames_per_step * e2e_steps / (ems / 1e3), "unit": "enc frames/s",
+            e2e_value, _ = dist.job_rate(w.frames_per_step * e2e_steps, a.elapsed_time(b))
+            line["e2e"] = {"value": e2e_value, "unit": "enc frames/s",
                            "h2d_bytes_per_step": est["h2d"], "d2h_bytes_per_step": est["d2h"],
                            "steps": e2e_steps, "host_wall_s": wall,
                            "path": "vst_enc_feed per layer and feed through the C ABI (no graph); each feed's "
@@ -959,7 +972,7 @@ def run_vst(args, dist):
             dspec = dict(WORKLOADS["dec_b1"])
             dspec["steps"] = args.dec_steps
             d = bench_dec(dspec, dev, stream, dist, args.dec_steps, args.warmup, peaks,
-                          not args.no_cpu and dist.rank == 0)
+                          want_cpu_baseline(args, dist))
             d["clocks"] = sampler2.stop()
             line["dec"] = d
             sampler3 = ClockSampler(dist.local_rank)
@@ -973,7 +986,7 @@ def run_vst(args, dist):
             d["clocks"] = sampler4.stop()
             line["offline"] = d
 
-    if not args.no_cpu and dist.rank == 0:
+    if want_cpu_baseline(args, dist):
         v, dt, sample = cpu_baseline_enc(spec, 4 if spec["layers"] >= 4 else spec["layers"], cpu_threads())
         v1, dt1, sample1 = cpu_baseline_enc(spec, 1, 1)
         line["cpu_baseline"] = {"value": v, "unit": "enc frames/s", "cores": cpu_threads(), "kind": "oracle",

@@ -129,6 +129,13 @@ VST_API vst_status vst_ctx_info_get(const vst_ctx* c, vst_ctx_info* out);
 /* Read the ctx's device error word (blocking: synchronises `stream`). Returns VST_OK, or
  * VST_E_TIMEOUT when a kernel of this ctx abandoned a bounded wait, and clears the word. */
 VST_API vst_status vst_ctx_check(vst_ctx* c, void* stream);
+/* Test helper for failure detection: one device wait of the kind every kernel uses for its
+ * copies and MMAs (an mbarrier wait bounded to 2 s of %globaltimer time), recorded in this
+ * ctx's error word. complete = 1: the wait is satisfied at once. complete = 0: nothing
+ * completes it; it gives up after the limit, the kernel records a time-out and returns, and
+ * the next vst_ctx_check reports VST_E_TIMEOUT (and clears it). Nothing faults, traps or
+ * stays pending: the ctx remains usable. Enqueued on `stream`; VST_E_INVAL for a NULL ctx. */
+VST_API vst_status vst_ctx_selftest_wait(vst_ctx* c, int32_t complete, void* stream);
 
 /* ---- encoder chunk path (streaming plan, "SHIPPED" and "Unbounded length") -------------
  * Feed n_new >= 0 frames: q [n_new][H][D], k/v [n_new][Hk][D] -> out [n_new][H][D]. Frames

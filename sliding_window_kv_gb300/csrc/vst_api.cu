@@ -612,6 +612,16 @@ vst_status vst_ctx_check(vst_ctx* c, void* stream)
     return VST_OK;
 }
 
+vst_status vst_ctx_selftest_wait(vst_ctx* c, int32_t complete, void* stream)
+{
+    if (!c)
+        return VST_E_INVAL;
+    DeviceGuard g(c->m->device);
+    if (!g.ok || launch_wait_selftest(c->err, complete ? 1 : 0, as_stream(stream)) != cudaSuccess)
+        return VST_E_CUDA;
+    return VST_OK;
+}
+
 vst_status vst_enc_plan(const vst_config* cfg, int64_t n_kv, int64_t abs_base, int32_t n_new, int32_t* batch,
                         int32_t* compact, int32_t max_steps, int32_t* n_steps, int64_t* n_kv_out,
                         int64_t* abs_base_out)

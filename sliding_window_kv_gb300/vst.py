@@ -45,7 +45,7 @@ K_ROPE_APPEND, K_COMPACT, K_ENC_ATTN, K_DEC_STEP, K_COUNT = 0, 1, 2, 3, 4
 
 EXPORTS = ["vst_config_default", "vst_module_create", "vst_module_destroy", "vst_module_config",
            "vst_ctx_bytes", "vst_ctx_create", "vst_ctx_reset", "vst_ctx_destroy", "vst_ctx_info_get",
-           "vst_ctx_check", "vst_enc_feed", "vst_enc_feed_batch", "vst_ctx_compact", "vst_enc_plan",
+           "vst_ctx_check", "vst_ctx_selftest_wait", "vst_enc_feed", "vst_enc_feed_batch", "vst_ctx_compact", "vst_enc_plan",
            "vst_offline_bytes", "vst_offline_create", "vst_offline_destroy", "vst_enc_offline", "vst_offline_check",
            "vst_dec_step", "vst_dec_step_noalloc", "vst_dec_prefill", "vst_dec_append", "vst_prof_enable", "vst_prof_read", "vst_launch_count",
            "vst_kernel_name", "vst_status_str", "vst_version"]
@@ -73,6 +73,7 @@ def lib():
             "vst_ctx_destroy": ([P], I32),
             "vst_ctx_info_get": ([P, ctypes.POINTER(CtxInfo)], I32),
             "vst_ctx_check": ([P, P], I32),
+            "vst_ctx_selftest_wait": ([P, I32, P], I32),
             "vst_enc_feed": ([P, P, P, P, I32, P, P], I32),
             "vst_enc_feed_batch": ([PP, I32, P, P, P, I32, P, P], I32),
             "vst_ctx_compact": ([P, P], I32),
@@ -184,6 +185,10 @@ def ctx_info_get(c: int) -> CtxInfo:
 
 def ctx_check(c: int, stream=None) -> int:
     return lib().vst_ctx_check(c, _stream(stream))
+
+
+def ctx_selftest_wait(c: int, complete: bool, stream=None):
+    _check(lib().vst_ctx_selftest_wait(c, 1 if complete else 0, _stream(stream)), "vst_ctx_selftest_wait")
 
 
 def enc_feed(c: int, q, k, v, out, stream=None, n_new: int | None = None):
