@@ -21,6 +21,11 @@
 
 #include "vst_internal.h"
 
+namespace vst {
+// selftest.cu: one bounded device wait recorded in `err` (satisfied at once if `complete`).
+cudaError_t launch_wait_selftest(int* err, int complete, cudaStream_t s);
+}  // namespace vst
+
 using namespace vst;
 
 struct vst_module {

@@ -145,7 +145,6 @@ cudaError_t launch_enc_attn(const EncAttnCommon& c, const EncAttnJob* jobs, int 
                             cudaStream_t s);
 cudaError_t launch_enc_attn_split(const EncAttnCommon& c, const EncAttnJob* jobs, int n_jobs, int grid_x,
                             cudaStream_t s);
-cudaError_t launch_wait_selftest(int* err, int complete, cudaStream_t s);
 cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, int total_work,
                             cudaStream_t s);
 
