@@ -406,6 +406,70 @@ def test_dec_batched_equals_single(dev, dec_module):
         c.close()
 
 
+def test_dec_batch_over_64_streams(dev, dec_module):
+    """70 streams in one vst_dec_step call: the library launches them as 64 + 6 jobs. Every
+    stream's rows equal the single-stream step's, fills from empty to past one tile."""
+    n, steps = 70, 2
+    fills = [(37 * s) % 300 for s in range(n)]
+    seqs = [_dec_seq(14, s, 0, f + steps) for s, f in enumerate(fills)]
+    ctxs = [vst.Ctx(dec_module) for _ in range(n)]
+    for c, (q, k, v), f in zip(ctxs, seqs, fills):
+        if f:
+            vst.dec_append(c.handle, k[:f].to(dev), v[:f].to(dev))
+    outs = []
+    for s in range(steps):
+        Q, K, V = (torch.stack([seqs[j][i][fills[j] + s] for j in range(n)]).to(dev) for i in range(3))
+        O = torch.empty_like(Q)
+        vst.dec_step([c.handle for c in ctxs], Q, K, V, O)
+        outs.append(O)
+    torch.cuda.synchronize()
+    for c in ctxs:
+        assert vst.ctx_check(c.handle) == vst.OK
+        c.close()
+    for i in (0, 1, 63, 64, 69):
+        single = _run_dec(dec_module, *seqs[i], fill=fills[i], steps=steps)
+        for s in range(steps):
+            assert torch.equal(outs[s][i], single[s]), (i, s)
+
+
+def test_enc_batch_over_64_contexts(dev, enc_module):
+    """66 encoder contexts in one vst_enc_feed_batch call: launched as 64 contexts (the loop
+    shape) and 2 (the split shape for a one-tile batch), with compactions due in both groups.
+    Every context's rows equal those of the context fed alone."""
+    n, T, step = 66, 1600, 100
+    pre = [1400 + (s % 3) * 40 for s in range(n)]     # every context compacts during the feeds
+    seqs = [_enc_inputs(15, s, pre[s] + T) for s in range(n)]
+
+    def prefed(s):
+        ctx = vst.Ctx(enc_module)
+        o = torch.empty((pre[s], 20, 64), dtype=torch.bfloat16, device=dev)
+        vst.enc_feed(ctx.handle, *(x[:pre[s]].to(dev) for x in seqs[s]), o)
+        return ctx
+
+    ctxs = [prefed(s) for s in range(n)]
+    Q, K, V = (torch.stack([seqs[s][i][pre[s]:] for s in range(n)]).to(dev) for i in range(3))
+    OUT = torch.empty_like(Q)
+    for t0 in range(0, T, step):
+        o = torch.empty_like(Q[:, t0:t0 + step].contiguous())
+        vst.enc_feed_batch([c.handle for c in ctxs], Q[:, t0:t0 + step].contiguous(),
+                           K[:, t0:t0 + step].contiguous(), V[:, t0:t0 + step].contiguous(), o, step)
+        OUT[:, t0:t0 + step] = o
+    torch.cuda.synchronize()
+    for c in ctxs:
+        assert vst.ctx_check(c.handle) == vst.OK
+        assert c.info().n_compactions >= 1
+        c.close()
+    for s in (0, 1, 63, 64, 65):
+        ctx = prefed(s)
+        out = torch.empty((T, 20, 64), dtype=torch.bfloat16, device=dev)
+        for t0 in range(0, T, step):
+            vst.enc_feed(ctx.handle, *(x[pre[s] + t0:pre[s] + t0 + step].to(dev) for x in seqs[s]),
+                         out[t0:t0 + step])
+        torch.cuda.synchronize()
+        ctx.close()
+        assert torch.equal(OUT[s], out), s
+
+
 def test_dec_append_ring_contents(dev, dec_module):
     """Token p lands in slot p % 8192 as bf16(RoPE(k, p)) (within bf16 rounding of the fp64
     oracle) and V bit for bit; the step path writes the same bytes as the append path."""
