@@ -119,13 +119,36 @@ def _check(s: int, what: str):
 def _ptr(t) -> int:
     if t is None:
         return 0
-    if isinstance(t, int):
+    if isinstance(t, int):  # a raw device pointer
         return t
-        # raw device pointer
     import torch
     if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
         raise ValueError("expected a contiguous bf16 CUDA tensor")
     return t.data_ptr()
+
+
+# ctx handle -> its module's config, for the size checks below (filled by ctx_create)
+_ctx_cfg: dict = {}
+
+
+def _need(t, n_elems: int, name: str):
+    """Refuse a tensor holding fewer elements than the call reads or writes from its pointer
+    (raw integer pointers are the caller's responsibility)."""
+    if t is None or isinstance(t, int):
+        return
+    if t.numel() < n_elems:
+        raise ValueError("%s: %d elements, the call needs %d" % (name, t.numel(), n_elems))
+
+
+def _need_io(cfg, rows: int, q, k, v, out):
+    """q and out hold `rows` rows of [H][D], k and v `rows` rows of [Hk][D]."""
+    if cfg is None:
+        return
+    hq, hk = rows * cfg.n_heads * cfg.head_dim, rows * cfg.n_kv_heads * cfg.head_dim
+    _need(q, hq, "q")
+    _need(k, hk, "k")
+    _need(v, hk, "v")
+    _need(out, hq, "out")
 
 
 def _stream(stream) -> int:
@@ -166,6 +189,7 @@ def ctx_bytes(m: int) -> int:
 def ctx_create(m: int, dev_mem: int = 0, nbytes: int = 0, stream=None) -> int:
     h = ctypes.c_void_p()
     _check(lib().vst_ctx_create(m, dev_mem or None, nbytes, _stream(stream), ctypes.byref(h)), "vst_ctx_create")
+    _ctx_cfg[h.value] = module_config(m)
     return h.value
 
 
@@ -175,6 +199,7 @@ def ctx_reset(c: int, stream=None):
 
 def ctx_destroy(c: int):
     _check(lib().vst_ctx_destroy(c), "vst_ctx_destroy")
+    _ctx_cfg.pop(c, None)
 
 
 def ctx_info_get(c: int) -> CtxInfo:
@@ -193,6 +218,7 @@ def ctx_selftest_wait(c: int, complete: bool, stream=None):
 
 def enc_feed(c: int, q, k, v, out, stream=None, n_new: int | None = None):
     n = q.shape[0] if n_new is None else n_new
+    _need_io(_ctx_cfg.get(c), n, q, k, v, out)
     _check(lib().vst_enc_feed(c, _ptr(q), _ptr(k), _ptr(v), n, _ptr(out), _stream(stream)), "vst_enc_feed")
 
 
@@ -203,6 +229,7 @@ def _handles(ctxs):
 
 def enc_feed_batch(ctxs, q, k, v, out, n_new: int, stream=None):
     h, keep = _handles(ctxs)
+    _need_io(_ctx_cfg.get(ctxs[0]) if ctxs else None, len(ctxs) * n_new, q, k, v, out)
     _check(lib().vst_enc_feed_batch(h, len(ctxs), _ptr(q), _ptr(k), _ptr(v), n_new, _ptr(out), _stream(stream)),
            "vst_enc_feed_batch")
 
@@ -225,6 +252,7 @@ def enc_plan(cfg: Config, n_kv: int, abs_base: int, n_new: int, max_steps: int =
 
 def dec_step(ctxs, q, k, v, out, stream=None):
     h, keep = _handles(ctxs)
+    _need_io(_ctx_cfg.get(ctxs[0]) if ctxs else None, len(ctxs), q, k, v, out)
     _check(lib().vst_dec_step(h, len(ctxs), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream)),
            "vst_dec_step")
 
@@ -232,6 +260,7 @@ def dec_step(ctxs, q, k, v, out, stream=None):
 def dec_step_noalloc(ctxs, q, k, v, out, stream=None):
     """vst_dec_step with its scratch in the library's static device array (no allocation)."""
     h, keep = _handles(ctxs)
+    _need_io(_ctx_cfg.get(ctxs[0]) if ctxs else None, len(ctxs), q, k, v, out)
     _check(lib().vst_dec_step_noalloc(h, len(ctxs), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream)),
            "vst_dec_step_noalloc")
 
@@ -239,6 +268,7 @@ def dec_step_noalloc(ctxs, q, k, v, out, stream=None):
 def dec_prefill(c: int, q, k, v, out, n: int | None = None, stream=None):
     """vst_dec_prefill: n tokens of one decoder ctx, q/out [n][H][D], k/v [n][Hk][D]."""
     n = q.shape[0] if n is None else n
+    _need_io(_ctx_cfg.get(c), n, q, k, v, out)
     _check(lib().vst_dec_prefill(c, _ptr(q), _ptr(k), _ptr(v), n, _ptr(out), _stream(stream)), "vst_dec_prefill")
 
 
@@ -248,10 +278,11 @@ class Offline:
     def __init__(self, module: "Module", B: int, T: int):
         out = ctypes.c_void_p()
         _check(lib().vst_offline_create(module.handle, B, T, None, 0, ctypes.byref(out)), "vst_offline_create")
-        self.handle, self.B, self.T = out.value, B, T
+        self.handle, self.B, self.T, self.cfg = out.value, B, T, module.cfg
 
     def run(self, q, k, v, out, left: int, right: int = 0, stream=None):
         """vst_enc_offline: q, k, v, out [B][T][H][D]."""
+        _need_io(self.cfg, self.B * self.T, q, k, v, out)
         _check(lib().vst_enc_offline(self.handle, _ptr(q), _ptr(k), _ptr(v), left, right, _ptr(out),
                                      _stream(stream)), "vst_enc_offline")
 
@@ -270,6 +301,7 @@ def offline_bytes(module_handle: int, B: int, T: int) -> int:
 
 def dec_append(c: int, k, v, n: int | None = None, stream=None):
     n = k.shape[0] if n is None else n
+    _need_io(_ctx_cfg.get(c), n, None, k, v, None)
     _check(lib().vst_dec_append(c, _ptr(k), _ptr(v), n, _stream(stream)), "vst_dec_append")
 
 

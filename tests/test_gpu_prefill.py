@@ -178,8 +178,8 @@ def test_prefill_larger_ring(dev, dec_module):
 
 
 def test_prefill_arguments(dev, dec_module):
-    """n = 0 is a no-op; a negative n or positions past max_position are refused with
-    nothing enqueued and the ctx unchanged."""
+    """n = 0 is a no-op; a negative n, positions past max_position or tensors shorter than n
+    tokens are refused with nothing enqueued and the ctx unchanged."""
     ctx = _Ctx(dec_module, dev)
     q, k, v = _dec_seq(25, 0, 4)
     out = torch.empty((4, 32, 128), dtype=torch.bfloat16, device=dev)
@@ -188,8 +188,13 @@ def test_prefill_arguments(dev, dec_module):
     assert vst.ctx_info_get(ctx.handle).abs_next == 0
     with pytest.raises(RuntimeError):
         vst.dec_prefill(ctx.handle, qd, kd, vd, out, n=-1)
+    # past max_position: refused by the library (raw pointers bypass the binding's size check)
     with pytest.raises(RuntimeError):
-        vst.dec_prefill(ctx.handle, qd, kd, vd, out, n=dec_module.cfg.max_position + 1)
+        vst.dec_prefill(ctx.handle, qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), out.data_ptr(),
+                        n=dec_module.cfg.max_position + 1)
+    # more tokens than the tensors hold: refused by the binding before the call
+    with pytest.raises(ValueError):
+        vst.dec_prefill(ctx.handle, qd, kd, vd, out, n=5)
     assert vst.ctx_info_get(ctx.handle).abs_next == 0
     assert vst.ctx_check(ctx.handle) == vst.OK
     ctx.close()

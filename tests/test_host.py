@@ -110,3 +110,20 @@ def test_enc_plan_hand_cases():
     assert steps == [(50, 1)] and (n_kv, base) == (800, 750)
     steps, n_kv, base = vst.enc_plan(cfg, 1486, 0, 50)
     assert steps == [(50, 0)] and (n_kv, base) == (1536, 0)
+
+
+def test_binding_refuses_short_tensors():
+    """The binding checks every tensor against the rows the call reads or writes before it
+    reaches the library (whose pointers carry no size)."""
+    import torch
+    cfg = vst.config_default(vst.ENC)
+    rows, hd = 10, cfg.n_heads * cfg.head_dim
+    full = torch.empty(rows * hd, dtype=torch.bfloat16)
+    vst._need_io(cfg, rows, full, full, full, full)
+    short = torch.empty(rows * hd - 1, dtype=torch.bfloat16)
+    for i in range(4):
+        args = [full] * 4
+        args[i] = short
+        with pytest.raises(ValueError):
+            vst._need_io(cfg, rows, *args)
+    vst._need_io(None, rows, short, short, short, short)  # unknown ctx: nothing to check against
