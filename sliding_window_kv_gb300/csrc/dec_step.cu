@@ -190,6 +190,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
         tmem_relinquish();
     }
+    // What the prologue of a decoder step reads right after the wait -- the group's four query
+    // heads, the (cos, sin) row of pos and, if this CTA stores the step's key, its K and V
+    // rows -- is pulled into L2 now, so that those loads hit L2. (A prefill chunk's launch
+    // follows its own append, which the prefetches would only compete with.)
+    if (!c.appended) {
+        if (tid == 32) {
+            prefetch_l2(job.q + (long long)g * kG * kD, kG * kD * 2);
+        } else if (tid == 64) {
+            prefetch_l2(c.rope + pos * (kD / 2), kD * 4);
+        } else if (tid == 96 && has_new) {
+            prefetch_l2(job.k + (long long)g * kD, kD * 2);
+            prefetch_l2(job.v + (long long)g * kD, kD * 2);
+        }
+    }
     griddep_wait();
     if (tid == 0 && !c.early)
         issue_first();

@@ -234,6 +234,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(&s_tmem), kTmemCols);
         tmem_relinquish();
     }
+    // What the prologue reads right after the wait -- row r's query and (cos, sin) row and,
+    // if row r of the first key tile is new, its K and V -- is pulled into L2 now, one
+    // 128- or 256-byte prefetch per thread, so that those loads hit L2.
+    {
+        const long long i = t_begin * 128 + s.r - job.pos0;  // batch row at row r of the first tile
+        if (s.q == 0 && s.r < nrows)
+            prefetch_l2(job.q + ((long long)(row0 + s.r) * c.H + h) * kD, kD * 2);
+        else if (s.q == 1 && s.r < nrows)
+            prefetch_l2(c.rope + (p_first + s.r) * (kD / 2), kD * 4);
+        else if (s.q >= 2 && i >= 0 && i < c.n_rows)
+            prefetch_l2((s.q == 2 ? job.k : job.v) + (i * c.H + h) * kD, kD * 2);
+    }
     griddep_wait();
     if (s.tid == 0 && !c.early)
         issue_first_tile();

@@ -155,6 +155,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// Warm L2 with `bytes` (a multiple of 16) of global memory at `p` (16-byte aligned) through
+// the TMA unit. Nothing lands in the CTA and nothing waits for it. The prefetch observes no
+// value: a write by another kernel, before or after it, updates the L2 line like any other
+// (L2 is the device's point of coherence), so it may be issued before griddep_wait for data
+// the previous kernel may still write.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05 (TMEM, MMA)
 
 // Allocate ncols TMEM columns (power of two >= 32); the address is written to smem.

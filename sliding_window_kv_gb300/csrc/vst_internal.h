@@ -150,7 +150,10 @@ cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, 
 
 // Launch with programmatic stream serialization: the kernel may start while the previous
 // kernel in the stream is finishing; it runs griddep_wait() before touching anything that
-// kernel may produce or consume.
+// kernel may produce or consume. Every kernel of the library releases its dependents
+// (griddep_launch_dependents) only after its own griddep_wait has returned, so when a
+// launch starts, every kernel before its immediate predecessor has completed: what it
+// does before its wait overlaps that one predecessor and nothing earlier.
 template <class Kernel, class Params>
 cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Params& p)
 {

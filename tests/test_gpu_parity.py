@@ -100,7 +100,7 @@ def test_enc_config0_parity_and_bit_exact(dev, enc_module):
     assert torch.equal(out_c, out_n)
 
 
-@pytest.mark.parametrize("sched", ["ones_then_big", "ragged", "max_batch_edges"])
+@pytest.mark.parametrize("sched", ["ones_then_big", "ragged", "max_batch_edges", "empty_feeds"])
 def test_enc_chunking_not_observable(dev, enc_module, sched):
     T = 1700
     q, k, v = _enc_inputs(7, 3, T)
@@ -112,8 +112,12 @@ def test_enc_chunking_not_observable(dev, enc_module, sched):
         chunks = []
         while sum(chunks) < T:
             chunks.append(int(min(T - sum(chunks), rng.choice([1, 3, 49, 50, 127, 128, 129, 300, 511]))))
-    else:
+    elif sched == "max_batch_edges":
         chunks = [511, 512, 513, T - 1536]
+    else:  # feeds of zero rows between 50-frame feeds change nothing
+        chunks = []
+        while sum(chunks) < T:
+            chunks += [min(50, T - sum(chunks)), 0] + ([0] if len(chunks) % 7 == 0 else [])
     out, info = _feed(enc_module, q, k, v, chunks)
     assert info.abs_next == T
     assert torch.equal(out, ref), sched
