@@ -29,9 +29,11 @@
 //
 // Launch shape (split): for a batch of a single query tile, one CTA per (context, head,
 // group of `split` consecutive key tiles), with groups just large enough that every CTA
-// starts in the first wave. Each CTA writes each tile's (m_t, l_t, O_t) to scratch; the
-// last CTA of the (context, head) folds the tiles in ascending order, with the fold of
-// enc_common.cuh. The first tile's new rows are rotated and stored to the ring in the
+// starts in the first wave. The CTA of the last group (the merger) folds every tile of the
+// (context, head) in ascending order, with the fold of enc_common.cuh. The others write
+// each tile's (m_t, l_t, O_t) to scratch and count themselves in with one releasing
+// increment; the merger keeps its own last tile in shared memory and waits (bounded) for
+// the count, so its handoff costs one acquiring poll and no fence. The first tile's new rows are rotated and stored to the ring in the
 // prologue, so their global loads overlap those of the queries. The loop shape
 // (enc_attn.cu) gives the same bits: tiles are fixed by absolute position, folded in
 // ascending order, and every row's arithmetic comes from enc_common.cuh.
@@ -61,7 +63,7 @@ constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmS = 0;    // S tile: columns [0, 128)
 constexpr uint32_t kTmO = 128;  // O tile: columns [128, 192)
 
-constexpr int kMergeGroup = 8;  // split mode: tile partials loaded together by the last CTA
+constexpr int kMergeGroup = 8;  // tile partials loaded together by the merger
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64, false, true);
@@ -269,6 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t ph_k = 0, ph_v = 0, ph_m = 0;
     bool pend_k = s.tid == 0, pend_v = s.tid == 0;
+    // The CTA of the last key tiles (the merger) folds every tile of (job, head); the others
+    // publish their tile partials to scratch and count themselves in.
+    const long long others = (t_hi - t_lo) / c.split;
+    const bool merger = (long long)blockIdx.x == others;
     const uint32_t elect = s.warp == 0 ? elect_one_sync() : 0u;  // lane of warp 0 that issues MMAs
     int fail = 0, aborted = 0;
 
@@ -368,11 +374,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < kDq; ++j)
                 ot[j] = __uint_as_float(ov[j]);
         }
-        {
-            // tile partial of (row r, quarter q) -> scratch [h][tile][q][row][16]: a warp's
-            // 32 rows of one quarter are 2 KB contiguous; only rows of the batch are kept
-            const long long slot_t = (long long)h * c.split_tiles + (t - t_lo);
-            if (r < nrows) {
+        if (r < nrows) {
+            if (merger && t == t_hi) {
+                // the merger's own last tile stays in shared memory: O as [row][64] floats in
+                // the P buffer (the PV MMA that read it has completed), (m_t, l_t) per row in
+                // the row-max area (last read before the barrier after V landed)
+                float* lo_o = reinterpret_cast<float*>(s.sP) + r * kD + kDq * s.q;
+#pragma unroll
+                for (int d = 0; d < kDq; d += 4)
+                    *reinterpret_cast<float4*>(lo_o + d) = make_float4(ot[d], ot[d + 1], ot[d + 2], ot[d + 3]);
+                if (s.q == 0)
+                    reinterpret_cast<float2*>(s.red_m)[r] = make_float2(mt, lt);
+            } else {
+                // tile partial of (row r, quarter q) -> scratch [h][tile][q][row][16]: a warp's
+                // 32 rows of one quarter are 2 KB contiguous; only rows of the batch are kept
+                const long long slot_t = (long long)h * c.split_tiles + (t - t_lo);
                 float* po = job.part_o + ((slot_t * 4 + s.q) * 128 + r) * kDq;
 #pragma unroll
                 for (int d = 0; d < kDq; d += 4)
@@ -390,34 +406,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     griddep_launch_dependents();
-    if (aborted) {
-        if (s.tid == 0) {
-            // A bounded wait gave up: record it, let copies still in flight land, then release
-            // TMEM and leave.
-            atomicExch(job.err, kErrTimeout);
-            if (pend_k)
-                mbar_wait(s.bar_k, ph_k);
-            if (pend_v)
-                mbar_wait(s.bar_v, ph_v);
-        }
+    if (aborted && s.tid == 0) {
+        // A bounded wait gave up: record it and let copies still in flight land. The CTA
+        // still takes part in the handoff below, so that the merger does not wait out its
+        // own limit, then releases TMEM and leaves.
+        atomicExch(job.err, kErrTimeout);
+        if (pend_k)
+            mbar_wait(s.bar_k, ph_k);
+        if (pend_v)
+            mbar_wait(s.bar_v, ph_v);
+    }
+    if (!merger) {
+        // The CTA barrier orders every thread's partials before thread 0's releasing
+        // increment (cumulative), which the merger acquires.
+        __syncthreads();
+        if (s.tid == 0)
+            red_add_release_gpu(job.counters + h, 1u);
     } else {
-        // the last CTA of (job, head) folds all tiles in ascending order. The
-        // CTA barrier orders every thread's partial before thread 0's counter update
-        // (acquire-release, cumulative); the barrier after it passes what the last CTA's
-        // thread 0 acquired on to its readers.
+        if (t_end > t_begin)
+            __threadfence();  // this CTA's own earlier tile partials, read back from scratch below
         __syncthreads();
         if (s.tid == 0) {
-            const unsigned prev = atom_add_acq_rel_gpu(job.counters + h, 1u);
-            s_last = prev == (unsigned)((t_hi - t_lo) / c.split);  // CTAs of this (job, head) - 1
+            // Wait until the other CTAs of (job, head) have counted themselves in, then re-arm
+            // the counter for the next launch; the barrier after it passes what thread 0
+            // acquired on to the readers.
+            const bool all_in = wait_count(job.counters + h, (unsigned)others);
+            job.counters[h] = 0u;
+            if (!all_in)
+                atomicExch(job.err, kErrTimeout);
+            s_last = all_in && !aborted;
         }
         __syncthreads();
         if (s_last) {
             // All threads of the CTA share the merge: item (row, g) folds dims [8g, 8g+8) of
             // a row over the tiles in ascending order, in groups of up to kMergeGroup tiles
-            // whose loads are all issued before their folds.
+            // whose loads are all issued before their folds. The last tile is this CTA's own,
+            // from shared memory.
             const int nt = (int)(t_hi - t_lo + 1);
             const float* pml0 = job.part_ml + (long long)h * c.split_tiles * 128 * 2;
             const float* po0 = job.part_o + (long long)h * c.split_tiles * 128 * kD;
+            const float* own_o = reinterpret_cast<const float*>(s.sP);
+            const float2* own_ml = reinterpret_cast<const float2*>(s.red_m);
             for (int it = s.tid; it < nrows * 8; it += kThreads) {
                 const int row = it >> 3, g = it & 7;  // dims [8g, 8g+8): quarter g / 2, half g % 2
                 float m = -INFINITY, l = 0.f, om[8];
@@ -432,8 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < kMergeGroup; ++u) {
                         ml[u] = make_float2(-INFINITY, 0.f);
                         xa[u] = xb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (u < ng) {
-                            const long long tile = g0 + u;
+                        const long long tile = g0 + u;
+                        if (u < ng && tile == nt - 1) {
+                            ml[u] = own_ml[row];
+                            const float4* src = reinterpret_cast<const float4*>(own_o + row * kD + 8 * g);
+                            xa[u] = src[0];
+                            xb[u] = src[1];
+                        } else if (u < ng) {
                             ml[u] = __ldcg(reinterpret_cast<const float2*>(pml0 + (tile * 128 + row) * 2));
                             const float* src = po0 + ((tile * 4 + (g >> 1)) * 128 + row) * kDq + 8 * (g & 1);
                             xa[u] = __ldcg(reinterpret_cast<const float4*>(src));
@@ -448,8 +482,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 enc::store_out<8>(job.out + ((long long)(row0 + row) * c.H + h) * kD, om, l, 8 * g);
             }
-            if (s.tid == 0)
-                job.counters[h] = 0u;
         }
     }
     tc_fence_before();

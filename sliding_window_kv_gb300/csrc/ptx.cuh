@@ -107,6 +107,35 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v
     return old;
 }
 
+// Add v at GPU scope with release semantics, without waiting for a result: the writes this
+// thread has made or observed (its CTA's, once ordered before it by a CTA barrier) are
+// visible to any thread that acquires the new count.
+__device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *p >= target, acquiring what the releases that counted it published; false
+// after kWaitLimitNs.
+__device__ __forceinline__ bool wait_count(const unsigned* p, unsigned target)
+{
+    if (ld_acquire_gpu(p) >= target)
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(p) < target) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------- TMA
 
 // Order this thread's generic-proxy shared-memory writes before later async-proxy reads
