@@ -410,6 +410,47 @@ def test_dec_batched_equals_single(dev, dec_module):
         c.close()
 
 
+def test_dec_64_streams_uniform_fill_sampled(dev, dec_module):
+    """The 64-stream decoder workload in the launch configuration the benchmark times: one
+    layer of 64 contexts whose caches are filled to lengths drawn uniformly from [1, 8192]
+    (seed 4, the same recipe: 81 to 8132 keys), then 4 batched steps. The shortest, the
+    median and the longest stream are compared with the oracle, on each row's own window,
+    at the first and the last step."""
+    seed, S, steps, W = 4, 64, 4, 8192
+    fills = synth.uniform_int(synth.tensor_key(seed, 99), S, 1, W)
+    ctxs = [vst.Ctx(dec_module) for _ in range(S)]
+    qs, ks, vs = [], [], []
+    for s, f in enumerate(fills):
+        k = synth.frames(synth.tensor_key(seed, s, 0, 1), 0, f + steps, 8, 128, dev)
+        v = synth.frames(synth.tensor_key(seed, s, 0, 2), 0, f + steps, 8, 128, dev)
+        vst.dec_append(ctxs[s].handle, k[:f], v[:f])
+        qs.append(synth.frames(synth.tensor_key(seed, s, 0, 0), f, steps, 32, 128, dev))
+        ks.append(k[f:])
+        vs.append(v[f:])
+    Q, K, V = (torch.stack(x, 1).contiguous() for x in (qs, ks, vs))  # [steps][S][...]
+    O = torch.empty_like(Q)
+    for t in range(steps):
+        vst.dec_step([c.handle for c in ctxs], Q[t], K[t], V[t], O[t])
+    torch.cuda.synchronize()
+    for c in ctxs:
+        assert vst.ctx_check(c.handle) == vst.OK
+        c.close()
+    got = O.float().cpu().double().numpy()
+    order = sorted(range(S), key=lambda s: fills[s])
+    for s in (order[0], order[S // 2], order[-1]):
+        f = fills[s]
+        qb = synth.bits(synth.frames(synth.tensor_key(seed, s, 0, 0), f, steps, 32, 128, "cpu"))
+        for t in (0, steps - 1):
+            i = f + t
+            j0 = max(0, i - W + 1)
+            kb = synth.bits(synth.frames(synth.tensor_key(seed, s, 0, 1), j0, i - j0 + 1, 8, 128, "cpu"))
+            vb = synth.bits(synth.frames(synth.tensor_key(seed, s, 0, 2), j0, i - j0 + 1, 8, 128, "cpu"))
+            want = oracle.attention_row(qb[t], kb, vb, i, W)
+            d = np.abs(got[t, s] - want)
+            assert np.isfinite(got[t, s]).all(), (s, t)
+            assert d.max() <= MAX_TOL and d.mean() <= MEAN_TOL, (s, f, t, d.max(), d.mean())
+
+
 def test_dec_batch_over_64_streams(dev, dec_module):
     """70 streams in one vst_dec_step call: the library launches them as 64 + 6 jobs. Every
     stream's rows equal the single-stream step's, fills from empty to past one tile."""
