@@ -91,6 +91,31 @@ def test_offline_lookahead_parity(dev, enc_module, left, right):
         assert d.max() <= MAX_TOL and d.mean() <= MEAN_TOL, (b, d.max(), d.mean())
 
 
+def test_offline_full_clips_sampled(dev, enc_module):
+    """The offline workload the benchmark times, one layer: 4 clips x 4416 frames (seed 8,
+    the same recipe) with left 750 and a right lookahead of 4. Rows at the clip ends, at
+    query-tile edges and in the middle are compared with the oracle, each on its own window
+    [i - 749, i + 3]."""
+    seed, B, T, left, right = 8, 4, 4416, 750, 4
+    mk = lambda n: torch.stack([synth.frames(synth.tensor_key(seed, b, 0, n), 0, T, H, D, dev) for b in range(B)])
+    q, k, v = mk(0), mk(1), mk(2)
+    plan = vst.Offline(enc_module, B, T)
+    out = torch.empty_like(q)
+    plan.run(q, k, v, out, left, right)
+    torch.cuda.synchronize()
+    assert plan.check() == vst.OK
+    plan.close()
+    got = out.float().cpu().double().numpy()
+    for b in (0, 3):
+        for i in (0, 1, 127, 128, 749, 750, 2000, 4351, 4352, 4412, 4415):
+            a0, a1 = max(0, i - left + 1), min(T, i + right)  # keys of row i: [i - left + 1, i + right - 1]
+            win = [synth.bits(synth.frames(synth.tensor_key(seed, b, 0, n), a0, a1 - a0, H, D, "cpu")) for n in range(3)]
+            want = oracle.attention_lr(*win, left, right, pos0=a0, rows=(i - a0, i - a0 + 1))[0]
+            d = np.abs(got[b, i] - want)
+            assert np.isfinite(got[b, i]).all(), (b, i)
+            assert d.max() <= MAX_TOL and d.mean() <= MEAN_TOL, (b, i, d.max(), d.mean())
+
+
 def test_offline_layer_pattern(dev, enc_module):
     """The per-layer window pattern of the pages' Moonshine variant, (16, 4) (16, 4) (16, 0)
     (16, 0) (16, 4) (16, 4), one call per layer on one plan."""
