@@ -432,17 +432,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 template <int J>
 static cudaError_t launch_dec_j(const KParams<DecCommon, DecJob, J>& p, int total_work, cudaStream_t s)
 {
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
+    static std::atomic<unsigned long long> configured{0};
     const uint32_t smem = Layout::kSmemBytes;
-    if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(dec_step_kernel<J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = 1;
-    }
+    const cudaError_t e = smem_limit_once(configured, dec_step_kernel<J>, (int)smem);
+    if (e != cudaSuccess)
+        return e;
     const dim3 grid((unsigned)total_work, (unsigned)p.c.Hk);
     return launch_pdl(dec_step_kernel<J>, grid, dim3(kThreads), smem, s, p);
 }

@@ -10,8 +10,9 @@
 // ("RECOMMENDED implementation").
 //
 // With a right lookahead (offline clips, "Moonshine streaming forward map", Encoder table,
-// per-layer sliding-window mask row), frame i also sees [i+1, i+right] of the batch; right
-// is 0 on the streaming path.
+// per-layer sliding-window mask row), frame i also sees [i+1, i+right] of the batch, right
+// being EncAttnCommon::right (the host passes the mask's R - 1: "0 < j - i < R"); right is 0
+// on the streaming path.
 //
 // Keys are visited in tiles of 128 ABSOLUTE positions [128t, 128t+128), loaded whole by
 // TMA from ring slots 128t - abs_base (rows outside the ring read as zero): the batch's own
@@ -400,16 +401,10 @@ template <int J>
 static cudaError_t launch_enc_attn_j(const KParams<EncAttnCommon, EncAttnJob, J>& p, int n_jobs, int grid_x,
                                      cudaStream_t s)
 {
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(enc_attn_kernel<J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = 1;
-    }
+    static std::atomic<unsigned long long> configured{0};
+    const cudaError_t e = smem_limit_once(configured, enc_attn_kernel<J>, (int)kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
     const dim3 grid((unsigned)grid_x, (unsigned)p.c.H, (unsigned)n_jobs);
     return launch_pdl(enc_attn_kernel<J>, grid, dim3(kThreads), kSmemBytes, s, p);
 }

@@ -496,16 +496,10 @@ template <int J>
 static cudaError_t launch_enc_attn_split_j(const KParams<EncAttnCommon, EncAttnJob, J>& p, int n_jobs, int grid_x,
                                      cudaStream_t s)
 {
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(enc_attn_split_kernel<J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = 1;
-    }
+    static std::atomic<unsigned long long> configured{0};
+    const cudaError_t e = smem_limit_once(configured, enc_attn_split_kernel<J>, (int)kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
     const dim3 grid((unsigned)grid_x, (unsigned)p.c.H, (unsigned)n_jobs);
     return launch_pdl(enc_attn_split_kernel<J>, grid, dim3(kThreads), kSmemBytes, s, p);
 }

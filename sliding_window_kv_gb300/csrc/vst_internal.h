@@ -13,6 +13,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/vst.h"
@@ -77,7 +78,7 @@ struct EncAttnJob {
     const CUtensorMap* tmap_v;
     float* part_ml;          // split mode scratch: [H][split_tiles][128][2] (m_t, l_t)
     float* part_o;           // split mode scratch: [H][split_tiles][4 quarters][128][D / 4]
-    unsigned* counters;      // split mode: [H] tiles finished per head
+    unsigned* counters;      // split mode: [H] CTAs of each head that have published their partials
     int* err;
     long long pos0;          // absolute position of row 0
     long long abs_base;      // absolute position held by ring slot 0
@@ -147,6 +148,25 @@ cudaError_t launch_enc_attn_split(const EncAttnCommon& c, const EncAttnJob* jobs
                             cudaStream_t s);
 cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, int total_work,
                             cudaStream_t s);
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per
+// device: `done` (one per kernel instantiation, bit d for device d < 64) records where it is
+// set. Safe from several host threads: a first call racing another sets the same attribute
+// twice, which the runtime allows.
+template <class Kernel>
+cudaError_t smem_limit_once(std::atomic<unsigned long long>& done, Kernel kernel, int bytes)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && ((done.load(std::memory_order_acquire) >> dev) & 1ull))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev < 64)
+        done.fetch_or(1ull << dev, std::memory_order_release);
+    return e;
+}
 
 // Launch with programmatic stream serialization: the kernel may start while the previous
 // kernel in the stream is finishing; it runs griddep_wait() before touching anything that
