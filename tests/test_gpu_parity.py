@@ -123,6 +123,22 @@ def test_enc_chunking_not_observable(dev, enc_module, sched):
     assert torch.equal(out, ref), sched
 
 
+@pytest.mark.parametrize("chunk_ms", [500, 1000, 2000, 20000])
+def test_enc_chunk_sizes_of_the_pages(dev, enc_module, chunk_ms):
+    """The streaming chunk sizes the family doc validates ("Voxtral Realtime", Capability
+    Validation, Streaming row, item (3): 500, 1000, 2000 and 20000 ms) are feeds of 25, 50,
+    100 and 1000 encoder frames at 50 frames per second. Over 2600 frames (compactions at
+    every size) each gives the bits of one single feed."""
+    T = 2600
+    q, k, v = _enc_inputs(9, 0, T)
+    ref, _ = _feed(enc_module, q, k, v, [T])
+    n = chunk_ms // 20
+    chunks = [min(n, T - a) for a in range(0, T, n)]
+    out, info = _feed(enc_module, q, k, v, chunks)
+    assert info.abs_next == T and info.n_compactions >= 1
+    assert torch.equal(out, ref), chunk_ms
+
+
 def test_enc_long_stream_parity_sampled(dev, enc_module):
     """5000 frames in 50-frame feeds (lazy compactions): sampled rows against the oracle
     computed from each row's own window."""
