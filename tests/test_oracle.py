@@ -370,12 +370,26 @@ def check_lr_causal_case_is_windowed_attention():
         assert np.array_equal(oracle.attention_lr(qb, kb, vb, L, 0), oracle.attention(qb, kb, vb, window=L))
 
 
+def check_lr_window_locality():
+    """A row computed from its own span alone, [i - L + 1, i + R - 1] cut out of the clip and
+    placed at its absolute positions, equals the whole-clip row bit for bit (the offline
+    parity tests sample rows this way)."""
+    T, H, D = 200, 2, 16
+    qb, kb, vb = (_randn_bits((T, H, D), s) for s in (150, 151, 152))
+    for L, R in ((16, 4), (150, 4), (1, 1), (40, 0)):
+        whole = oracle.attention_lr(qb, kb, vb, L, R)
+        for i in (0, 1, 15, 16, 100, 149, 150, 196, 199):
+            a0, a1 = max(0, i - L + 1), min(T, i + max(R, 1))
+            row = oracle.attention_lr(qb[a0:a1], kb[a0:a1], vb[a0:a1], L, R, pos0=a0, rows=(i - a0, i - a0 + 1))[0]
+            assert np.array_equal(row, whole[i]), (L, R, i)
+
+
 ATTENTION_CHECKS = [check_bruteforce_tiny, check_long_window_is_causal_sdpa,
                     check_window_one_returns_v, check_zero_query_gives_window_mean,
                     check_decoder_window_8192, check_gqa_groups, check_position_shift_invariance,
                     check_window_locality, check_chunking_not_observable, check_lr_bruteforce_tiny,
                     check_lr_bidirectional_is_sdpa, check_lr_zero_query_span_mean,
-                    check_lr_causal_case_is_windowed_attention]
+                    check_lr_causal_case_is_windowed_attention, check_lr_window_locality]
 
 
 @pytest.mark.parametrize("check", ATTENTION_CHECKS)
