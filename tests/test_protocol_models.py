@@ -1,0 +1,281 @@
+"""Models of the kernels' cross-thread protocols, run on the CPU over random interleavings.
+
+The loop shape of the chunk attention (enc_attn.cu) coordinates one control warp, eight
+softmax warps, the TMA unit and the tensor pipe through mbarriers and pairwise named
+barriers. The split shape (enc_attn_split.cu) hands tile partials from its CTAs to one
+merging CTA through a counter. Each model replays its protocol's waits, arrivals and buffer
+uses in the order the kernel issues them, and a seeded scheduler picks which agent moves
+next; copies and MMAs complete whenever the scheduler lets them. A run fails on a deadlock
+(no agent can move) or when a read finds a tile other than the one the protocol promises.
+Planted protocol mistakes must fail, so the models are known to catch what they look for.
+"""
+import random
+
+import pytest
+
+
+class Hazard(Exception):
+    pass
+
+
+class Barrier:
+    """An mbarrier: `count` arrivals complete a phase; waiters wait on a phase parity."""
+
+    def __init__(self, count):
+        self.count, self.pending, self.completed = count, count, 0
+
+    def arrive(self):
+        self.pending -= 1
+        if self.pending < 0:
+            raise Hazard("barrier over-arrived")
+        if self.pending == 0:
+            self.completed += 1
+            self.pending = self.count
+
+    def passed(self, parity):
+        return (self.completed & 1) != parity
+
+
+def _expect(cond, msg):
+    if not cond:
+        raise Hazard(msg)
+
+
+# ---------------------------------------------------------------- loop shape (enc_attn.cu)
+
+def loop_shape_run(n, seed, mistake=None, n_warps=8):
+    """One CTA over n key tiles. Control warp: K double-buffered two tiles ahead, one V
+    buffer, S of tile t+1 into the other TMEM buffer once O of tile t-1 there has been read
+    by every softmax warp, PV of tile t in two key halves as each half of P lands, then V of
+    tile t+1 once O of tile t is done. Softmax warps (two per query row, half h owning score
+    columns [64h, 64h+64)): row max of S_t, exchange with the partner warp, fold O_{t-1},
+    exps of S_t into P. PV's first half writes O into the first 64 columns of S_t's buffer,
+    which only half 0 reads."""
+    rng = random.Random(seed)
+    bars = {k: Barrier(1) for k in ("K0", "K1", "V", "S0", "S1", "O0", "O1")}
+    for k in ("F0", "F1", "Q"):
+        bars[k] = Barrier(n_warps)
+    bars["P0"], bars["P1"] = Barrier(n_warps // 2), Barrier(n_warps // 2)
+    mem = {"K0": None, "K1": None, "V": None, "O0": None, "O1": None,
+           "S0h0": None, "S0h1": None, "S1h0": None, "S1h1": None, "P": [None] * n_warps, "Q": [False] * n_warps}
+    copies, mmas = [], []  # copies land in any order; the tensor pipe runs its queue in order
+
+    def control():
+        ph = dict.fromkeys(bars, 0)
+
+        def wait(k):
+            ph[k] ^= 1
+            return ("wait", k, ph[k] ^ 1)
+
+        def fetch_k(t):
+            copies.append(("K%d" % (t & 1), t))
+
+        def fetch_v(t):
+            copies.append(("V", t))
+
+        fetch_k(0)
+        if n > 1:
+            fetch_k(1)
+        fetch_v(0)
+        yield wait("Q")
+        yield wait("K0")
+        mmas.extend([("S", 0), ("commit", "S0")])
+        for t in range(n):
+            b, nb = t & 1, (t & 1) ^ 1
+            if t + 2 <= n - 1:
+                if mistake != "k_before_s_done":
+                    yield wait("S%d" % b)
+                fetch_k(t + 2)
+            if t < n - 1:
+                yield wait("K%d" % nb)
+                if t > 0 and mistake != "s_before_o_read":
+                    yield wait("F%d" % nb)
+                mmas.extend([("S", t + 1), ("commit", "S%d" % nb)])
+            yield wait("V")
+            yield wait("P0")
+            mmas.append(("PV0", t))
+            yield wait("P1")
+            mmas.extend([("PV1", t), ("commit", "O%d" % b)])
+            if t < n - 1:
+                if mistake != "v_before_o_done":
+                    yield wait("O%d" % b)
+                fetch_v(t + 1)
+
+    def softmax(w):
+        ph = dict.fromkeys(bars, 0)
+        half, pair = w // (n_warps // 2), w % (n_warps // 2)
+
+        def wait(k):
+            ph[k] ^= 1
+            return ("wait", k, ph[k] ^ 1)
+
+        yield ("do", lambda: mem["Q"].__setitem__(w, True))  # queries rotated in place
+        yield ("arrive", "Q")
+        for t in range(n):
+            b, nb = t & 1, (t & 1) ^ 1
+            s = "S%dh%d" % (b, half)
+            yield wait("S%d" % b)
+            yield ("do", lambda t=t, s=s: _expect(mem[s] == t, "row max of warp %d reads %s = %s, not tile %d" % (w, s, mem[s], t)))
+            yield ("pair", pair, t)
+            if t > 0:
+                yield wait("O%d" % nb)
+                yield ("do", lambda t=t, nb=nb: _expect(mem["O%d" % nb] == t - 1, "fold of warp %d reads O%d = %s, not tile %d" % (w, nb, mem["O%d" % nb], t - 1)))
+                yield ("arrive", "F%d" % nb)
+            yield ("do", lambda t=t, s=s: _expect(mem[s] == t, "exps of warp %d read %s = %s, not tile %d" % (w, s, mem[s], t)))
+            yield ("do", lambda t=t: mem["P"].__setitem__(w, t))
+            yield ("arrive", "P%d" % half)
+        yield ("pair", pair, n)
+        last = (n - 1) & 1
+        yield wait("O%d" % last)
+        yield ("do", lambda: _expect(mem["O%d" % last] == n - 1, "last fold of warp %d reads O = %s" % (w, mem["O%d" % last])))
+
+    def run_mma(op):
+        if op[0] == "commit":
+            bars[op[1]].arrive()
+            return
+        t = op[1]
+        b = t & 1
+        if op[0] == "S":
+            _expect(mem["K%d" % b] == t, "S of tile %d reads K%d = %s" % (t, b, mem["K%d" % b]))
+            _expect(all(mem["Q"]), "S issued before every query row was rotated")
+            mem["S%dh0" % b] = mem["S%dh1" % b] = t
+            mem["O%d" % b] = None
+        elif op[0] == "PV0":
+            _expect(mem["V"] == t, "PV of tile %d reads V = %s" % (t, mem["V"]))
+            _expect(all(p == t for p in mem["P"][:n_warps // 2]), "PV0 of tile %d reads P = %s" % (t, mem["P"]))
+            mem["S%dh0" % b] = None  # O overwrites the score columns of half 0
+            mem["O%d" % b] = ("half", t)
+        else:
+            _expect(mem["V"] == t, "PV1 of tile %d reads V = %s" % (t, mem["V"]))
+            _expect(all(p == t for p in mem["P"][n_warps // 2:]), "PV1 of tile %d reads P = %s" % (t, mem["P"]))
+            _expect(mem["O%d" % b] == ("half", t), "PV halves of tile %d out of order" % t)
+            mem["O%d" % b] = t
+
+    agents = {"control": control()}
+    agents.update(("warp%d" % w, softmax(w)) for w in range(n_warps))
+    _schedule(agents, bars, rng, copies, mmas, mem, run_mma)
+
+
+def _schedule(agents, bars, rng, copies, mmas, mem, run_mma):
+    cur = {k: next(g, None) for k, g in agents.items()}
+    for _ in range(500000):
+        ready = []
+        for k, ins in cur.items():
+            if ins is None:
+                continue
+            if ins[0] == "wait":
+                if bars[ins[1]].passed(ins[2]):
+                    ready.append(k)
+            elif ins[0] == "pair":
+                if sum(1 for v in cur.values() if v is not None and v[:3] == ins[:3]) == 2:
+                    ready.append(k)
+            else:
+                ready.append(k)
+        choices = ready + (["copy"] if copies else []) + (["mma"] if mmas else [])
+        if not choices:
+            if all(v is None for v in cur.values()):
+                return
+            raise Hazard("deadlock: " + repr({k: v for k, v in cur.items() if v is not None}))
+        c = rng.choice(choices)
+        if c == "copy":
+            buf, t = copies.pop(rng.randrange(len(copies)))
+            mem[buf] = t
+            bars[buf].arrive()
+        elif c == "mma":
+            run_mma(mmas.pop(0))
+        elif cur[c][0] == "pair":
+            for k in [k for k, v in cur.items() if v is not None and v[:3] == cur[c][:3]]:
+                cur[k] = next(agents[k], None)
+        else:
+            ins = cur[c]
+            if ins[0] == "arrive":
+                bars[ins[1]].arrive()
+            elif ins[0] == "do":
+                ins[1]()
+            cur[c] = next(agents[c], None)
+    raise Hazard("no end in sight")
+
+
+@pytest.mark.parametrize("n_tiles", [1, 2, 3, 4, 5, 7, 8])
+def test_loop_shape_protocol(n_tiles):
+    for seed in range(60):
+        loop_shape_run(n_tiles, 1000 * n_tiles + seed)
+
+
+@pytest.mark.parametrize("mistake", ["k_before_s_done", "s_before_o_read", "v_before_o_done"])
+def test_loop_shape_model_catches_planted_mistakes(mistake):
+    caught = 0
+    for seed in range(200):
+        try:
+            loop_shape_run(5, seed, mistake)
+        except Hazard:
+            caught += 1
+    assert caught > 0, mistake
+
+
+# ---------------------------------------------------------------- split shape handoff (enc_attn_split.cu)
+
+def split_handoff_run(n_others, seed, launches=2, mistake=None):
+    """Successive launches over one (context, head). Each non-merging CTA stores its tile
+    partial (the stores drain to L2 in any order), passes the CTA barrier and counts itself
+    in with a releasing add, which takes effect only after the CTA's stores have drained. The
+    merger polls the count with acquiring loads until it reaches n_others, reads every
+    partial, and re-arms the count to zero before the launch ends. The next launch starts
+    only after every CTA of this one has finished."""
+    rng = random.Random(seed)
+    mem = {"count": 0}  # the counter lives in the context's memory across launches
+    partial = {}        # scratch: non-merging CTA -> the launch whose partial it holds
+    for launch in range(launches):
+        pending = []    # (CTA, launch) partial stores not yet drained to L2
+
+        def other(i):
+            pending.append((i, launch))
+            yield "store"
+            if mistake != "count_before_store_drains":
+                while any(p[0] == i for p in pending):
+                    yield "release waits for the stores"
+            mem["count"] += 1
+            yield "counted in"
+
+        def merger():
+            while mem["count"] < n_others:
+                yield "poll"
+            for i in range(n_others):
+                _expect(partial.get(i) == launch,
+                        "merger of launch %d reads the partial of CTA %d from launch %s" % (launch, i, partial.get(i)))
+            if mistake != "no_rearm":
+                mem["count"] = 0
+            yield "merged"
+
+        agents = {i: other(i) for i in range(n_others)}
+        agents["merger"] = merger()
+        cur = {k: next(g, None) for k, g in agents.items()}
+        for _ in range(100000):
+            live = [k for k, v in cur.items() if v is not None]
+            if not live and not pending:
+                break
+            c = rng.choice(live + (["drain"] if pending else []))
+            if c == "drain":
+                i, l = pending.pop(rng.randrange(len(pending)))
+                partial[i] = l
+            else:
+                cur[c] = next(agents[c], None)
+        else:
+            raise Hazard("no end in sight")
+
+
+@pytest.mark.parametrize("n_others", [0, 1, 6])
+def test_split_handoff_protocol(n_others):
+    for seed in range(200):
+        split_handoff_run(n_others, seed)
+
+
+@pytest.mark.parametrize("mistake", ["count_before_store_drains", "no_rearm"])
+def test_split_handoff_model_catches_planted_mistakes(mistake):
+    caught = 0
+    for seed in range(200):
+        try:
+            split_handoff_run(6, seed, launches=3, mistake=mistake)
+        except Hazard:
+            caught += 1
+    assert caught > 0, mistake
