@@ -2,7 +2,8 @@
 
 The loop shape of the chunk attention (enc_attn.cu) coordinates one control warp, eight
 softmax warps, the TMA unit and the tensor pipe through mbarriers and pairwise named
-barriers. The split shape (enc_attn_split.cu) hands tile partials from its CTAs to one
+barriers; the decoder (dec_step.cu) streams K and V through one and two buffers between
+CTA barriers. The split shape (enc_attn_split.cu) hands tile partials from its CTAs to one
 merging CTA through a counter. Each model replays its protocol's waits, arrivals and buffer
 uses in the order the kernel issues them, and a seeded scheduler picks which agent moves
 next; copies and MMAs complete whenever the scheduler lets them. A run fails on a deadlock
@@ -116,7 +117,7 @@ def loop_shape_run(n, seed, mistake=None, n_warps=8):
             s = "S%dh%d" % (b, half)
             yield wait("S%d" % b)
             yield ("do", lambda t=t, s=s: _expect(mem[s] == t, "row max of warp %d reads %s = %s, not tile %d" % (w, s, mem[s], t)))
-            yield ("pair", pair, t)
+            yield ("group", pair, t, 2)
             if t > 0:
                 yield wait("O%d" % nb)
                 yield ("do", lambda t=t, nb=nb: _expect(mem["O%d" % nb] == t - 1, "fold of warp %d reads O%d = %s, not tile %d" % (w, nb, mem["O%d" % nb], t - 1)))
@@ -124,7 +125,7 @@ def loop_shape_run(n, seed, mistake=None, n_warps=8):
             yield ("do", lambda t=t, s=s: _expect(mem[s] == t, "exps of warp %d read %s = %s, not tile %d" % (w, s, mem[s], t)))
             yield ("do", lambda t=t: mem["P"].__setitem__(w, t))
             yield ("arrive", "P%d" % half)
-        yield ("pair", pair, n)
+        yield ("group", pair, n, 2)
         last = (n - 1) & 1
         yield wait("O%d" % last)
         yield ("do", lambda: _expect(mem["O%d" % last] == n - 1, "last fold of warp %d reads O = %s" % (w, mem["O%d" % last])))
@@ -166,8 +167,8 @@ def _schedule(agents, bars, rng, copies, mmas, mem, run_mma):
             if ins[0] == "wait":
                 if bars[ins[1]].passed(ins[2]):
                     ready.append(k)
-            elif ins[0] == "pair":
-                if sum(1 for v in cur.values() if v is not None and v[:3] == ins[:3]) == 2:
+            elif ins[0] == "group":  # ("group", id, tag, size): a named barrier of `size` agents
+                if sum(1 for v in cur.values() if v is not None and v[:3] == ins[:3]) == ins[3]:
                     ready.append(k)
             else:
                 ready.append(k)
@@ -183,7 +184,7 @@ def _schedule(agents, bars, rng, copies, mmas, mem, run_mma):
             bars[buf].arrive()
         elif c == "mma":
             run_mma(mmas.pop(0))
-        elif cur[c][0] == "pair":
+        elif cur[c][0] == "group":
             for k in [k for k, v in cur.items() if v is not None and v[:3] == cur[c][:3]]:
                 cur[k] = next(agents[k], None)
         else:
@@ -208,6 +209,87 @@ def test_loop_shape_model_catches_planted_mistakes(mistake):
     for seed in range(200):
         try:
             loop_shape_run(5, seed, mistake)
+        except Hazard:
+            caught += 1
+    assert caught > 0, mistake
+
+
+# ---------------------------------------------------------------- decoder split (dec_step.cu)
+
+def decoder_run(n, seed, mistake=None, n_agents=4):
+    """One CTA of a decoder split over n key tiles. Thread 0 requests the copies and warp 0
+    issues the MMAs; every thread takes part in the softmax and the fold. One K buffer (K of
+    tile i+1 requested once S of tile i is done), two V buffers (V of tile i+2 once O of tile
+    i is done), S in two TMEM buffers, O in one, P in shared memory; the CTA barriers are
+    the kernel's __syncthreads."""
+    rng = random.Random(seed)
+    bars = {k: Barrier(1) for k in ("K", "V0", "V1", "S0", "S1", "O")}
+    mem = {"K": None, "V0": None, "V1": None, "S0": None, "S1": None, "O": None, "P": [None] * n_agents,
+           "Q": [False] * n_agents}
+    copies, mmas = [], []
+
+    def thread(a):
+        issuer = a == 0
+        if issuer:
+            copies.append(("K", 0))
+            copies.append(("V0", 0))
+            if n > 1:
+                copies.append(("V1", 1))
+        yield ("do", lambda: mem["Q"].__setitem__(a, True))
+        yield ("group", "cta", "prologue", n_agents)
+        for i in range(n):
+            b = i & 1
+            if issuer:
+                yield ("wait", "K", i & 1)
+                mmas.extend([("S", i), ("commit", "S%d" % b)])
+                if mistake == "k_before_s_done" and i + 1 < n:
+                    copies.append(("K", i + 1))
+            yield ("group", "cta", ("s", i), n_agents)
+            yield ("wait", "S%d" % b, (i >> 1) & 1)
+            if issuer and i + 1 < n and mistake != "k_before_s_done":
+                copies.append(("K", i + 1))
+            yield ("do", lambda i=i, b=b: _expect(mem["S%d" % b] == i, "softmax of thread %d reads S%d = %s, not tile %d" % (a, b, mem["S%d" % b], i)))
+            yield ("do", lambda i=i: mem["P"].__setitem__(a, i))
+            yield ("wait", "V%d" % b, (i >> 1) & 1)
+            yield ("group", "cta", ("o", i), n_agents)
+            if issuer:
+                mmas.extend([("O", i), ("commit", "O")])
+                if mistake == "v_before_o_done" and i + 2 < n:
+                    copies.append(("V%d" % b, i + 2))
+            yield ("wait", "O", i & 1)
+            if issuer and i + 2 < n and mistake != "v_before_o_done":
+                copies.append(("V%d" % b, i + 2))
+            yield ("do", lambda i=i: _expect(mem["O"] == i, "fold of thread %d reads O = %s, not tile %d" % (a, mem["O"], i)))
+
+    def run_mma(op):
+        if op[0] == "commit":
+            bars[op[1]].arrive()
+            return
+        i = op[1]
+        if op[0] == "S":
+            _expect(mem["K"] == i, "S of tile %d reads K = %s" % (i, mem["K"]))
+            _expect(all(mem["Q"]), "S issued before the query heads were rotated")
+            mem["S%d" % (i & 1)] = i
+        else:
+            _expect(mem["V%d" % (i & 1)] == i, "O of tile %d reads V%d = %s" % (i, i & 1, mem["V%d" % (i & 1)]))
+            _expect(all(p == i for p in mem["P"]), "O of tile %d reads P = %s" % (i, mem["P"]))
+            mem["O"] = i
+
+    _schedule({"thread%d" % a: thread(a) for a in range(n_agents)}, bars, rng, copies, mmas, mem, run_mma)
+
+
+@pytest.mark.parametrize("n_tiles", [1, 2, 3, 4])
+def test_decoder_protocol(n_tiles):
+    for seed in range(150):
+        decoder_run(n_tiles, 100 * n_tiles + seed)
+
+
+@pytest.mark.parametrize("mistake", ["k_before_s_done", "v_before_o_done"])
+def test_decoder_model_catches_planted_mistakes(mistake):
+    caught = 0
+    for seed in range(200):
+        try:
+            decoder_run(4, seed, mistake)
         except Hazard:
             caught += 1
     assert caught > 0, mistake
