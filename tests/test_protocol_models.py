@@ -4,7 +4,8 @@ The loop shape of the chunk attention (enc_attn.cu) coordinates one control warp
 softmax warps, the TMA unit and the tensor pipe through mbarriers and pairwise named
 barriers; the decoder (dec_step.cu) streams K and V through one and two buffers between
 CTA barriers. The split shape (enc_attn_split.cu) hands tile partials from its CTAs to one
-merging CTA through a counter. Each model replays its protocol's waits, arrivals and buffer
+merging CTA through a counter, and the ring compaction (compact.cu) moves rows within one
+buffer, overlapping itself when few rows are dropped. Each model replays its protocol's waits, arrivals and buffer
 uses in the order the kernel issues them, and a seeded scheduler picks which agent moves
 next; copies and MMAs complete whenever the scheduler lets them. A run fails on a deadlock
 (no agent can move) or when a read finds a tile other than the one the protocol promises.
@@ -361,3 +362,52 @@ def test_split_handoff_model_catches_planted_mistakes(mistake):
         except Hazard:
             caught += 1
     assert caught > 0, mistake
+
+
+# ---------------------------------------------------------------- ring compaction (compact.cu)
+
+def compaction_run(src_row, keep, seed, split=None):
+    """The move ring[s] <- ring[src_row + s], s in [0, keep), by `split` CTAs per plane, CTA
+    p owning destination rows [p * ceil(keep / split), ...). Each CTA loads all its source
+    rows, passes its CTA barrier, then stores; the CTAs interleave in any order. With no
+    `split` given, the launcher's rule: two CTAs per plane only when the move cannot overlap
+    itself (src_row >= keep), one otherwise. Returns the rows the move left at [0, keep)."""
+    rng = random.Random(seed)
+    if split is None:
+        split = 2 if src_row >= keep else 1
+    ring = list(range(src_row + keep))  # row r holds the value r
+    rows_per = -(-keep // split)
+
+    def cta(p):
+        lo, hi = p * rows_per, min(keep, (p + 1) * rows_per)
+        held = {}
+        order = list(range(lo, hi))
+        rng.shuffle(order)
+        for s in order:  # loads, in whatever order the threads issue them
+            held[s] = ring[src_row + s]
+            yield
+        rng.shuffle(order)
+        for s in order:  # stores, after the CTA barrier
+            ring[s] = held[s]
+            yield
+
+    agents = [cta(p) for p in range(split)]
+    while agents:
+        a = rng.choice(agents)
+        if next(a, "done") == "done":
+            agents.remove(a)
+    return ring[:keep]
+
+
+@pytest.mark.parametrize("src_row", [0, 1, 100, 749, 750, 786, 1200])
+def test_compaction_move(src_row):
+    keep = 750
+    for seed in range(20):
+        assert compaction_run(src_row, keep, seed) == list(range(src_row, src_row + keep)), (src_row, seed)
+
+
+def test_compaction_model_catches_split_of_an_overlapping_move():
+    keep = 750
+    bad = sum(compaction_run(src_row, keep, seed, split=2) != list(range(src_row, src_row + keep))
+              for src_row in (100, 400, 700) for seed in range(20))
+    assert bad > 0
