@@ -296,6 +296,87 @@ def test_decoder_model_catches_planted_mistakes(mistake):
     assert caught > 0, mistake
 
 
+# ---------------------------------------------------------------- split shape CTA (enc_attn_split.cu)
+
+def split_cta_run(n, seed, mistake=None, n_agents=4):
+    """One CTA of the split shape over its n key tiles. Thread 0 requests the copies and warp
+    0 issues the MMAs; one K and one V buffer, each refilled for the next tile once the MMA
+    that read it is done; S and O in TMEM (separate columns); one mbarrier for both MMA
+    commits; CTA barriers between the phases."""
+    rng = random.Random(seed)
+    bars = {k: Barrier(1) for k in ("K", "V", "M")}
+    mem = {"K": None, "V": None, "S": None, "O": None, "P": [None] * n_agents, "Q": [False] * n_agents}
+    copies, mmas = [], []
+
+    def thread(a):
+        issuer = a == 0
+        ph_m = 0
+        if issuer:
+            copies.extend([("K", 0), ("V", 0)])
+        yield ("do", lambda: mem["Q"].__setitem__(a, True))
+        yield ("group", "cta", "prologue", n_agents)
+        for t in range(n):
+            yield ("wait", "K", t & 1)
+            yield ("group", "cta", ("k", t), n_agents)
+            if issuer:
+                mmas.extend([("S", t), ("commit", "M")])
+                if mistake == "k_before_s_done" and t + 1 < n:
+                    copies.append(("K", t + 1))
+            yield ("wait", "M", ph_m)
+            ph_m ^= 1
+            if issuer and t + 1 < n and mistake != "k_before_s_done":
+                copies.append(("K", t + 1))
+            yield ("do", lambda t=t: _expect(mem["S"] == t, "row max of thread %d reads S = %s, not tile %d" % (a, mem["S"], t)))
+            yield ("group", "cta", ("max", t), n_agents)
+            yield ("do", lambda t=t: _expect(mem["S"] == t, "exps of thread %d read S = %s, not tile %d" % (a, mem["S"], t)))
+            yield ("do", lambda t=t: mem["P"].__setitem__(a, t))
+            yield ("wait", "V", t & 1)
+            yield ("group", "cta", ("v", t), n_agents)
+            if issuer:
+                mmas.extend([("O", t), ("commit", "M")])
+                if mistake == "v_before_o_done" and t + 1 < n:
+                    copies.append(("V", t + 1))
+            yield ("wait", "M", ph_m)
+            ph_m ^= 1
+            if issuer and t + 1 < n and mistake != "v_before_o_done":
+                copies.append(("V", t + 1))
+            yield ("do", lambda t=t: _expect(mem["O"] == t, "partial of thread %d reads O = %s, not tile %d" % (a, mem["O"], t)))
+            yield ("group", "cta", ("end", t), n_agents)
+
+    def run_mma(op):
+        if op[0] == "commit":
+            bars[op[1]].arrive()
+            return
+        t = op[1]
+        if op[0] == "S":
+            _expect(mem["K"] == t, "S of tile %d reads K = %s" % (t, mem["K"]))
+            _expect(all(mem["Q"]), "S issued before every query row was rotated")
+            mem["S"] = t
+        else:
+            _expect(mem["V"] == t, "O of tile %d reads V = %s" % (t, mem["V"]))
+            _expect(all(p == t for p in mem["P"]), "O of tile %d reads P = %s" % (t, mem["P"]))
+            mem["O"] = t
+
+    _schedule({"thread%d" % a: thread(a) for a in range(n_agents)}, bars, rng, copies, mmas, mem, run_mma)
+
+
+@pytest.mark.parametrize("n_tiles", [1, 2, 3])
+def test_split_cta_protocol(n_tiles):
+    for seed in range(150):
+        split_cta_run(n_tiles, 10 * n_tiles + seed)
+
+
+@pytest.mark.parametrize("mistake", ["k_before_s_done", "v_before_o_done"])
+def test_split_cta_model_catches_planted_mistakes(mistake):
+    caught = 0
+    for seed in range(200):
+        try:
+            split_cta_run(3, seed, mistake)
+        except Hazard:
+            caught += 1
+    assert caught > 0, mistake
+
+
 # ---------------------------------------------------------------- split shape handoff (enc_attn_split.cu)
 
 def split_handoff_run(n_others, seed, launches=2, mistake=None):
