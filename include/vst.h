@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
     VST_OK = 0,
     VST_E_INVAL = -1,       /* bad argument (null pointer, size, position past the table) */
-    VST_E_UNSUPPORTED = -2, /* configuration this build has no kernel for */
+    VST_E_UNSUPPORTED = -2, /* configuration the library has no kernel for */
     VST_E_CUDA = -3,        /* a CUDA runtime call failed */
     VST_E_STATE = -4,       /* ctx is failed (earlier CUDA error) or of the wrong kind */
     VST_E_TIMEOUT = -5,     /* a kernel gave up on a bounded wait (reported by vst_ctx_check) */
@@ -72,7 +72,7 @@ typedef enum { VST_ENC = 1, VST_DEC = 2 } vst_kind;
  *   decoder: kind VST_DEC, H = 32, Hk = 8, D = 128, W = 8192, ring 8192 (or any multiple
  *            of 128 >= W), max_batch 1
  * with rope_theta 1e6 and max_position 131072 (the decoder's position cap, family doc,
- * Streaming row, item (5)). Supported by this build: encoder D = 64 with H = Hk; decoder
+ * Streaming row, item (5)). Supported by the library: encoder D = 64 with H = Hk; decoder
  * D = 128 with H = 4 * Hk. Other values return VST_E_UNSUPPORTED from vst_module_create. */
 typedef struct {
     int32_t kind;         /* vst_kind */
