@@ -154,6 +154,20 @@ VST_API vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const
 /* Compact now, whatever the fill (keeps the last W rows); no-op when n_kv <= W. */
 VST_API vst_status vst_ctx_compact(vst_ctx* c, void* stream);
 
+/* Host-only: the launch shape of the chunk attention for one batch of `batch` frames over
+ * n_ctx contexts of n_heads heads, whose widest window spans max_key_tiles key tiles of 128
+ * absolute positions, when the GPU holds resident_ctas CTAs of the split shape at once (the
+ * SMs the stream can use -- the device's, lowered by an MPS active-thread percentage in the
+ * environment or by the stream's green context -- times the split shape's CTAs per SM).
+ * *split = 0: the loop shape, one CTA per (ctx, head, 128-frame query tile), *grid_x query
+ * tiles. *split = k > 0: the split shape, one CTA per (ctx, head, group of k key tiles),
+ * *grid_x groups; chosen only for a single query tile when n_ctx x n_heads < resident_ctas,
+ * with k the least that keeps the grid within resident_ctas: the shape's merging CTA waits
+ * for the other CTAs of its (ctx, head), so they must all be resident together. Both shapes
+ * give the same bits. VST_E_INVAL for non-positive sizes or NULL outputs. Needs no GPU. */
+VST_API vst_status vst_enc_launch_shape(int32_t n_heads, int32_t n_ctx, int32_t batch, int32_t max_key_tiles,
+                                        int64_t resident_ctas, int32_t* split, int32_t* grid_x);
+
 /* Host-only: the schedule vst_enc_feed would enqueue for a ctx in state (n_kv, abs_base)
  * fed n_new frames. Writes up to max_steps entries: batch[i] frames appended in step i,
  * compact[i] = 1 if a compaction precedes it. Returns the step count in *n_steps and the

@@ -344,23 +344,26 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     griddep_launch_dependents();
-    if (aborted) {
-        if (tid == 0) {
-            // A bounded wait gave up: record it, give copies in flight a bounded chance to
-            // land, release TMEM and leave.
-            atomicExch(job.err, kErrTimeout);
-            mbar_wait(bar_k, 0);
-            mbar_wait(bar_v(0), 0);
-            mbar_wait(bar_v(1), 0);
-        }
-    } else {
+    if (aborted && tid == 0) {
+        // A bounded wait gave up: record it and give copies in flight a bounded chance to
+        // land. The CTA still counts itself in below, so that the merge counter of (stream, g)
+        // ends this launch at zero like any other: the launch's output is undefined (the
+        // error word says so), the next launch's is not.
+        atomicExch(job.err, kErrTimeout);
+        mbar_wait(bar_k, 0);
+        mbar_wait(bar_v(0), 0);
+        mbar_wait(bar_v(1), 0);
+    }
+    {
         // ---- this split's partial; the last CTA of (stream, g) folds all splits in order.
         // The CTA barrier orders every thread's partial before thread 0's counter update
         // (acquire-release), which also makes the other CTAs' partials visible to the last CTA.
         const int hq = g * kG + hh;
-        job.part_o[((long long)hq * c.S + sl) * kD + row] = o;
-        if ((warp & 3) == 0 && lane == 0)
-            *reinterpret_cast<float2*>(job.part_ml + ((long long)hq * c.S + sl) * 2) = make_float2(m, l);
+        if (!aborted) {
+            job.part_o[((long long)hq * c.S + sl) * kD + row] = o;
+            if ((warp & 3) == 0 && lane == 0)
+                *reinterpret_cast<float2*>(job.part_ml + ((long long)hq * c.S + sl) * 2) = make_float2(m, l);
+        }
         __syncthreads();
         if (tid == 0) {
             const unsigned prev = atom_add_acq_rel_gpu(job.counters + g, 1u);

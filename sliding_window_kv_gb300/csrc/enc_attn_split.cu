@@ -428,10 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (s.tid == 0) {
             // Wait until the other CTAs of (job, head) have counted themselves in, then re-arm
-            // the counter for the next launch; the barrier after it passes what thread 0
-            // acquired on to the readers.
+            // the counter for the next launch by taking their counts back out: a CTA that
+            // arrives after the wait gave up still adds its one, so the counter is zero when
+            // the grid ends either way. The barrier after it passes what thread 0 acquired on
+            // to the readers.
             const bool all_in = wait_count(job.counters + h, (unsigned)others);
-            job.counters[h] = 0u;
+            atomicSub(job.counters + h, (unsigned)others);
             if (!all_in)
                 atomicExch(job.err, kErrTimeout);
             s_last = all_in && !aborted;
@@ -502,6 +504,29 @@ static cudaError_t launch_enc_attn_split_j(const KParams<EncAttnCommon, EncAttnJ
         return e;
     const dim3 grid((unsigned)grid_x, (unsigned)p.c.H, (unsigned)n_jobs);
     return launch_pdl(enc_attn_split_kernel<J>, grid, dim3(kThreads), kSmemBytes, s, p);
+}
+
+template <int J>
+static cudaError_t split_blocks_per_sm_j(int* n)
+{
+    static std::atomic<unsigned long long> configured{0};
+    const cudaError_t e = smem_limit_once(configured, enc_attn_split_kernel<J>, (int)kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, enc_attn_split_kernel<J>, kThreads, kSmemBytes);
+}
+
+cudaError_t enc_attn_split_blocks_per_sm(int* n)
+{
+    // the least over the job-table sizes a launch may use
+    int a = 0, b = 0, d = 0;
+    cudaError_t e = split_blocks_per_sm_j<1>(&a);
+    if (e == cudaSuccess)
+        e = split_blocks_per_sm_j<8>(&b);
+    if (e == cudaSuccess)
+        e = split_blocks_per_sm_j<kMaxJobs>(&d);
+    *n = e == cudaSuccess ? min(a, min(b, d)) : 0;
+    return e;
 }
 
 cudaError_t launch_enc_attn_split(const EncAttnCommon& c, const EncAttnJob* jobs, int n_jobs, int grid_x, cudaStream_t s)

@@ -12,6 +12,7 @@
 
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <atomic>
 #include <mutex>
@@ -32,6 +33,8 @@ struct vst_module {
     vst_config cfg;
     int device;
     int n_sms;     // SMs of the device (launch-shape choice)
+    int sms_usable;    // n_sms, lowered to the share an MPS active-thread percentage leaves
+    int split_per_sm;  // split-shape CTAs one SM holds at once (0: never use the split shape)
     float2* rope;  // device [max_position][D/2]
     int splits;    // scratch slots per head: decoder splits per step / encoder key tiles
     CUtensorMap* rope_map;  // device: tensor map over the rope table (128-row boxes)
@@ -86,6 +89,7 @@ int dec_splits(const vst_config& c) { return (c.window - 1 + kDecSplit - 1) / kD
 int enc_split_tiles(const vst_config& c) { return (c.window + 127 + 127) / kEncTileN + 1; }
 
 int scratch_slots(const vst_config& c) { return c.kind == VST_DEC ? dec_splits(c) : enc_split_tiles(c); }
+
 
 Layout layout_of(const vst_config& c)
 {
@@ -283,6 +287,85 @@ int record_touch(cudaStream_t s, const vst_ctx* const* ctxs, int n)
     return early;
 }
 
+// ---- co-residency of the split shape
+// The split shape's merger waits for the other CTAs of its (ctx, head), so a split-shape grid
+// must be resident all at once. These give the SMs a launch on a stream can use.
+
+// The device's SM count, lowered to the share that an MPS active-thread percentage set in
+// the environment leaves this process (rounded down).
+int mps_sm_limit(int n_sms)
+{
+    const char* e = std::getenv("CUDA_MPS_ACTIVE_THREAD_PERCENTAGE");
+    if (!e)
+        return n_sms;
+    char* end = nullptr;
+    const double pct = std::strtod(e, &end);
+    if (end == e || !(pct > 0.0) || pct >= 100.0)
+        return n_sms;
+    return (int)std::floor(n_sms * pct / 100.0);
+}
+
+struct GreenFns {
+    PFN_cuStreamGetGreenCtx_v12040 stream_ctx = nullptr;
+    PFN_cuGreenCtxGetDevResource_v12040 resource = nullptr;
+};
+
+const GreenFns& green_fns()
+{
+    static GreenFns f;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuStreamGetGreenCtx", &a, 12040, cudaEnableDefault, &qa) ==
+                cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuGreenCtxGetDevResource", &b, 12040, cudaEnableDefault, &qb) ==
+                cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            f.stream_ctx = reinterpret_cast<PFN_cuStreamGetGreenCtx_v12040>(a);
+            f.resource = reinterpret_cast<PFN_cuGreenCtxGetDevResource_v12040>(b);
+        }
+    });
+    return f;
+}
+
+// SMs a launch on stream s can use: the module's usable count, or fewer when s belongs to a
+// green context (that context's SM resource).
+int stream_sms(const vst_module* m, cudaStream_t s)
+{
+    int sms = m->sms_usable;
+    const GreenFns& f = green_fns();
+    CUgreenCtx gc = nullptr;
+    if (f.stream_ctx && f.stream_ctx(reinterpret_cast<CUstream>(s), &gc) == CUDA_SUCCESS && gc) {
+        CUdevResource r;
+        std::memset(&r, 0, sizeof r);
+        if (f.resource(gc, &r, CU_DEV_RESOURCE_TYPE_SM) == CUDA_SUCCESS)
+            sms = std::min(sms, (int)r.sm.smCount);
+    }
+    return sms;
+}
+
+// Launch shape of one batch of the chunk attention (the same bits either way). Loop shape
+// (false): one CTA per (ctx, head, query tile), grid_x = query tiles. Split shape (true), for
+// a batch of one query tile when n_ctx x n_heads CTAs would leave most SMs idle: one CTA per
+// (ctx, head, group of per_cta consecutive key tiles), the groups just large enough that the
+// grid has at most `resident` CTAs, all of which the GPU holds at once.
+bool enc_shape(int n_heads, int n_ctx, int q_tiles, int max_tiles, long long resident, int* per_cta, int* grid_x)
+{
+    *per_cta = 0;
+    *grid_x = q_tiles;
+    if (q_tiles != 1 || max_tiles < 1 || (long long)n_ctx * n_heads >= resident)
+        return false;
+    int k = 1;
+    while ((long long)n_ctx * n_heads * ((max_tiles + k - 1) / k) > resident)
+        ++k;
+    *per_cta = k;
+    *grid_x = (max_tiles + k - 1) / k;
+    return true;
+}
+
 // Zero the error word, counters and both rings (not the tensor maps).
 cudaError_t clear_ctx(vst_ctx* c, cudaStream_t s)
 {
@@ -449,6 +532,9 @@ vst_status vst_module_create(const vst_config* cfg, vst_module** out)
     m->splits = scratch_slots(*cfg);
     if (cudaDeviceGetAttribute(&m->n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || m->n_sms <= 0)
         m->n_sms = 148;
+    m->sms_usable = mps_sm_limit(m->n_sms);
+    if (cfg->kind != VST_ENC || enc_attn_split_blocks_per_sm(&m->split_per_sm) != cudaSuccess)
+        m->split_per_sm = 0;
     if (cudaMalloc(&m->rope, n * sizeof(float2)) != cudaSuccess) {
         delete m;
         return VST_E_NOMEM;
@@ -611,7 +697,12 @@ vst_status vst_ctx_check(vst_ctx* c, void* stream)
         cudaStreamSynchronize(s) != cudaSuccess)
         return VST_E_CUDA;
     if (host_err != 0) {
-        cudaMemsetAsync(c->err, 0, sizeof(int), s);
+        // Clear the error word and, for good measure, the merge counters (every CTA counts
+        // itself in even when it gives up, so they should read zero already once the
+        // launches have ended, which the synchronisation above ensures).
+        cudaMemsetAsync(c->mem, 0, kTmapOffset, s);
+        if (c->pf_mem)
+            cudaMemsetAsync(c->pf_mem, 0, c->pf_bytes, s);
         return VST_E_TIMEOUT;
     }
     return VST_OK;
@@ -661,6 +752,18 @@ vst_status vst_enc_plan(const vst_config* cfg, int64_t n_kv, int64_t abs_base, i
         *n_kv_out = n_kv;
     if (abs_base_out)
         *abs_base_out = abs_base;
+    return VST_OK;
+}
+
+vst_status vst_enc_launch_shape(int32_t n_heads, int32_t n_ctx, int32_t batch, int32_t max_key_tiles,
+                                int64_t resident_ctas, int32_t* split, int32_t* grid_x)
+{
+    if (n_heads <= 0 || n_ctx <= 0 || batch <= 0 || max_key_tiles <= 0 || resident_ctas < 0 || !split || !grid_x)
+        return VST_E_INVAL;
+    int per_cta = 0, gx = 0;
+    enc_shape(n_heads, n_ctx, (batch + kEncTileM - 1) / kEncTileM, max_key_tiles, resident_ctas, &per_cta, &gx);
+    *split = per_cta;
+    *grid_x = gx;
     return VST_OK;
 }
 
@@ -721,12 +824,10 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
                 if (tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc, cj, ncj, s); }) != cudaSuccess)
                     return fail_all(ctxs, n_ctx);
             }
-            // Launch shape, same bits either way: one CTA per (ctx, head, query tile) (two
-            // CTAs per SM) when that fills the GPU; otherwise (a single query tile) one CTA per
-            // (ctx, head, group of key tiles), with groups just large enough that every CTA
-            // starts in the first wave (one CTA per SM).
-            const bool split = q_tiles == 1 && (long long)nj * H < m->n_sms;
-            int grid_x = q_tiles;
+            // Launch shape, same bits either way (enc_shape): the loop shape when it fills the
+            // GPU, else the split shape with a grid the stream's SMs hold at once.
+            const long long resident = q_tiles == 1 ? (long long)stream_sms(m, s) * m->split_per_sm : 0;
+            const bool split_candidate = q_tiles == 1 && (long long)nj * H < resident;
             int max_tiles = 0;
             for (int i = 0; i < nj; ++i) {
                 vst_ctx* c = ctxs[c0 + i];
@@ -734,19 +835,14 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
                 ej[i] = EncAttnJob{qb + row * H * D, kb + row * Hk * D, vb + row * Hk * D, ob + row * H * D,
                                    c->k_ring, c->v_ring, c->tmap_k, c->tmap_v, c->part_ml, c->part_o,
                                    c->counters, c->err, c->abs_next, c->abs_base, c->n_kv, i};
-                if (split) {
+                if (split_candidate) {
                     const long long lo = c->abs_next - cfg.window + 1 > 0 ? c->abs_next - cfg.window + 1 : 0;
                     const int tiles = (int)((c->abs_next + b - 1) / kEncTileN - lo / kEncTileN + 1);
                     max_tiles = tiles > max_tiles ? tiles : max_tiles;
                 }
             }
-            int per_cta = 0;
-            if (split) {
-                per_cta = 1;
-                while ((long long)nj * H * ((max_tiles + per_cta - 1) / per_cta) > m->n_sms)
-                    ++per_cta;
-                grid_x = (max_tiles + per_cta - 1) / per_cta;
-            }
+            int per_cta = 0, grid_x = q_tiles;
+            const bool split = enc_shape(H, nj, q_tiles, max_tiles, resident, &per_cta, &grid_x);
             if (!split) {
                 // Loop shape: the batch's K' and V rows go to the ring first (kernel a), so
                 // that every key tile of the attention arrives whole by TMA.
@@ -1222,9 +1318,8 @@ vst_status vst_dec_step_noalloc(vst_ctx* const* ctxs, int32_t n_streams, const v
         if (cudaMemsetAsync(scratch + (size_t)i * per_stream + ml_bytes + o_bytes, 0, cnt_bytes, s) != cudaSuccess)
             return fail_all(ctxs, n_streams);
     record_touch(s, ctxs, n_streams);  // dc.early stays 0: this launch follows the memsets
-    if (launch_dec_step(dc, jobs, n_streams, work, s) != cudaSuccess)
+    if (tracked(VST_K_DEC_STEP, s, [&] { return launch_dec_step(dc, jobs, n_streams, work, s); }) != cudaSuccess)
         return fail_all(ctxs, n_streams);
-    g_launches.fetch_add(1, std::memory_order_relaxed);
     for (int i = 0; i < n_streams; ++i)
         ctxs[i]->abs_next += 1;
     return VST_OK;

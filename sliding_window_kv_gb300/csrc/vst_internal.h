@@ -148,6 +148,9 @@ cudaError_t launch_enc_attn_split(const EncAttnCommon& c, const EncAttnJob* jobs
                             cudaStream_t s);
 cudaError_t launch_dec_step(const DecCommon& c, const DecJob* jobs, int n_jobs, int total_work,
                             cudaStream_t s);
+// CTAs of the split shape that one SM holds at once (0 on error); the split shape's merger
+// waits for the other CTAs of its grid, so its grid must fit the SMs at this occupancy.
+cudaError_t enc_attn_split_blocks_per_sm(int* n);
 
 // Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per
 // device: `done` (one per kernel instantiation, bit d for device d < 64) records where it is

@@ -46,6 +46,7 @@ K_ROPE_APPEND, K_COMPACT, K_ENC_ATTN, K_DEC_STEP, K_COUNT = 0, 1, 2, 3, 4
 EXPORTS = ["vst_config_default", "vst_module_create", "vst_module_destroy", "vst_module_config",
            "vst_ctx_bytes", "vst_ctx_create", "vst_ctx_reset", "vst_ctx_destroy", "vst_ctx_info_get",
            "vst_ctx_check", "vst_ctx_selftest_wait", "vst_enc_feed", "vst_enc_feed_batch", "vst_ctx_compact", "vst_enc_plan",
+           "vst_enc_launch_shape",
            "vst_offline_bytes", "vst_offline_create", "vst_offline_destroy", "vst_enc_offline", "vst_offline_check",
            "vst_dec_step", "vst_dec_step_noalloc", "vst_dec_prefill", "vst_dec_append", "vst_prof_enable", "vst_prof_read", "vst_launch_count",
            "vst_kernel_name", "vst_status_str", "vst_version"]
@@ -79,6 +80,7 @@ def lib():
             "vst_ctx_compact": ([P, P], I32),
             "vst_enc_plan": ([ctypes.POINTER(Config), I64, I64, I32, ctypes.POINTER(I32), ctypes.POINTER(I32), I32,
                               ctypes.POINTER(I32), ctypes.POINTER(I64), ctypes.POINTER(I64)], I32),
+            "vst_enc_launch_shape": ([I32, I32, I32, I32, I64, ctypes.POINTER(I32), ctypes.POINTER(I32)], I32),
             "vst_dec_step": ([PP, I32, P, P, P, P, P], I32),
             "vst_dec_step_noalloc": ([PP, I32, P, P, P, P, P], I32),
             "vst_dec_prefill": ([P, P, P, P, I32, P, P], I32),
@@ -248,6 +250,16 @@ def enc_plan(cfg: Config, n_kv: int, abs_base: int, n_new: int, max_steps: int =
                               ctypes.byref(nk), ctypes.byref(ab)), "vst_enc_plan")
     k = min(n.value, max_steps)
     return [(batch[i], comp[i]) for i in range(k)], nk.value, ab.value
+
+
+def enc_launch_shape(n_heads: int, n_ctx: int, batch: int, max_key_tiles: int, resident_ctas: int):
+    """(split, grid_x) of the chunk attention's launch: split = 0 for the loop shape, else key
+    tiles per CTA of the split shape (host-only; see vst_enc_launch_shape)."""
+    sp = ctypes.c_int32()
+    gx = ctypes.c_int32()
+    _check(lib().vst_enc_launch_shape(n_heads, n_ctx, batch, max_key_tiles, resident_ctas, ctypes.byref(sp),
+                                      ctypes.byref(gx)), "vst_enc_launch_shape")
+    return sp.value, gx.value
 
 
 def dec_step(ctxs, q, k, v, out, stream=None):

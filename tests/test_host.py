@@ -127,3 +127,36 @@ def test_binding_refuses_short_tensors():
         with pytest.raises(ValueError):
             vst._need_io(cfg, rows, *args)
     vst._need_io(None, rows, short, short, short, short)  # unknown ctx: nothing to check against
+
+
+def test_split_shape_grid_fits_the_resident_ctas():
+    """The split shape of the chunk attention has a CTA that waits for the other CTAs of its
+    (ctx, head), so its grid must be resident at once: checked with faked SM counts (a full
+    GB300 at one split CTA per SM, an MPS share, a small green context, no occupancy)."""
+    shape = vst.enc_launch_shape
+    # one stream of 20 heads, a 50-frame feed: 7 or 8 key tiles of the 750 window
+    assert shape(20, 1, 50, 7, 152) == (1, 7)     # 140 CTAs fit 152 SMs
+    assert shape(20, 1, 50, 8, 152) == (2, 4)     # 160 do not: pairs of tiles, 80 CTAs
+    assert shape(20, 1, 50, 7, 76) == (3, 3)      # half the SMs (MPS 50 %): 60 CTAs
+    assert shape(20, 1, 50, 7, 20) == (0, 1)      # one CTA per head would not leave room: loop shape
+    assert shape(20, 1, 50, 7, 0) == (0, 1)       # no split CTA fits an SM: loop shape
+    assert shape(20, 1, 129, 8, 152) == (0, 2)    # two query tiles: loop shape
+    assert shape(20, 8, 100, 8, 152) == (0, 1)    # 160 (ctx, head) pairs fill the GPU: loop shape
+    rng = random.Random(7)
+    for _ in range(3000):
+        H, n, b, t = rng.randint(1, 32), rng.randint(1, 64), rng.randint(1, 512), rng.randint(1, 9)
+        res = rng.choice([0, 1, 8, 20, 76, 100, 152, 304, rng.randint(0, 400)])
+        k, gx = shape(H, n, b, t, res)
+        if k == 0:
+            assert gx == (b + 127) // 128
+            assert b > 128 or n * H >= res
+        else:
+            assert b <= 128 and n * H < res
+            assert gx == -(-t // k)
+            assert n * H * gx <= res                              # the whole grid is resident
+            assert k == 1 or n * H * -(-t // (k - 1)) > res       # and k is the least that fits
+    for bad in [(0, 1, 50, 7, 152), (20, 0, 50, 7, 152), (20, 1, 0, 7, 152), (20, 1, 50, 0, 152),
+                (20, 1, 50, 7, -1)]:
+        with pytest.raises(vst.VstError) as e:
+            shape(*bad)
+        assert e.value.status == vst.E_INVAL

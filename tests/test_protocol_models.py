@@ -445,6 +445,143 @@ def test_split_handoff_model_catches_planted_mistakes(mistake):
     assert caught > 0, mistake
 
 
+# ---------------------------------------------------------------- merge counters after a time-out
+
+def _run_agents(agents, pending, partial, rng):
+    cur = {k: next(g, None) for k, g in agents.items()}
+    for _ in range(200000):
+        live = [k for k, v in cur.items() if v is not None]
+        if not live and not pending:
+            return
+        c = rng.choice(live + (["drain"] if pending else []))
+        if c == "drain":
+            i, l = pending.pop(rng.randrange(len(pending)))
+            partial[i] = l
+        else:
+            cur[c] = next(agents[c], None)
+    raise Hazard("no end in sight")
+
+
+def decoder_merge_run(n_splits, seed, launches=3, mistake=None):
+    """Successive decoder launches over one (stream, KV head) (dec_step.cu). Each split's CTA
+    stores its partial and counts itself in with an acquire-release add; the CTA that sees
+    the count reach n_splits - 1 folds every partial and re-arms the count to zero. In the
+    first launch some CTAs give up on a bounded wait: they store nothing but still count
+    themselves in, and that launch's output is undefined. Every later launch must fold only
+    its own partials, exactly once."""
+    rng = random.Random(seed)
+    mem = {"count": 0}
+    partial = {}
+    for launch in range(launches):
+        aborts = {i for i in range(n_splits) if launch == 0 and rng.random() < 0.4}
+        pending, merged = [], []
+
+        def cta(i, aborts=aborts, pending=pending, merged=merged, launch=launch):
+            if i not in aborts:
+                pending.append((i, launch))
+                yield "store"
+                while any(p[0] == i for p in pending):
+                    yield "release waits for the stores"
+            elif mistake == "abort_not_counted":
+                return
+            prev = mem["count"]
+            mem["count"] = prev + 1
+            yield "counted in"
+            if prev == n_splits - 1:
+                if not aborts:
+                    for u in range(n_splits):
+                        _expect(partial.get(u) == launch, "launch %d folds the partial of split %d from launch %s"
+                                % (launch, u, partial.get(u)))
+                mem["count"] = 0
+                merged.append(launch)
+                yield "merged"
+
+        _run_agents({i: cta(i) for i in range(n_splits)}, pending, partial, rng)
+        if launch > 0:
+            _expect(merged == [launch], "launch %d merged %d times" % (launch, len(merged)))
+        _expect(mem["count"] == 0, "launch %d ends with the count at %d" % (launch, mem["count"]))
+
+
+def merger_timeout_run(n_others, seed, launches=3, mistake=None, limit=40):
+    """Successive split-shape launches over one (context, head) (enc_attn_split.cu). In the
+    first launch one CTA is late, so the merger's bounded poll may give up before it has
+    counted itself in; the merger then re-arms the counter by taking its n_others counts
+    back out, and the late CTA's add still lands before the launch ends. Every later launch
+    must fold only its own partials."""
+    rng = random.Random(seed)
+    mem = {"count": 0}
+    partial = {}
+    for launch in range(launches):
+        late = rng.randrange(n_others) if launch == 0 else -1
+        pending = []
+
+        def other(i, pending=pending, launch=launch, late=late):
+            pending.append((i, launch))
+            yield "store"
+            while any(p[0] == i for p in pending):
+                yield "release waits for the stores"
+            if i == late:
+                for _ in range(4 * limit):
+                    yield "late"
+            mem["count"] += 1
+            yield "counted in"
+
+        def merger(launch=launch):
+            polls, all_in = 0, True
+            while mem["count"] < n_others:
+                polls += 1
+                if polls > limit:
+                    all_in = False
+                    break
+                yield "poll"
+            if all_in and launch > 0:
+                for i in range(n_others):
+                    _expect(partial.get(i) == launch, "merger of launch %d reads the partial of CTA %d from launch %s"
+                            % (launch, i, partial.get(i)))
+            if mistake == "rearm_by_zeroing":
+                mem["count"] = 0
+            else:
+                mem["count"] -= n_others
+            yield "merged"
+
+        agents = {i: other(i) for i in range(n_others)}
+        agents["merger"] = merger()
+        _run_agents(agents, pending, partial, rng)
+        _expect(mem["count"] == 0, "launch %d ends with the count at %d" % (launch, mem["count"]))
+
+
+@pytest.mark.parametrize("n_splits", [1, 2, 17])
+def test_decoder_merge_counter_after_abort(n_splits):
+    for seed in range(200):
+        decoder_merge_run(n_splits, seed)
+
+
+def test_decoder_merge_model_catches_an_uncounted_abort():
+    caught = 0
+    for seed in range(200):
+        try:
+            decoder_merge_run(17, seed, mistake="abort_not_counted")
+        except Hazard:
+            caught += 1
+    assert caught > 0
+
+
+@pytest.mark.parametrize("n_others", [1, 6])
+def test_split_merger_counter_after_timeout(n_others):
+    for seed in range(200):
+        merger_timeout_run(n_others, seed)
+
+
+def test_split_merger_model_catches_rearm_by_zeroing():
+    caught = 0
+    for seed in range(200):
+        try:
+            merger_timeout_run(6, seed, mistake="rearm_by_zeroing")
+        except Hazard:
+            caught += 1
+    assert caught > 0
+
+
 # ---------------------------------------------------------------- ring compaction (compact.cu)
 
 def compaction_run(src_row, keep, seed, split=None):

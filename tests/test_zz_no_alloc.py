@@ -2,12 +2,13 @@
 call time (a real-time streaming thread that must not block on cudaMalloc, or a process
 whose device memory belongs to another allocator). Its scratch lives in a static device
 array inside libvst; the test checks, through the C ABI, that two calls in a row give what
-vst_dec_step gives on identical contexts, and that calls beyond the array's limit are
-refused. This file is collected last on purpose."""
+vst_dec_step gives on identical contexts, that those rows also agree with the fp64 oracle,
+and that calls beyond the array's limit are refused. This file is collected last on purpose."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from sliding_window_kv_gb300 import synth, vst
 
 pytestmark = pytest.mark.gpu
@@ -53,6 +54,15 @@ def test_noalloc_matches_dec_step_two_calls(dev):
         assert torch.isfinite(got.float()).all()
         assert d.max().item() <= MAX_TOL and d.mean().item() <= MEAN_TOL, (step, d.max().item())
         assert torch.equal(got, ref), step
+        # each stream's row against the oracle computed from that row's own window
+        outs = got.float().cpu().double().numpy()
+        for s, ((q, k, v), f) in enumerate(zip(seqs, fills)):
+            i = f + step
+            j0 = max(0, i - 8191)
+            qb, kb, vb = (synth.bits(x[:i + 1].cpu()) for x in (q, k, v))
+            want = oracle.attention_row(qb[i], kb[j0:i + 1], vb[j0:i + 1], i, 8192)
+            e = np.abs(outs[s] - want)
+            assert e.max() <= MAX_TOL and e.mean() <= MEAN_TOL, (step, s, e.max(), e.mean())
     for c in ref_ctxs + na_ctxs:
         assert vst.ctx_check(c.handle) == vst.OK
         c.close()
