@@ -8,10 +8,13 @@ clip through all 32 layers (contexts reset at the start of the step), so every s
 feed bookkeeping, compaction, RoPE + append and chunk attention. `value` is encoder frames
 per second with inputs resident in HBM, measured on CUDA-graph replays of the step.
 
-The same line carries `dec`: the decoder step workload (26 layers, GQA 32q/8kv x 128, KV
-filled to 8192, batch 1, 256 steps across the ring wrap) in decoder steps per second, so
-both halves of the metric are reported. `--workload` selects the other configurations for
-exploration (they print the same kind of line).
+The same line carries every other configuration of the metric as an object: `dec`, the
+decoder step workload (26 layers, GQA 32q/8kv x 128, KV filled to 8192, batch 1, 256 steps
+across the ring wrap) in decoder steps per second, with its own end-to-end figure through
+the C ABI; `dec_b64`, 64 decoder streams with fills uniform in [1, 8192]; `enc_long16`, 16
+encoder streams with staggered starts in 512-frame batches (15300 frames each, many
+compactions); and the next rows, `prefill` (the 39-token prompt) and `offline` (4 whole
+clips). `--workload` runs one configuration alone (it prints the same kind of line).
 
 Inputs are synthetic (seeded counter-based bf16 ~N(0,1), sliding_window_kv_gb300.synth);
 the per-step inputs and caches exceed the 129 MB L2, so no flush is needed between steps.
@@ -455,6 +458,78 @@ class DecWorkload:
                 vst.dec_step([c.handle for c in self.ctxs[l]], self.Q[l][t], self.K[l][t], self.V[l][t],
                              self.O[l][t], stream)
 
+    def e2e_setup(self, stream):
+        """End-to-end decoding as a client runs it: each step's inputs (every layer's q, k, v
+        for every stream) sit in one pinned host block and go to the GPU in one copy on a copy
+        stream; the step's 26 vst_dec_step calls wait for that copy only, and the step's
+        outputs come back in one copy on a third stream."""
+        import ctypes
+        import torch
+        vst = self.vst
+        L = vst.lib()
+        sp = vst._stream(stream)
+        dev = self.Q[0].device
+        nq, nk = self.S * DEC_H * DEC_D, self.S * DEC_HK * DEC_D
+        per_layer = nq + 2 * nk
+        st = {"hin": [], "din": [], "hout": [], "dout": [], "calls": []}
+        st["arrays"] = [(ctypes.c_void_p * self.S)(*[c.handle for c in self.ctxs[l]]) for l in range(self.L)]
+        for t in range(self.steps):
+            hin = torch.empty(self.L * per_layer, dtype=torch.bfloat16, pin_memory=True)
+            for l in range(self.L):
+                base = l * per_layer
+                hin[base:base + nq].copy_(self.Q[l][t].reshape(-1).cpu())
+                hin[base + nq:base + nq + nk].copy_(self.K[l][t].reshape(-1).cpu())
+                hin[base + nq + nk:base + per_layer].copy_(self.V[l][t].reshape(-1).cpu())
+            din = torch.empty_like(hin, device=dev)
+            hout = torch.empty(self.L * nq, dtype=torch.bfloat16, pin_memory=True)
+            dout = torch.empty_like(hout, device=dev)
+            calls = []
+            for l in range(self.L):
+                base = l * per_layer
+                calls.append((L.vst_dec_step, (st["arrays"][l], self.S, din[base:].data_ptr(),
+                                               din[base + nq:].data_ptr(), din[base + nq + nk:].data_ptr(),
+                                               dout[l * nq:].data_ptr(), sp)))
+            st["hin"].append(hin)
+            st["din"].append(din)
+            st["hout"].append(hout)
+            st["dout"].append(dout)
+            st["calls"].append(calls)
+        st["copy"] = torch.cuda.Stream(dev)
+        st["back"] = torch.cuda.Stream(dev)
+        n_groups = -(-self.steps // self.E2E_GROUP)
+        st["ev_in"] = [torch.cuda.Event() for _ in range(n_groups)]
+        st["ev_out"] = [torch.cuda.Event() for _ in range(n_groups)]
+        st["h2d"] = sum(x.numel() * 2 for x in st["hin"])
+        st["d2h"] = sum(x.numel() * 2 for x in st["hout"])
+        return st
+
+    E2E_GROUP = 8  # steps per cross-stream synchronisation
+
+    def e2e_run(self, st, stream):
+        """All the steps end to end (the caches must hold the fill only: call rewind first)."""
+        import torch
+        n = self.steps
+        groups = [range(g, min(n, g + self.E2E_GROUP)) for g in range(0, n, self.E2E_GROUP)]
+        st["copy"].wait_stream(stream)
+        with torch.cuda.stream(st["copy"]):
+            for gi, grp in enumerate(groups):
+                for t in grp:
+                    st["din"][t].copy_(st["hin"][t], non_blocking=True)
+                st["ev_in"][gi].record(st["copy"])
+        for gi, grp in enumerate(groups):
+            stream.wait_event(st["ev_in"][gi])
+            for t in grp:
+                for fn, args in st["calls"][t]:
+                    if fn(*args) != 0:
+                        raise RuntimeError("vst_dec_step failed")
+            st["ev_out"][gi].record(stream)
+        with torch.cuda.stream(st["back"]):
+            for gi, grp in enumerate(groups):
+                st["back"].wait_event(st["ev_out"][gi])
+                for t in grp:
+                    st["hout"][t].copy_(st["dout"][t], non_blocking=True)
+        stream.wait_stream(st["back"])
+
     def kv_bytes(self, start_positions):
         """Algorithmic bytes of kernel (c) for one run of the steps starting at the given
         positions: K and V of every visible key (min(pos+1, W) keys x Hk x D x 2 B x 2)
@@ -745,7 +820,7 @@ def workload_config(name, spec):
         "l2": "KV cache read per step larger than L2 (no flush)"}
 
 
-def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu):
+def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu, e2e=False):
     import torch
     from sliding_window_kv_gb300 import vst
     w = DecWorkload(spec, dev, n_steps, dist.rank)
@@ -772,12 +847,45 @@ def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu):
                         "peak_source": src, "launches": nl, "avg_launch_us": launch_us,
                         "isolated_launch_us": 1e3 * kms / nl, "timing": TIMING_NOTE,
                         "algorithmic_bytes_per_launch": bytes_per_launch}}
+    if e2e:
+        # the same steps through the C ABI with host copies: the eager, captured and profiled
+        # runs above advanced each context's position on the host, and the e2e run steps on
+        # from there (at a full window every step reads the same number of keys)
+        est = w.e2e_setup(stream)
+        w.e2e_run(est, stream)  # warm-up
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        a.record(stream)
+        w.e2e_run(est, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        dist.barrier()
+        e2e_value, _ = dist.job_rate(w.steps, a.elapsed_time(b))
+        out["e2e"] = {"value": e2e_value, "unit": "dec steps/s",
+                      "h2d_bytes_per_step": est["h2d"] / w.steps, "d2h_bytes_per_step": est["d2h"] / w.steps,
+                      "steps": w.steps, "host_wall_s": wall,
+                      "path": "vst_dec_step per layer and step through the C ABI (no graph); each step's inputs "
+                              "(all layers) copied host to device in one copy on a copy stream, its outputs back "
+                              "on a third stream, one cross-stream wait per 8 steps, pinned memory, all inside "
+                              "the region"}
+        del est
     if want_cpu:
+        # the oracle on one stream at a full window, scaled to the workload's streams and
+        # their mean visible keys per step (its time per step is linear in the keys)
         v, dt, sample = cpu_baseline_dec(spec, 16, cpu_threads())
         v1, dt1, sample1 = cpu_baseline_dec(spec, 4, 1)
-        out["cpu_baseline"] = {"value": v, "unit": "dec steps/s", "cores": cpu_threads(), "kind": "oracle",
-                               "sample": sample, "seconds": dt,
-                               "single_thread": {"value": v1, "sample": sample1, "seconds": dt1}}
+        keys = statistics.mean(min(p + t + 1, DEC_W) for p in start_pos for t in range(w.steps)) * len(start_pos)
+        scale = DEC_W / keys
+        out["cpu_baseline"] = {"value": v * scale, "unit": "dec steps/s", "cores": cpu_threads(), "kind": "oracle",
+                               "sample": sample + ("; scaled to %d streams of %.0f visible keys on average"
+                                                   % (len(start_pos), keys / len(start_pos)) if scale != 1 else ""),
+                               "seconds": dt,
+                               "single_thread": {"value": v1 * scale, "sample": sample1, "seconds": dt1}}
     w.close()
     return out
 
@@ -853,6 +961,85 @@ def bench_prefill(spec, dev, stream, dist, steps, warmup, peaks):
     return out
 
 
+def bench_enc(spec, dev, stream, dist, steps, warmup, peaks, workload, e2e=True, want_cpu=False):
+    """One encoder streaming workload: `value` from CUDA-graph replays of the step, the
+    attention's roofline, the compaction's HBM fraction and (e2e) the same step through the
+    C ABI with host copies inside the region."""
+    import torch
+    from sliding_window_kv_gb300 import vst
+    w = EncWorkload(spec, dev, dist.rank)
+    w.run_step(stream)  # eager warm-up
+    torch.cuda.synchronize()
+    n0 = vst.launch_count()
+    g = capture(w.run_step, stream)
+    launches_per_step = vst.launch_count() - n0
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    value, ms = dist.job_rate(w.frames_per_step * steps, time_graph(g, stream, steps, dist))
+    prof = profiled_kernels(w.run_step, stream)
+    del g
+
+    # dominant kernel: chunk attention (kernel b), tensor-bound
+    nl, kms = prof["enc_attn_kernel"]
+    flops_per_launch = w.attn_flops() / max(1, nl)
+    launch_us = region_launch_us(prof, "enc_attn_kernel", ms / steps)
+    achieved = flops_per_launch / (launch_us / 1e6) / 1e12
+    hbm, tf, tfs, src = peaks
+    out = {"value": value, "unit": "enc frames/s", "ms_per_step": ms / steps,
+           "config": workload_config(workload, spec),
+           "roofline": {"kernel": "enc_attn_kernel", "bound": "tensor", "achieved": achieved, "peak": tf,
+                        "unit": "TFLOP/s", "frac": achieved / tf,
+                        "traffic": dram_traffic("enc_attn_kernel", flops_per_launch, workload),
+                        "peak_source": src + " bf16 burst", "launches": nl,
+                        "avg_launch_us": launch_us, "isolated_launch_us": 1e3 * kms / nl,
+                        "timing": TIMING_NOTE, "algorithmic_flops_per_launch": flops_per_launch},
+           "kernels": {k: {"launches": v[0], "total_ms": v[1]} for k, v in prof.items() if v[0]},
+           "gpu_launches": launches_per_step * steps}
+    ncmp, cms = prof["compact_kernel"]
+    if ncmp:
+        cb = w.compact_bytes() / ncmp
+        cus = region_launch_us(prof, "compact_kernel", ms / steps)
+        out["compaction"] = {"kernel": "compact_kernel", "bound": "hbm", "launches": ncmp,
+                             "avg_launch_us": cus, "isolated_launch_us": 1e3 * cms / ncmp,
+                             "timing": TIMING_NOTE, "algorithmic_bytes_per_launch": cb,
+                             "achieved_gbs": cb / (cus / 1e6) / 1e9, "frac": cb / (cus / 1e6) / 1e9 / hbm,
+                             "traffic": dram_traffic("compact_kernel", cb, workload, fallback=False)}
+
+    if e2e:
+        est = w.e2e_setup(stream)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        w.e2e_run(est, stream)  # warm-up
+        torch.cuda.synchronize()
+        e2e_steps = max(1, min(steps, 5))
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        a.record(stream)
+        for _ in range(e2e_steps):
+            w.e2e_run(est, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        dist.barrier()
+        e2e_value, _ = dist.job_rate(w.frames_per_step * e2e_steps, a.elapsed_time(b))
+        out["e2e"] = {"value": e2e_value, "unit": "enc frames/s",
+                      "h2d_bytes_per_step": est["h2d"], "d2h_bytes_per_step": est["d2h"],
+                      "steps": e2e_steps, "host_wall_s": wall,
+                      "path": "vst_enc_feed per layer and feed through the C ABI (no graph); each feed's "
+                              "inputs copied host to device in one copy on a copy stream, its outputs back "
+                              "on a third stream, one cross-stream wait per 8 feeds, pinned memory, all "
+                              "inside the region"}
+        del est
+    w.close()
+    if want_cpu:
+        v, dt, sample = cpu_baseline_enc(spec, 1, cpu_threads())
+        out["cpu_baseline"] = {"value": v, "unit": "enc frames/s", "cores": cpu_threads(), "kind": "oracle",
+                               "sample": sample, "seconds": dt}
+    return out
+
+
 def run_vst(args, dist):
     import torch
     from sliding_window_kv_gb300 import vst
@@ -899,104 +1086,52 @@ def run_vst(args, dist):
     if spec["kind"] == "dec":
         with torch.cuda.stream(stream):
             sampler.start()
-            d = bench_dec(spec, dev, stream, dist, spec["steps"], args.warmup, peaks, want_cpu_baseline(args, dist))
+            d = bench_dec(spec, dev, stream, dist, spec["steps"], args.warmup, peaks, want_cpu_baseline(args, dist),
+                          e2e=not args.no_e2e)
             clocks = sampler.stop()
         line.update({"value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"], "config": d["config"],
                      "roofline": d["roofline"], "gpu_launches": d["gpu_launches"], "clocks": clocks})
-        if "cpu_baseline" in d:
-            line["cpu_baseline"] = d["cpu_baseline"]
+        for k in ("cpu_baseline", "e2e"):
+            if k in d:
+                line[k] = d[k]
         if dist.rank == 0:
             print(json.dumps(line))
         return
 
-    w = EncWorkload(spec, dev, dist.rank)
     with torch.cuda.stream(stream):
-        w.run_step(stream)  # eager warm-up
-        torch.cuda.synchronize()
-        n0 = vst.launch_count()
-        g = capture(w.run_step, stream)
-        launches_per_step = vst.launch_count() - n0
-        for _ in range(args.warmup):
-            g.replay()
-        torch.cuda.synchronize()
         sampler.start()
-        value, ms = dist.job_rate(w.frames_per_step * args.steps, time_graph(g, stream, args.steps, dist))
-        prof = profiled_kernels(w.run_step, stream)
+        d = bench_enc(spec, dev, stream, dist, args.steps, args.warmup, peaks, args.workload, e2e=not args.no_e2e)
         clocks = sampler.stop()
-        del g
-
-        # dominant kernel: chunk attention (kernel b), tensor-bound
-        nl, kms = prof["enc_attn_kernel"]
-        flops_per_launch = w.attn_flops() / max(1, nl)
-        launch_us = region_launch_us(prof, "enc_attn_kernel", ms / args.steps)
-        achieved = flops_per_launch / (launch_us / 1e6) / 1e12
-        hbm, tf, tfs, src = peaks
-        line.update({"value": value, "unit": "enc frames/s", "ms_per_step": ms / args.steps,
-                     "config": workload_config(args.workload, spec),
-                     "roofline": {"kernel": "enc_attn_kernel", "bound": "tensor", "achieved": achieved, "peak": tf,
-                                  "unit": "TFLOP/s", "frac": achieved / tf,
-                                  "traffic": dram_traffic("enc_attn_kernel", flops_per_launch, args.workload),
-                                  "peak_source": src + " bf16 burst", "launches": nl,
-                                  "avg_launch_us": launch_us, "isolated_launch_us": 1e3 * kms / nl,
-                                  "timing": TIMING_NOTE, "algorithmic_flops_per_launch": flops_per_launch},
-                     "kernels": {k: {"launches": v[0], "total_ms": v[1]} for k, v in prof.items() if v[0]},
-                     "gpu_launches": launches_per_step * args.steps, "clocks": clocks})
-        ncmp, cms = prof["compact_kernel"]
-        if ncmp:
-            cb = w.compact_bytes() / ncmp
-            cus = region_launch_us(prof, "compact_kernel", ms / args.steps)
-            line["compaction"] = {"kernel": "compact_kernel", "bound": "hbm", "launches": ncmp,
-                                  "avg_launch_us": cus, "isolated_launch_us": 1e3 * cms / ncmp,
-                                  "timing": TIMING_NOTE, "algorithmic_bytes_per_launch": cb,
-                                  "achieved_gbs": cb / (cus / 1e6) / 1e9, "frac": cb / (cus / 1e6) / 1e9 / hbm}
-
-        if not args.no_e2e:
-            est = w.e2e_setup(stream)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            w.e2e_run(est, stream)  # warm-up
-            torch.cuda.synchronize()
-            e2e_steps = max(1, min(args.steps, 5))
-            dist.barrier()
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            a.record(stream)
-            for _ in range(e2e_steps):
-                w.e2e_run(est, stream)
-            b.record(stream)
-            torch.cuda.synchronize()
-            wall = time.perf_counter() - t0
-            dist.barrier()
-            e2e_value, _ = dist.job_rate(w.frames_per_step * e2e_steps, a.elapsed_time(b))
-            line["e2e"] = {"value": e2e_value, "unit": "enc frames/s",
-                           "h2d_bytes_per_step": est["h2d"], "d2h_bytes_per_step": est["d2h"],
-                           "steps": e2e_steps, "host_wall_s": wall,
-                           "path": "vst_enc_feed per layer and feed through the C ABI (no graph); each feed's "
-                                   "inputs copied host to device in one copy on a copy stream, its outputs back "
-                                   "on a third stream, one cross-stream wait per 8 feeds, pinned memory, all "
-                                   "inside the region"}
-            del est
-        w.close()
+        line.update({k: v for k, v in d.items() if k != "clocks"})
+        line["clocks"] = clocks
 
         if not args.no_dec and args.workload == "enc_stream":
-            sampler2 = ClockSampler(dist.local_rank)
-            sampler2.start()
+            # the other configurations of the metric, each an object of the line: the decoder
+            # at batch 1 (with its end-to-end figure), 64 decoder streams, 16 encoder streams
+            # in 512-frame batches, and the next rows (prefill, offline encoder)
+            def timed(fn):
+                smp = ClockSampler(dist.local_rank)
+                smp.start()
+                out = fn()
+                out["clocks"] = smp.stop()
+                torch.cuda.empty_cache()
+                return out
+
             dspec = dict(WORKLOADS["dec_b1"])
             dspec["steps"] = args.dec_steps
-            d = bench_dec(dspec, dev, stream, dist, args.dec_steps, args.warmup, peaks,
-                          want_cpu_baseline(args, dist))
-            d["clocks"] = sampler2.stop()
-            line["dec"] = d
-            sampler3 = ClockSampler(dist.local_rank)
-            sampler3.start()
-            d = bench_prefill(dict(WORKLOADS["dec_prefill39"]), dev, stream, dist, args.steps, args.warmup, peaks)
-            d["clocks"] = sampler3.stop()
-            line["prefill"] = d
-            sampler4 = ClockSampler(dist.local_rank)
-            sampler4.start()
-            d = bench_offline(dict(WORKLOADS["enc_offline4"]), dev, stream, dist, args.steps, args.warmup, peaks)
-            d["clocks"] = sampler4.stop()
-            line["offline"] = d
+            line["dec"] = timed(lambda: bench_dec(dspec, dev, stream, dist, args.dec_steps, args.warmup, peaks,
+                                                  want_cpu_baseline(args, dist), e2e=not args.no_e2e))
+            dspec64 = dict(WORKLOADS["dec_b64"])
+            dspec64["steps"] = args.dec_steps
+            line["dec_b64"] = timed(lambda: bench_dec(dspec64, dev, stream, dist, args.dec_steps, args.warmup, peaks,
+                                                      want_cpu_baseline(args, dist)))
+            line["enc_long16"] = timed(lambda: bench_enc(dict(WORKLOADS["enc_long16"]), dev, stream, dist,
+                                                         args.steps, args.warmup, peaks, "enc_long16", e2e=False,
+                                                         want_cpu=want_cpu_baseline(args, dist)))
+            line["prefill"] = timed(lambda: bench_prefill(dict(WORKLOADS["dec_prefill39"]), dev, stream, dist,
+                                                          args.steps, args.warmup, peaks))
+            line["offline"] = timed(lambda: bench_offline(dict(WORKLOADS["enc_offline4"]), dev, stream, dist,
+                                                          args.steps, args.warmup, peaks))
 
     if want_cpu_baseline(args, dist):
         v, dt, sample = cpu_baseline_enc(spec, 4 if spec["layers"] >= 4 else spec["layers"], cpu_threads())

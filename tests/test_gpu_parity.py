@@ -306,6 +306,42 @@ def test_enc_batch_equals_single(dev, enc_module, n_ctx, step):
         c.close()
 
 
+def test_enc_16_unstaggered_streams_512_batches(dev, enc_module):
+    """16 streams that all start at position 0, fed four 512-frame batches together (the
+    fourth after a compaction of all 16 rings in one launch): every loop-shape launch covers
+    the same positions in every context, from one key tile per query tile at the start of
+    the clip to seven after the compaction, with ring slots below zero for the first key
+    tile. Sampled rows of three streams against the oracle; stream 0 re-fed alone in
+    50-frame feeds (the split shape) gives the same bits."""
+    S, T, B = 16, 2048, 512
+    seqs = [_enc_inputs(7, s, T) for s in range(S)]
+    ctxs = [vst.Ctx(enc_module) for _ in range(S)]
+    Q, K, V = (torch.stack([seqs[s][i] for s in range(S)]).to(dev) for i in range(3))
+    OUT = torch.empty_like(Q)
+    for t0 in range(0, T, B):
+        o = torch.empty_like(Q[:, t0:t0 + B].contiguous())
+        vst.enc_feed_batch([c.handle for c in ctxs], Q[:, t0:t0 + B].contiguous(), K[:, t0:t0 + B].contiguous(),
+                           V[:, t0:t0 + B].contiguous(), o, B)
+        OUT[:, t0:t0 + B] = o
+    torch.cuda.synchronize()
+    for c in ctxs:
+        assert vst.ctx_check(c.handle) == vst.OK
+        info = c.info()
+        assert (info.n_kv, info.abs_base, info.abs_next, info.n_compactions) == (1262, 786, 2048, 1)
+    got = OUT.float().cpu().double().numpy()
+    for s in (0, 7, 15):
+        qb, kb, vb = (synth.bits(x) for x in seqs[s])
+        for i in (0, 127, 128, 511, 512, 1535, 1536, 1663, 2047):
+            j0 = max(0, i - 749)
+            want = oracle.attention_row(qb[i], kb[j0:i + 1], vb[j0:i + 1], i, 750)
+            d = np.abs(got[s, i] - want)
+            assert d.max() <= MAX_TOL and d.mean() <= MEAN_TOL, (s, i, d.max(), d.mean())
+    alone, _ = _feed(enc_module, *seqs[0], [50] * (T // 50) + [T % 50])
+    assert torch.equal(alone, OUT[0])
+    for c in ctxs:
+        c.close()
+
+
 def test_enc_16_streams_512_batches(dev, enc_module):
     """The 16-stream launch configuration: streams with staggered starts (a first feed of
     96 s frames), then 512-frame batches through vst_enc_feed_batch (every batch launch is
