@@ -20,23 +20,32 @@
 // this launch. Per tile:
 //   S   = Q' K'^T      tcgen05.mma M=128 N=128 K=64, A/B K-major bf16 in smem, D in TMEM
 //   softmax            tile-local max m_t, p = 2^(s*log2e/sqrt(D) - m_t), l_t = sum p;
-//                      P -> smem as bf16
-//   O_t = P V          tcgen05.mma M=128 N=64 K=128, A = P (K-major), B = V (MN-major)
+//                      P -> TMEM as bf16 pairs, over the S columns already read
+//   O_t = P V          tcgen05.mma M=128 N=32 K=128 per 32 output dims, A = P from TMEM,
+//                      B = V (MN-major smem)
 //   fold               (m, l, o) <- fold((m, l, o), (m_t, l_t, O_t)), ascending t
 // A tile where a row sees no key is skipped for that row (exact no-op).
 //
-// Threads: 256 per CTA, two CTAs per SM. Query row r (TMEM lane r) is shared by the two
-// threads (r, half), one in each group of four warps: thread (r, half) owns score quarters
-// 2 half and 2 half + 1 (columns [64 half, 64 half + 64)), output dims [32 half, 32 half
-// + 32) and RoPE pairs [16 half, 16 half + 16). Row max and row sum are combined from the
-// two halves through shared memory, (Q0 + Q1) + (Q2 + Q3) (enc_common.cuh).
+// Threads: 288 per CTA, two CTAs per SM. Eight softmax warps: query row r (TMEM lane r) is
+// shared by the two threads (r, half), one in each group of four warps; thread (r, half)
+// owns score columns [64 half, 64 half + 64), output dims [32 half, 32 half + 32) and RoPE
+// pairs [16 half, 16 half + 16). Row max and row sum are combined from the two halves
+// through shared memory, (Q0 + Q1) + (Q2 + Q3) (enc_common.cuh). One control warp issues
+// the TMA loads and the MMAs (converged, through its elected lane).
+//
+// Tensor memory: two 128-column buffers; tile t uses buffer (t - t_lo) & 1, whose columns
+// [64 half, 64 half + 64) belong to thread (r, half): they first hold its 64 scores of S_t,
+// then its 64 probabilities P_t as bf16 pairs in [64 half, 64 half + 32) (each written over
+// scores the thread has already read) and output dims [32 half, 32 half + 32) of O_t in
+// [64 half + 32, 64 half + 64), so no thread writes columns another still reads. Per tile,
+// each softmax thread takes the row max of S_t, then folds O_{t-1} (PV_{t-1} ran meanwhile;
+// the fold frees the other buffer for S_{t+1}), then takes the exps and writes P_t.
 //
 // Launch shape (loop): one CTA per (context, head, 128-query tile) folds its key tiles in
 // registers. The split shape for a single query tile (enc_attn_split.cu) gives the same
-// bits: tiles are fixed by absolute position and folded in ascending order, and every
-// row's arithmetic comes from enc_common.cuh -- so a row's result depends only on its own
-// window, never on how the stream was cut into feeds, on when the ring was compacted, or
-// on the launch shape.
+// bits: tiles are fixed by absolute position and folded in ascending order, every row's
+// arithmetic comes from enc_common.cuh, and the P V product reads the same bf16 values
+// from tensor memory that the split shape reads from shared memory.
 #include "common.cuh"
 #include "enc_common.cuh"
 #include "ptx.cuh"
@@ -47,37 +56,42 @@ namespace vst {
 namespace {
 
 constexpr int kSoftmaxThreads = 256;               // warps 0-7: two threads per query row
-constexpr int kThreads = kSoftmaxThreads + 32;        // warp 8: TMA and MMA issue
+constexpr int kThreads = kSoftmaxThreads + 32;     // warp 8: TMA and MMA issue
 constexpr int kD = 64;
-constexpr int kDh = kD / 2;                            // output dims per thread
-constexpr uint32_t kTileBytes = 128u * 128u;           // 128 rows x 128 B
+constexpr int kDh = kD / 2;                        // output dims per thread
+constexpr uint32_t kTileBytes = 128u * 128u;       // 128 rows x 128 B
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;         // two K buffers
+constexpr uint32_t kOffK = kOffQ + kTileBytes;     // two K buffers
 constexpr uint32_t kOffV = kOffK + 2 * kTileBytes;
-constexpr uint32_t kOffP = kOffV + kTileBytes;         // two 64-key blocks
-constexpr uint32_t kOffRedM = kOffP + 2 * kTileBytes;  // float [2 tile parities][2 halves][128]
+constexpr uint32_t kOffCs = kOffV + kTileBytes;    // (cos, sin) rows of the queries: 128 x 256 B; once
+                                                   // Q' is rotated, its first 16 KB are V buffer 1
+constexpr uint32_t kOffRedM = kOffCs + 2 * kTileBytes;  // float [2 tile parities][2 halves][128]
 constexpr uint32_t kOffRedL = kOffRedM + 2 * 2 * 128 * 4;
 constexpr uint32_t kOffBar = kOffRedL + 2 * 2 * 128 * 4;
-constexpr int kNumBars = 13;
+constexpr int kNumBars = 14;
 constexpr uint32_t kSmemBytes = kOffBar + 8 * kNumBars + 1024;  // + slack to align the base to 1024
-constexpr uint32_t kTmemCols = 256;  // two 128-column buffers: S_t, then O_t in its first 64 columns
+constexpr uint32_t kTmemCols = 256;  // two 128-column buffers (S_t, then P_t and O_t)
+constexpr uint32_t kTmO = 32;        // output dims [32 h, 32 h + 32) at columns 64 h + kTmO of a buffer
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
-constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64, false, true);
+constexpr uint32_t kIdescO = idesc_bf16_f32(128, 32, false, true);
 
 // mbarriers (index = bit in the phase and pending masks)
 constexpr int kBarK = 0;      // 0, 1: K buffer landed (TMA)
-constexpr int kBarV = 2;      // V tile landed (TMA)
+constexpr int kBarV = 2;      // V buffer 0 landed (TMA); buffer 1: kBarV1
 constexpr int kBarS = 3;      // 3, 4: S in TMEM buffer ready (MMA commit)
 constexpr int kBarO = 5;      // 5, 6: O in TMEM buffer ready (MMA commit)
 constexpr int kBarFree = 7;   // 7, 8: O in TMEM buffer read by all eight softmax warps
 constexpr int kBarP = 9;      // 9, 10: P keys [64 half, 64 half + 64) written by the four warps of that half
 constexpr int kBarQ = 11;     // Q' written by all eight softmax warps
 constexpr int kBarQin = 12;   // raw queries and their (cos, sin) rows landed (TMA)
+constexpr int kBarV1 = 13;    // V buffer 1 landed (TMA)
 constexpr uint32_t kQinBytes = kTileBytes + 128u * kD * 4u;  // 128 query rows + 128 table rows
 
 }  // namespace
 
+// Two CTAs per SM: nine warps each, so one SM sub-partition holds five warps, which caps a
+// thread at 96 registers (5 x 32 x 96 of its 16,384).
 template <int J>
 __global__ void __launch_bounds__(kThreads, 2)
     enc_attn_kernel(const __grid_constant__ KParams<EncAttnCommon, EncAttnJob, J> p)
@@ -98,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     uint8_t* sQ = smem + kOffQ;
-    uint8_t* sP = smem + kOffP;
+    uint8_t* sCs = smem + kOffCs;
     float* red_m = reinterpret_cast<float*>(smem + kOffRedM);  // [parity][half][128]
     float* red_l = reinterpret_cast<float*>(smem + kOffRedL);
     const uint32_t bar0 = smem_u32(smem + kOffBar);
@@ -123,12 +137,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == 8) {
         // ================= control warp: TMA loads and MMA issue =================
-        // Key tile t uses TMEM buffer and K buffer (t - t_lo) & 1; V has one buffer. For tile t:
-        //   S_t done -> fetch K_{t+2} into the buffer K_t used
+        // Key tile t uses TMEM, K and V buffers (t - t_lo) & 1. For tile t:
         //   K_{t+1} landed, O_{t-1} read by every softmax warp -> S_{t+1} = Q' K_{t+1}^T
-        //   V_t landed, P_t keys [0, 64) written -> first four K steps of O_t = P_t V_t, into the
-        //   first 64 columns of S_t's buffer; P_t keys [64, 128) written -> the last four
-        //   O_t done -> fetch V_{t+1}
+        //   S_t done -> fetch K_{t+2} into the buffer K_t used
+        //   V_t landed, P_t keys [0, 64) written -> first four K steps of O_t dims [0, 32) = P_t V_t
+        //   (A from TMEM); P_t keys [64, 128) written -> the last four, then all eight of dims
+        //   [32, 64) (their accumulator overlays the scores of keys [96, 128))
+        //   O_t done -> fetch V_{t+2} into the buffer V_t used
         // The whole warp runs this code; the elected lane alone issues copies and MMAs.
         const uint32_t e = elect_one_sync();
         uint32_t ph = 0, pend = 0;  // pend: copies and MMAs started and not yet seen complete
@@ -150,12 +165,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             pend |= 1u << (kBarK + kb);
         };
+        auto v_buf = [&](long long t) { return smem_u32(smem + (((t - t_lo) & 1) ? kOffCs : kOffV)); };
+        auto v_bar = [&](long long t) { return ((t - t_lo) & 1) ? kBarV1 : kBarV; };
         auto issue_v = [&](long long t) {
             if (e) {
-                mbar_arrive_expect_tx(bar(kBarV), kTileBytes);
-                tma_load_3d(smem_u32(smem + kOffV), job.tmap_v, bar(kBarV), 0, (int)(t * 128 - job.abs_base), h);
+                mbar_arrive_expect_tx(bar(v_bar(t)), kTileBytes);
+                tma_load_3d(v_buf(t), job.tmap_v, bar(v_bar(t)), 0, (int)(t * 128 - job.abs_base), h);
             }
-            pend |= 1u << kBarV;
+            pend |= 1u << v_bar(t);
         };
         auto issue_s = [&](long long t) {
             const int b = (int)((t - t_lo) & 1);
@@ -167,19 +184,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             mma_commit_if(bar(kBarS + b), e);
             pend |= 1u << (kBarS + b);
         };
-        auto issue_pv = [&](long long t, int kh) {  // K steps [4 kh, 4 kh + 4): keys [64 kh, 64 kh + 64)
-            const int b = (int)((t - t_lo) & 1);
-            const uint32_t v = smem_u32(smem + kOffV);
+        // K steps [k0, k1) (keys [16 k0, 16 k1)) of output dims [32 nh, 32 nh + 32): A = P_t, whose
+        // keys [64 kh, 64 kh + 64) sit in columns [64 kh, 64 kh + 32) of the buffer, 16 keys per
+        // eight columns; B = V_t's dims [32 nh, 32 nh + 32) (64 bytes into each row)
+        auto issue_pv = [&](long long t, int nh, int kh) {  // K steps [4 kh, 4 kh + 4)
+            const uint32_t tb = tmem + 128u * (uint32_t)((t - t_lo) & 1);
+            const uint64_t vd = smem_desc_sw128(v_buf(t) + 8192 * kh + 64 * nh, kTileBytes, 1024);
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const int kk = 4 * kh + k4;
-                mma_bf16_ss_if(tmem + 128u * b, smem_desc_sw128(smem_u32(sP) + kh * kTileBytes + 32 * k4, 16, 1024),
-                               smem_desc_sw128(v + 2048 * kk, kTileBytes, 1024), kIdescO, kk > 0 ? 1u : 0u, e);
-            }
-            if (kh == 1) {
-                mma_commit_if(bar(kBarO + b), e);
-                pend |= 1u << (kBarO + b);
-            }
+            for (int k4 = 0; k4 < 4; ++k4)  // the descriptor's address field counts 16-byte units
+                mma_bf16_ts_if(tb + 64u * nh + kTmO, tb + 64u * kh + 8u * k4, vd + (uint64_t)(128 * k4), kIdescO,
+                               kh > 0 || k4 > 0 ? 1u : 0u, e);
         };
         auto issue_first = [&]() {
             issue_k(t_lo);
@@ -190,14 +204,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         // The first ring tiles may be requested before the previous kernel in the stream has
         // finished when the host says that kernel did not touch this ring (early). The rows of
-        // the constant (cos, sin) table go at once (into P, unused until the first exps), the
-        // queries once the previous kernel is done.
+        // the constant (cos, sin) table go at once, the queries once the previous kernel is done.
         if (e) {
             tmap_acquire(job.tmap_k);
             tmap_acquire(job.tmap_v);
             tmap_acquire(c.tmap_rope);
             mbar_arrive_expect_tx(bar(kBarQin), kQinBytes);
-            tma_load_2d(smem_u32(sP), c.tmap_rope, bar(kBarQin), 0, (int)p_first);
+            tma_load_2d(smem_u32(sCs), c.tmap_rope, bar(kBarQin), 0, (int)p_first);
         }
         pend |= 1u << kBarQin;  // waited by the softmax warps; here only after a failure
         if (c.early)
@@ -207,20 +220,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             tma_load_4d(smem_u32(sQ), &c.tmap_q, bar(kBarQin), 0, h, row0, job.q_z);
         if (!c.early)
             issue_first();
-        if (!wait(kBarQ) || !wait(kBarK))
+        if (!wait(kBarQ) || !wait(kBarK)) {
             fail = 1;
-        else
+        } else {
             issue_s(t_lo);
+            if (t_lo < t_hi)
+                issue_v(t_lo + 1);  // the (cos, sin) rows are no longer needed
+        }
 
         for (long long t = t_lo; !fail && t <= t_hi; ++t) {
             const int b = (int)((t - t_lo) & 1), nb = b ^ 1;
-            if (t + 2 <= t_hi) {
-                if (!wait(kBarS + b)) {
-                    fail = 1;
-                    break;
-                }
-                issue_k(t + 2);
-            }
             if (t < t_hi) {
                 if (!wait(kBarK + nb) || (t > t_lo && !wait(kBarFree + nb))) {
                     fail = 1;
@@ -229,24 +238,35 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc_fence_after();
                 issue_s(t + 1);
             }
-            if (!wait(kBarV) || !wait(kBarP)) {
+            if (t + 2 <= t_hi) {
+                if (!wait(kBarS + b)) {
+                    fail = 1;
+                    break;
+                }
+                issue_k(t + 2);
+            }
+            if (!wait(v_bar(t)) || !wait(kBarP)) {
                 fail = 1;
                 break;
             }
             tc_fence_after();
-            issue_pv(t, 0);
+            issue_pv(t, 0, 0);
             if (!wait(kBarP + 1)) {
                 fail = 1;
                 break;
             }
             tc_fence_after();
-            issue_pv(t, 1);
-            if (t < t_hi) {
+            issue_pv(t, 0, 1);
+            issue_pv(t, 1, 0);
+            issue_pv(t, 1, 1);
+            mma_commit_if(bar(kBarO + b), e);
+            pend |= 1u << (kBarO + b);
+            if (t + 2 <= t_hi) {
                 if (!wait(kBarO + b)) {
                     fail = 1;
                     break;
                 }
-                issue_v(t + 1);
+                issue_v(t + 2);
             }
         }
         if (fail) {
@@ -257,6 +277,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int i = 0; i < kBarFree; ++i)
                 if ((pend >> i) & 1u)
                     mbar_wait(bar(i), (ph >> i) & 1u);
+            if ((pend >> kBarV1) & 1u)
+                mbar_wait(bar(kBarV1), (ph >> kBarV1) & 1u);
             mbar_wait(bar(kBarQin), 0);
         }
         __syncwarp();
@@ -269,15 +291,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int half = warp >> 2;
         const int pair_bar = 1 + (warp & 3);   // named barrier of warps w and w + 4 (the same rows)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const long long pq = p_first + r;
         const bool row_real = r < nrows;
+        // keys relative to the query tile's first position: the batch's last key, and the first
+        // key of the current tile
+        const int kl = (int)(key_last - p_first);
+        int rel = (int)(t_lo * 128 - p_first);
 
         griddep_wait();
         // Raw query row r (zero past the batch) and its (cos, sin) row landed by TMA: rotate
         // this thread's two quarters in place.
         int qfail = mbar_wait(bar(kBarQin), 0) ? 0 : 1;
         if (!qfail) {
-            const float2* cs = reinterpret_cast<const float2*>(sP + r * (kD * 4));
+            const float2* cs = reinterpret_cast<const float2*>(sCs + r * (kD * 4));
             enc::rotate_quarter_in_place(sQ, cs, r, 2 * half);
             enc::rotate_quarter_in_place(sQ, cs, r, 2 * half + 1);
         }
@@ -294,7 +319,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         float mt_prev = -INFINITY;  // tile-local max of the previous tile, folded one tile late
         uint32_t ph = 0;
         int fail = qfail;
-        // o <- fold(o, O_t) for tile t in TMEM buffer b, with m_t = mt and l_t from red_l
+        // o <- fold(o, O_t) for the tile in TMEM buffer b, with m_t = mt and l_t from red_l
+        // (both halves' sums, ordered before this read by a pair barrier)
         auto fold_from = [&](int b, float mt) {
             if (mbar_wait(bar(kBarO + b), (ph >> (kBarO + b)) & 1u))
                 ph ^= 1u << (kBarO + b);
@@ -302,52 +328,62 @@ __global__ void __launch_bounds__(kThreads, 2)
                 fail = 1;
             tc_fence_after();
             const float lt = __fadd_rn(red_l[(b * 2 + 0) * 128 + r], red_l[(b * 2 + 1) * 128 + r]);
-            uint32_t ov[32];
-            tmem_ld_32x32b_x32(tmem + 128u * b + lane_base + kDh * half, ov);
-            tmem_ld_wait();
-            if (mt != -INFINITY) {
-                float ot[kDh];
+            // in two groups of 16 dims (the same operations per dim as one group of 32)
+            const enc::FoldCoef f = enc::fold_coef(m_run, mt);
 #pragma unroll
-                for (int d = 0; d < kDh; ++d)
-                    ot[d] = __uint_as_float(ov[d]);
-                enc::fold_tile<kDh>(m_run, l_run, o, mt, lt, ot);
+            for (int g = 0; g < 2; ++g) {
+                uint32_t ov[16];
+                tmem_ld_32x32b_x16(tmem + 128u * b + lane_base + 64 * half + kTmO + 16 * g, ov);
+                tmem_ld_wait();
+                if (mt != -INFINITY) {
+                    float ot[16];
+#pragma unroll
+                    for (int d = 0; d < 16; ++d)
+                        ot[d] = __uint_as_float(ov[d]);
+                    enc::fold_apply<16>(o + 16 * g, ot, f);
+                }
             }
+            if (mt != -INFINITY)
+                enc::fold_finish(m_run, l_run, lt, f);
         };
 
-        for (long long t = t_lo; t <= t_hi; ++t) {
+        for (long long t = t_lo; t <= t_hi; ++t, rel += 128) {
             const int b = (int)((t - t_lo) & 1), nb = b ^ 1;
-            const uint32_t tm_b = tmem + 128u * b + lane_base + 64 * half;
+
+            // ---- S_t: this thread's 64 columns of row r, as two quarters of 32
             if (mbar_wait(bar(kBarS + b), (ph >> (kBarS + b)) & 1u))
                 ph ^= 1u << (kBarS + b);
             else
                 fail = 1;
             tc_fence_after();
-
-            // ---- tile-local row max of this thread's half of row r, one quarter at a time
+            const uint32_t tm_s = tmem + 128u * b + lane_base + 64 * half;  // this thread's columns
             int lo = 1, hi = 0;  // visible columns of row r in this tile; empty unless r is real
             if (row_real) {
-                lo = (int)max(-1LL, min(128LL, pq - c.W + 1 - t * 128));
-                hi = (int)max(-1LL, min(128LL, min(pq + c.right, key_last) - t * 128));
+                lo = max(-1, min(128, r - c.W + 1 - rel));
+                hi = max(-1, min(128, min(r + c.right, kl) - rel));
             }
             const uint32_t mask0 = enc::visible_mask(64 * half, lo, hi), mask1 = enc::visible_mask(64 * half + 32, lo, hi);
+
+            // ---- tile-local row max of row r, one quarter at a time
             float mh;
             {
                 uint32_t sv[32];
-                tmem_ld_32x32b_x32(tm_b, sv);
+                tmem_ld_32x32b_x32(tm_s, sv);
                 tmem_ld_wait();
                 mh = enc::quarter_max(sv, mask0);
-                tmem_ld_32x32b_x32(tm_b + 32, sv);
+                tmem_ld_32x32b_x32(tm_s + 32, sv);
                 tmem_ld_wait();
                 mh = fmaxf(mh, enc::quarter_max(sv, mask1));
             }
             red_m[(b * 2 + half) * 128 + r] = mh;
-            if (bar_sync_or(pair_bar, 64, fail)) {
+            if (bar_sync_or(pair_bar, 64, fail)) {  // also orders the partner's l of the previous tile
                 aborted = 1;
                 break;
             }
             const float mt = __fmul_rn(fmaxf(red_m[(b * 2) * 128 + r], red_m[(b * 2 + 1) * 128 + r]), c.scale_log2);
 
-            // ---- fold of the previous tile (its PV ran while this tile's max was taken)
+            // ---- fold of the previous tile (its PV ran while this tile's max was taken); frees its
+            // buffer for S_{t+1}
             if (t > t_lo) {
                 fold_from(nb, mt_prev);
                 tc_fence_before();
@@ -356,27 +392,34 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mbar_arrive(bar(kBarFree + nb));
             }
 
-            // ---- tile-local exps (P of the previous tile has been consumed: its O is ready)
-            float lh;
+            // ---- tile-local exps, quarter by quarter (S_t read again); P_t over this thread's
+            // scores already read
+            float l0, l1;
             {
                 uint32_t sv[32];
-                tmem_ld_32x32b_x32(tm_b, sv);
+                tmem_ld_32x32b_x32(tm_s, sv);
                 tmem_ld_wait();
-                lh = enc::quarter_exp(sv, mask0, 2 * half, c.scale_log2, -mt, sP, r);
-                tmem_ld_32x32b_x32(tm_b + 32, sv);
+                l0 = enc::quarter_exp_to(sv, mask0, c.scale_log2, -mt,
+                                         [&](int qd, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+                                             tmem_st_32x32b_x4(tm_s + 4 * qd, w0, w1, w2, w3);
+                                         });
+                tmem_ld_32x32b_x32(tm_s + 32, sv);
                 tmem_ld_wait();
-                lh = __fadd_rn(lh, enc::quarter_exp(sv, mask1, 2 * half + 1, c.scale_log2, -mt, sP, r));
+                l1 = enc::quarter_exp_to(sv, mask1, c.scale_log2, -mt,
+                                         [&](int qd, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+                                             tmem_st_32x32b_x4(tm_s + 16 + 4 * qd, w0, w1, w2, w3);
+                                         });
             }
-            red_l[(b * 2 + half) * 128 + r] = lh;
-            fence_proxy_async_smem();  // P (generic stores) before the MMA reads it
-            tc_fence_before();         // and S_t read before O_t overwrites it
+            red_l[(b * 2 + half) * 128 + r] = __fadd_rn(l0, l1);
+            tmem_st_wait();
+            tc_fence_before();  // P_t written (and S_t read) before the MMAs use the columns
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar(kBarP + half));
             mt_prev = mt;
         }
         // ---- fold of the last tile
-        if (bar_sync_or(pair_bar, 64, fail))  // also orders red_l of the last tile
+        if (!aborted && bar_sync_or(pair_bar, 64, fail))  // orders the partner's l of the last tile
             aborted = 1;
         if (!aborted) {
             fold_from((int)((t_hi - t_lo) & 1), mt_prev);

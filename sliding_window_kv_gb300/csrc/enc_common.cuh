@@ -55,7 +55,7 @@ __device__ __forceinline__ float max32(const float (&x)[32])
 // Max over the visible columns (bit j of `mask` for column j) of a quarter held in sv.
 // Called by whole warps: the branch between the all-visible path and the per-column selects
 // is taken for the whole warp at once (the selects give the same value when every bit is set).
-__device__ __forceinline__ float quarter_max(const uint32_t (&sv)[32], uint32_t mask)
+__device__ __forceinline__ float quarter_max(const uint32_t* sv, uint32_t mask)
 {
     if (__all_sync(0xffffffffu, mask == 0u))
         return -INFINITY;
@@ -72,18 +72,19 @@ __device__ __forceinline__ float quarter_max(const uint32_t (&sv)[32], uint32_t 
     return max32(x);
 }
 
-// Probabilities of quarter q (columns [32 q, 32 q + 32)) of row `row` (neg = -m_t), visible
-// columns in `mask`: written as bf16 into the K-major P operand (two 64-key blocks, 128-B
-// swizzle); returns the quarter sum. Columns are taken in ascending order, eight at a time;
-// a hidden column is 0. Called by whole warps (the branches are taken warp by warp).
-__device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], uint32_t mask, int q, float scale_log2,
-                                             float neg, uint8_t* sP, int row)
+// Probabilities of a quarter (32 columns, neg = -m_t), visible columns in `mask`, as bf16
+// pairs handed to `sink(qd, w0, w1, w2, w3)` eight columns at a time: w_i holds columns
+// 8 qd + 2i (low half) and 8 qd + 2i + 1; returns the quarter sum. Columns are taken in
+// ascending order; a hidden column is 0. Called by whole warps (the branches are taken warp
+// by warp).
+template <class Sink>
+__device__ __forceinline__ float quarter_exp_to(const uint32_t* sv, uint32_t mask, float scale_log2, float neg,
+                                                Sink&& sink)
 {
     if (__all_sync(0xffffffffu, mask == 0u)) {  // nothing visible: P = 0 and the sum is 0, as below
 #pragma unroll
         for (int qd = 0; qd < 4; ++qd)
-            *reinterpret_cast<uint4*>(sP + (q >> 1) * kTileBytes + sw128_offset(row, (q & 1) * 4 + qd)) =
-                make_uint4(0u, 0u, 0u, 0u);
+            sink(qd, 0u, 0u, 0u, 0u);
         return 0.f;
     }
     // Paired fp32 operations (__ffma2_rn, __fadd2_rn) round each lane exactly as the scalar
@@ -109,11 +110,20 @@ __device__ __forceinline__ float quarter_exp(const uint32_t (&sv)[32], uint32_t 
         l23 = __fadd2_rn(l23, make_float2(pv[2], pv[3]));
         l01 = __fadd2_rn(l01, make_float2(pv[4], pv[5]));
         l23 = __fadd2_rn(l23, make_float2(pv[6], pv[7]));
-        const uint4 w = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
-                                   pack_bf16(pv[6], pv[7]));
-        *reinterpret_cast<uint4*>(sP + (q >> 1) * kTileBytes + sw128_offset(row, (q & 1) * 4 + qd)) = w;
+        sink(qd, pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
     }
     return __fadd_rn(__fadd_rn(l01.x, l01.y), __fadd_rn(l23.x, l23.y));
+}
+
+// The same for quarter q (columns [32 q, 32 q + 32)) of row `row`, written as bf16 into the
+// K-major P operand in shared memory (two 64-key blocks, 128-B swizzle).
+__device__ __forceinline__ float quarter_exp(const uint32_t* sv, uint32_t mask, int q, float scale_log2, float neg,
+                                             uint8_t* sP, int row)
+{
+    return quarter_exp_to(sv, mask, scale_log2, neg, [&](int qd, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+        *reinterpret_cast<uint4*>(sP + (q >> 1) * kTileBytes + sw128_offset(row, (q & 1) * 4 + qd)) =
+            make_uint4(w0, w1, w2, w3);
+    });
 }
 
 // Merge of a tile-local softmax state (mt, lt, ot) into a running state (m, l, o):

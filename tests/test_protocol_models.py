@@ -46,20 +46,29 @@ def _expect(cond, msg):
 # ---------------------------------------------------------------- loop shape (enc_attn.cu)
 
 def loop_shape_run(n, seed, mistake=None, n_warps=8):
-    """One CTA over n key tiles. Control warp: K double-buffered two tiles ahead, one V
-    buffer, S of tile t+1 into the other TMEM buffer once O of tile t-1 there has been read
-    by every softmax warp, PV of tile t in two key halves as each half of P lands, then V of
-    tile t+1 once O of tile t is done. Softmax warps (two per query row, half h owning score
-    columns [64h, 64h+64)): row max of S_t, exchange with the partner warp, fold O_{t-1},
-    exps of S_t into P. PV's first half writes O into the first 64 columns of S_t's buffer,
-    which only half 0 reads."""
+    """One CTA over n key tiles. Tile t uses TMEM buffer, K buffer and V buffer t & 1; V
+    buffer 1 is the shared memory that first holds the queries' (cos, sin) rows. In each TMEM
+    buffer the columns [64h, 64h+64) of half h hold, for each warp of that half (its own
+    lanes), quarter 0 and quarter 1 of its scores S_t; P_t is written over quarter 0 and
+    O_t (output dims [32h, 32h+32)) over quarter 1.
+    Control warp: K two tiles ahead (once S of the tile that used the buffer is done); V_0
+    early, V_1 once every softmax warp has rotated its queries; S of tile t+1 once O of tile
+    t-1 in that buffer has been read by every softmax warp; PV of tile t: dims [0, 32) with
+    keys [0, 64) once half 0's P lands, then with keys [64, 128) and dims [32, 64) with all
+    keys once half 1's P lands; V of tile t+2 once O of tile t is done.
+    Softmax warps: rotate the queries (reading the (cos, sin) rows); per tile: read both
+    score quarters (row max), exchange with the partner warp, fold O_{t-1}, read quarter 0
+    again and write P over it, read quarter 1 again and write the rest of P over quarter 0."""
     rng = random.Random(seed)
-    bars = {k: Barrier(1) for k in ("K0", "K1", "V", "S0", "S1", "O0", "O1")}
+    bars = {k: Barrier(1) for k in ("K0", "K1", "V0", "V1", "S0", "S1", "O0", "O1")}
     for k in ("F0", "F1", "Q"):
         bars[k] = Barrier(n_warps)
     bars["P0"], bars["P1"] = Barrier(n_warps // 2), Barrier(n_warps // 2)
-    mem = {"K0": None, "K1": None, "V": None, "O0": None, "O1": None,
-           "S0h0": None, "S0h1": None, "S1h0": None, "S1h1": None, "P": [None] * n_warps, "Q": [False] * n_warps}
+    hw = n_warps // 2
+    mem = {"K0": None, "K1": None, "V0": None, "V1": "cs", "Q": [False] * n_warps}
+    for b in range(2):
+        for w in range(n_warps):
+            mem["q0_%d_%d" % (b, w)] = mem["q1_%d_%d" % (b, w)] = None
     copies, mmas = [], []  # copies land in any order; the tensor pipe runs its queue in order
 
     def control():
@@ -73,63 +82,80 @@ def loop_shape_run(n, seed, mistake=None, n_warps=8):
             copies.append(("K%d" % (t & 1), t))
 
         def fetch_v(t):
-            copies.append(("V", t))
+            copies.append(("V%d" % (t & 1), t))
 
         fetch_k(0)
         if n > 1:
             fetch_k(1)
         fetch_v(0)
+        if mistake == "v1_before_rotation" and n > 1:
+            fetch_v(1)
         yield wait("Q")
         yield wait("K0")
         mmas.extend([("S", 0), ("commit", "S0")])
+        if n > 1 and mistake != "v1_before_rotation":
+            fetch_v(1)
         for t in range(n):
             b, nb = t & 1, (t & 1) ^ 1
-            if t + 2 <= n - 1:
-                if mistake != "k_before_s_done":
-                    yield wait("S%d" % b)
-                fetch_k(t + 2)
             if t < n - 1:
                 yield wait("K%d" % nb)
                 if t > 0 and mistake != "s_before_o_read":
                     yield wait("F%d" % nb)
                 mmas.extend([("S", t + 1), ("commit", "S%d" % nb)])
-            yield wait("V")
+            if t + 2 <= n - 1:
+                if mistake != "k_before_s_done":
+                    yield wait("S%d" % b)
+                fetch_k(t + 2)
+            yield wait("V%d" % b)
             yield wait("P0")
-            mmas.append(("PV0", t))
+            mmas.append(("PV", t, 0, 0))
+            if mistake == "pv_dims_hi_before_p1":
+                mmas.append(("PV", t, 1, 0))
             yield wait("P1")
-            mmas.extend([("PV1", t), ("commit", "O%d" % b)])
-            if t < n - 1:
+            mmas.append(("PV", t, 0, 1))
+            if mistake != "pv_dims_hi_before_p1":
+                mmas.append(("PV", t, 1, 0))
+            mmas.extend([("PV", t, 1, 1), ("commit", "O%d" % b)])
+            if t + 2 <= n - 1:
                 if mistake != "v_before_o_done":
                     yield wait("O%d" % b)
-                fetch_v(t + 1)
+                fetch_v(t + 2)
 
     def softmax(w):
         ph = dict.fromkeys(bars, 0)
-        half, pair = w // (n_warps // 2), w % (n_warps // 2)
+        half, pair = w // hw, w % hw
 
         def wait(k):
             ph[k] ^= 1
             return ("wait", k, ph[k] ^ 1)
 
+        def expect(key, want, what):
+            return ("do", lambda: _expect(mem[key] == want, "%s of warp %d reads %s = %s, not %s"
+                                          % (what, w, key, mem[key], want)))
+
+        yield expect("V1", "cs", "rotation")  # the (cos, sin) rows, not a V tile yet
         yield ("do", lambda: mem["Q"].__setitem__(w, True))  # queries rotated in place
         yield ("arrive", "Q")
         for t in range(n):
             b, nb = t & 1, (t & 1) ^ 1
-            s = "S%dh%d" % (b, half)
+            q0, q1 = "q0_%d_%d" % (b, w), "q1_%d_%d" % (b, w)
             yield wait("S%d" % b)
-            yield ("do", lambda t=t, s=s: _expect(mem[s] == t, "row max of warp %d reads %s = %s, not tile %d" % (w, s, mem[s], t)))
+            yield expect(q0, ("S", t), "row max")
+            yield expect(q1, ("S", t), "row max")
             yield ("group", pair, t, 2)
             if t > 0:
                 yield wait("O%d" % nb)
-                yield ("do", lambda t=t, nb=nb: _expect(mem["O%d" % nb] == t - 1, "fold of warp %d reads O%d = %s, not tile %d" % (w, nb, mem["O%d" % nb], t - 1)))
+                yield expect("q1_%d_%d" % (nb, w), ("O", t - 1), "fold")
                 yield ("arrive", "F%d" % nb)
-            yield ("do", lambda t=t, s=s: _expect(mem[s] == t, "exps of warp %d read %s = %s, not tile %d" % (w, s, mem[s], t)))
-            yield ("do", lambda t=t: mem["P"].__setitem__(w, t))
+            yield expect(q0, ("S", t), "exps")
+            yield ("do", lambda q0=q0, t=t: mem.__setitem__(q0, ("Pa", t)))
+            yield expect(q1, ("S", t), "exps")
+            yield ("do", lambda q0=q0, t=t: mem.__setitem__(q0, ("P", t)))
             yield ("arrive", "P%d" % half)
         yield ("group", pair, n, 2)
         last = (n - 1) & 1
         yield wait("O%d" % last)
-        yield ("do", lambda: _expect(mem["O%d" % last] == n - 1, "last fold of warp %d reads O = %s" % (w, mem["O%d" % last])))
+        yield expect("q1_%d_%d" % (last, w), ("O", n - 1), "last fold")
 
     def run_mma(op):
         if op[0] == "commit":
@@ -140,18 +166,17 @@ def loop_shape_run(n, seed, mistake=None, n_warps=8):
         if op[0] == "S":
             _expect(mem["K%d" % b] == t, "S of tile %d reads K%d = %s" % (t, b, mem["K%d" % b]))
             _expect(all(mem["Q"]), "S issued before every query row was rotated")
-            mem["S%dh0" % b] = mem["S%dh1" % b] = t
-            mem["O%d" % b] = None
-        elif op[0] == "PV0":
-            _expect(mem["V"] == t, "PV of tile %d reads V = %s" % (t, mem["V"]))
-            _expect(all(p == t for p in mem["P"][:n_warps // 2]), "PV0 of tile %d reads P = %s" % (t, mem["P"]))
-            mem["S%dh0" % b] = None  # O overwrites the score columns of half 0
-            mem["O%d" % b] = ("half", t)
-        else:
-            _expect(mem["V"] == t, "PV1 of tile %d reads V = %s" % (t, mem["V"]))
-            _expect(all(p == t for p in mem["P"][n_warps // 2:]), "PV1 of tile %d reads P = %s" % (t, mem["P"]))
-            _expect(mem["O%d" % b] == ("half", t), "PV halves of tile %d out of order" % t)
-            mem["O%d" % b] = t
+            for w in range(n_warps):
+                mem["q0_%d_%d" % (b, w)] = mem["q1_%d_%d" % (b, w)] = ("S", t)
+            return
+        _, t, nh, kh = op  # dims [32 nh, 32 nh + 32), keys [64 kh, 64 kh + 64)
+        _expect(mem["V%d" % b] == t, "PV of tile %d reads V%d = %s" % (t, b, mem["V%d" % b]))
+        for w in range(kh * hw, kh * hw + hw):
+            key = "q0_%d_%d" % (b, w)
+            _expect(mem[key] == ("P", t), "PV of tile %d reads P from %s = %s" % (t, key, mem[key]))
+        for w in range(nh * hw, nh * hw + hw):  # the accumulator overlays quarter 1 of half nh
+            key = "q1_%d_%d" % (b, w)
+            mem[key] = ("Opart", t) if kh == 0 else (("O", t) if mem[key] == ("Opart", t) else ("bad", t))
 
     agents = {"control": control()}
     agents.update(("warp%d" % w, softmax(w)) for w in range(n_warps))
@@ -204,7 +229,8 @@ def test_loop_shape_protocol(n_tiles):
         loop_shape_run(n_tiles, 1000 * n_tiles + seed)
 
 
-@pytest.mark.parametrize("mistake", ["k_before_s_done", "s_before_o_read", "v_before_o_done"])
+@pytest.mark.parametrize("mistake", ["k_before_s_done", "s_before_o_read", "v_before_o_done", "v1_before_rotation",
+                                     "pv_dims_hi_before_p1"])
 def test_loop_shape_model_catches_planted_mistakes(mistake):
     caught = 0
     for seed in range(200):
