@@ -820,7 +820,7 @@ def workload_config(name, spec):
         "l2": "KV cache read per step larger than L2 (no flush)"}
 
 
-def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu, e2e=False):
+def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu, e2e=False, workload="dec_b1"):
     import torch
     from sliding_window_kv_gb300 import vst
     w = DecWorkload(spec, dev, n_steps, dist.rank)
@@ -843,7 +843,8 @@ def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu, e2e=Fal
            "ms_per_step": ms / w.steps, "gpu_launches": launches,
            "roofline": {"kernel": "dec_step_kernel", "bound": "hbm", "achieved": achieved, "peak": hbm,
                         "unit": "GB/s", "frac": achieved / hbm,
-                        "traffic": dram_traffic("dec_step_kernel", bytes_per_launch),
+                        "traffic": dram_traffic("dec_step_kernel", bytes_per_launch, workload,
+                                                fallback=workload == "dec_b1"),
                         "peak_source": src, "launches": nl, "avg_launch_us": launch_us,
                         "isolated_launch_us": 1e3 * kms / nl, "timing": TIMING_NOTE,
                         "algorithmic_bytes_per_launch": bytes_per_launch}}
@@ -1004,7 +1005,7 @@ def bench_enc(spec, dev, stream, dist, steps, warmup, peaks, workload, e2e=True,
                              "avg_launch_us": cus, "isolated_launch_us": 1e3 * cms / ncmp,
                              "timing": TIMING_NOTE, "algorithmic_bytes_per_launch": cb,
                              "achieved_gbs": cb / (cus / 1e6) / 1e9, "frac": cb / (cus / 1e6) / 1e9 / hbm,
-                             "traffic": dram_traffic("compact_kernel", cb, workload, fallback=False)}
+                             "traffic": dram_traffic("compact_kernel", cb, workload, fallback=workload == "enc_stream")}
 
     if e2e:
         est = w.e2e_setup(stream)
@@ -1087,7 +1088,7 @@ def run_vst(args, dist):
         with torch.cuda.stream(stream):
             sampler.start()
             d = bench_dec(spec, dev, stream, dist, spec["steps"], args.warmup, peaks, want_cpu_baseline(args, dist),
-                          e2e=not args.no_e2e)
+                          e2e=not args.no_e2e, workload=args.workload)
             clocks = sampler.stop()
         line.update({"value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"], "config": d["config"],
                      "roofline": d["roofline"], "gpu_launches": d["gpu_launches"], "clocks": clocks})
@@ -1124,7 +1125,7 @@ def run_vst(args, dist):
             dspec64 = dict(WORKLOADS["dec_b64"])
             dspec64["steps"] = args.dec_steps
             line["dec_b64"] = timed(lambda: bench_dec(dspec64, dev, stream, dist, args.dec_steps, args.warmup, peaks,
-                                                      want_cpu_baseline(args, dist)))
+                                                      want_cpu_baseline(args, dist), workload="dec_b64"))
             line["enc_long16"] = timed(lambda: bench_enc(dict(WORKLOADS["enc_long16"]), dev, stream, dist,
                                                          args.steps, args.warmup, peaks, "enc_long16", e2e=False,
                                                          want_cpu=want_cpu_baseline(args, dist)))

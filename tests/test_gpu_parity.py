@@ -52,7 +52,15 @@ def _compare(gpu_out, want, tag=""):
     assert np.isfinite(got).all(), tag
     assert d.max() <= MAX_TOL, "%s max|d| %.3e" % (tag, d.max())
     assert d.mean() <= MEAN_TOL, "%s mean|d| %.3e" % (tag, d.mean())
+    _report(tag or "whole output", [d])
     return d.max(), d.mean()
+
+
+def _report(tag, ds):
+    """Print the worst max|d| and the mean|d| over every sampled element (pytest -s shows it)."""
+    if ds:
+        allv = np.concatenate([x.ravel() for x in ds])
+        print("parity %s: %d rows, max|d| %.3e, mean|d| %.3e" % (tag, len(ds), allv.max(), allv.mean()))
 
 
 def _feed(module, q, k, v, chunks, compact_before=(), dev="cuda"):
@@ -152,11 +160,14 @@ def test_enc_long_stream_parity_sampled(dev, enc_module):
     qb, kb, vb = synth.bits(q), synth.bits(k), synth.bits(v)
     rows = [0, 1, 749, 750, 1499, 1500, 1536, 2287, 3333, 4999]
     got = out.float().cpu().double().numpy()
+    ds = []
     for i in rows:
         j0 = max(0, i - 749)
         want = oracle.attention_row(qb[i], kb[j0:i + 1], vb[j0:i + 1], i, 750)
         d = np.abs(got[i] - want)
+        ds.append(d)
         assert d.max() <= MAX_TOL and d.mean() <= MEAN_TOL, (i, d.max(), d.mean())
+    _report("5000 frames in 50-frame feeds", ds)
 
 
 class TorchCtx:
@@ -238,6 +249,7 @@ def test_enc_batch_compaction_ring_bytes(dev, enc_module):
     vst.enc_feed_batch([c.handle for c in fused], Q, K, V, OUT, b)
     torch.cuda.synchronize()
     got = OUT.float().cpu().double().numpy()
+    ds = []
     for s in range(3):
         ref = prefilled(s)
         if fills[s] + b > 1536:
@@ -257,8 +269,10 @@ def test_enc_batch_compaction_ring_bytes(dev, enc_module):
             j0 = max(0, p - 749)
             want = oracle.attention_row(qb[p], kb[j0:p + 1], vb[j0:p + 1], p, 750)
             d = np.abs(got[s, i] - want)
+            ds.append(d)
             assert d.max() <= MAX_TOL and d.mean() <= MEAN_TOL, (s, i, d.max(), d.mean())
         ref.close()
+    _report("batched compaction rows", ds)
     for c in fused:
         c.close()
 
@@ -329,13 +343,16 @@ def test_enc_16_unstaggered_streams_512_batches(dev, enc_module):
         info = c.info()
         assert (info.n_kv, info.abs_base, info.abs_next, info.n_compactions) == (1262, 786, 2048, 1)
     got = OUT.float().cpu().double().numpy()
+    ds = []
     for s in (0, 7, 15):
         qb, kb, vb = (synth.bits(x) for x in seqs[s])
         for i in (0, 127, 128, 511, 512, 1535, 1536, 1663, 2047):
             j0 = max(0, i - 749)
             want = oracle.attention_row(qb[i], kb[j0:i + 1], vb[j0:i + 1], i, 750)
             d = np.abs(got[s, i] - want)
+            ds.append(d)
             assert d.max() <= MAX_TOL and d.mean() <= MEAN_TOL, (s, i, d.max(), d.mean())
+    _report("16 streams from position 0, 512-frame batches", ds)
     alone, _ = _feed(enc_module, *seqs[0], [50] * (T // 50) + [T % 50])
     assert torch.equal(alone, OUT[0])
     for c in ctxs:
@@ -368,6 +385,7 @@ def test_enc_16_streams_512_batches(dev, enc_module):
         assert vst.ctx_check(ctxs[s].handle) == vst.OK
         assert ctxs[s].info().abs_next == offsets[s] + T
     got = OUT.float().cpu().double().numpy()
+    ds = []
     for s in (0, 5, 15):
         qb, kb, vb = (synth.bits(x) for x in seqs[s])
         for i in (0, 1, 511, 512, 1023, 1024, 1535):
@@ -375,7 +393,9 @@ def test_enc_16_streams_512_batches(dev, enc_module):
             j0 = max(0, p - 749)
             want = oracle.attention_row(qb[p], kb[j0:p + 1], vb[j0:p + 1], p, 750)
             d = np.abs(got[s, i] - want)
+            ds.append(d)
             assert d.max() <= MAX_TOL and d.mean() <= MEAN_TOL, (s, i, d.max(), d.mean())
+    _report("16 staggered streams, 512-frame batches", ds)
     s = 7
     alone, _ = _feed(enc_module, *seqs[s], [offsets[s]] + [50] * (T // 50) + [T % 50])
     assert torch.equal(alone[offsets[s]:], OUT[s])
