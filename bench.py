@@ -414,6 +414,23 @@ class EncWorkload:
         self.module.close()
 
 
+def host_enqueue_cost(calls, burst=256):
+    """Host time of a list of prepared C-ABI calls (fn, args), issued in bursts of `burst`
+    calls after a synchronisation so that no call waits for room in the launch queue:
+    (total ms, µs per call)."""
+    import torch
+    total = 0.0
+    for i in range(0, len(calls), burst):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for fn, args in calls[i:i + burst]:
+            if fn(*args) != 0:
+                raise RuntimeError("%s failed" % fn.__name__)
+        total += time.perf_counter() - t0
+    torch.cuda.synchronize()
+    return 1e3 * total, 1e6 * total / max(1, len(calls))
+
+
 class DecWorkload:
     """26 decoder layers; each stream's cache filled (untimed) then `steps` decoder steps.
     Inputs of step t, layer l are [S][H][D] / [S][Hk][D] slices of per-layer buffers."""
@@ -867,9 +884,13 @@ def bench_dec(spec, dev, stream, dist, n_steps, warmup, peaks, want_cpu, e2e=Fal
         wall = time.perf_counter() - t0
         dist.barrier()
         e2e_value, _ = dist.job_rate(w.steps, a.elapsed_time(b))
+        calls = [c for t in est["calls"] for c in t]  # the steps once more, timed on the host alone
+        host_ms, host_us = host_enqueue_cost(calls)
         out["e2e"] = {"value": e2e_value, "unit": "dec steps/s",
                       "h2d_bytes_per_step": est["h2d"] / w.steps, "d2h_bytes_per_step": est["d2h"] / w.steps,
                       "steps": w.steps, "host_wall_s": wall,
+                      "host_enqueue_ms_per_step": host_ms / w.steps, "host_us_per_call": host_us,
+                      "calls_per_step": len(calls) / w.steps,
                       "path": "vst_dec_step per layer and step through the C ABI (no graph); each step's inputs "
                               "(all layers) copied host to device in one copy on a copy stream, its outputs back "
                               "on a third stream, one cross-stream wait per 8 steps, pinned memory, all inside "
@@ -1025,9 +1046,14 @@ def bench_enc(spec, dev, stream, dist, steps, warmup, peaks, workload, e2e=True,
         wall = time.perf_counter() - t0
         dist.barrier()
         e2e_value, _ = dist.job_rate(w.frames_per_step * e2e_steps, a.elapsed_time(b))
+        # one more step's calls (context resets first), timed on the host alone
+        calls = list(est["resets"]) + [c for f in est["calls"] for c in f]
+        host_ms, host_us = host_enqueue_cost(calls)
+        n_calls = len(calls)
         out["e2e"] = {"value": e2e_value, "unit": "enc frames/s",
                       "h2d_bytes_per_step": est["h2d"], "d2h_bytes_per_step": est["d2h"],
                       "steps": e2e_steps, "host_wall_s": wall,
+                      "host_enqueue_ms_per_step": host_ms, "host_us_per_call": host_us, "calls_per_step": n_calls,
                       "path": "vst_enc_feed per layer and feed through the C ABI (no graph); each feed's "
                               "inputs copied host to device in one copy on a copy stream, its outputs back "
                               "on a third stream, one cross-stream wait per 8 feeds, pinned memory, all "

@@ -118,44 +118,65 @@ def _check(s: int, what: str):
         raise VstError(s, what)
 
 
-def _ptr(t) -> int:
+_torch = None
+_raw_stream = None  # (getter of the current stream's handle for a device index, current device index)
+
+
+def _t():
+    global _torch
+    if _torch is None:
+        import torch
+        _torch = torch
+    return _torch
+
+
+def _p(t, n_elems: int, name: str, bf16) -> int:
+    """Data pointer of a contiguous bf16 CUDA tensor holding at least n_elems elements; a raw
+    integer pointer passes through (the caller's responsibility) and None gives 0."""
     if t is None:
         return 0
-    if isinstance(t, int):  # a raw device pointer
+    if isinstance(t, int):
         return t
-    import torch
-    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-        raise ValueError("expected a contiguous bf16 CUDA tensor")
+    if t.dtype is not bf16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s: expected a contiguous bf16 CUDA tensor" % name)
+    if t.numel() < n_elems:
+        raise ValueError("%s: %d elements, the call needs %d" % (name, t.numel(), n_elems))
     return t.data_ptr()
+
+
+def _ptr(t) -> int:
+    return _p(t, 0, "tensor", _t().bfloat16)
 
 
 # ctx handle -> its module's config, for the size checks below (filled by ctx_create)
 _ctx_cfg: dict = {}
 
 
-def _need(t, n_elems: int, name: str):
-    """Refuse a tensor holding fewer elements than the call reads or writes from its pointer
-    (raw integer pointers are the caller's responsibility)."""
-    if t is None or isinstance(t, int):
-        return
-    if t.numel() < n_elems:
-        raise ValueError("%s: %d elements, the call needs %d" % (name, t.numel(), n_elems))
-
-
-def _need_io(cfg, rows: int, q, k, v, out):
-    """q and out hold `rows` rows of [H][D], k and v `rows` rows of [Hk][D]."""
-    if cfg is None:
-        return
-    hq, hk = rows * cfg.n_heads * cfg.head_dim, rows * cfg.n_kv_heads * cfg.head_dim
-    _need(q, hq, "q")
-    _need(k, hk, "k")
-    _need(v, hk, "v")
-    _need(out, hq, "out")
+def _io(cfg, rows: int, q, k, v, out):
+    """Pointers of q, k, v and out after the checks of _p: q and out hold `rows` rows of
+    [H][D], k and v `rows` rows of [Hk][D] (sizes unchecked when the config is unknown)."""
+    bf16 = _t().bfloat16
+    hq = hk = 0
+    if cfg is not None:
+        hq = rows * cfg.n_heads * cfg.head_dim
+        hk = rows * cfg.n_kv_heads * cfg.head_dim
+    return _p(q, hq, "q", bf16), _p(k, hk, "k", bf16), _p(v, hk, "v", bf16), _p(out, hq, "out", bf16)
 
 
 def _stream(stream) -> int:
+    """Handle of `stream` (a torch stream or a raw handle); None: torch's current stream on
+    the current device."""
+    global _raw_stream
     if stream is None:
-        import torch
+        torch = _t()
+        if _raw_stream is None:
+            h = torch.cuda.current_stream().cuda_stream  # also initialises CUDA
+            get = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+            dev = getattr(torch._C, "_cuda_getDevice", None)
+            _raw_stream = (get, dev) if get is not None and dev is not None else False
+            return h
+        if _raw_stream:
+            return _raw_stream[0](_raw_stream[1]())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
@@ -220,8 +241,8 @@ def ctx_selftest_wait(c: int, complete: bool, stream=None):
 
 def enc_feed(c: int, q, k, v, out, stream=None, n_new: int | None = None):
     n = q.shape[0] if n_new is None else n_new
-    _need_io(_ctx_cfg.get(c), n, q, k, v, out)
-    _check(lib().vst_enc_feed(c, _ptr(q), _ptr(k), _ptr(v), n, _ptr(out), _stream(stream)), "vst_enc_feed")
+    pq, pk, pv, po = _io(_ctx_cfg.get(c), n, q, k, v, out)
+    _check(lib().vst_enc_feed(c, pq, pk, pv, n, po, _stream(stream)), "vst_enc_feed")
 
 
 def _handles(ctxs):
@@ -231,8 +252,8 @@ def _handles(ctxs):
 
 def enc_feed_batch(ctxs, q, k, v, out, n_new: int, stream=None):
     h, keep = _handles(ctxs)
-    _need_io(_ctx_cfg.get(ctxs[0]) if ctxs else None, len(ctxs) * n_new, q, k, v, out)
-    _check(lib().vst_enc_feed_batch(h, len(ctxs), _ptr(q), _ptr(k), _ptr(v), n_new, _ptr(out), _stream(stream)),
+    pq, pk, pv, po = _io(_ctx_cfg.get(ctxs[0]) if ctxs else None, len(ctxs) * n_new, q, k, v, out)
+    _check(lib().vst_enc_feed_batch(h, len(ctxs), pq, pk, pv, n_new, po, _stream(stream)),
            "vst_enc_feed_batch")
 
 
@@ -264,24 +285,24 @@ def enc_launch_shape(n_heads: int, n_ctx: int, batch: int, max_key_tiles: int, r
 
 def dec_step(ctxs, q, k, v, out, stream=None):
     h, keep = _handles(ctxs)
-    _need_io(_ctx_cfg.get(ctxs[0]) if ctxs else None, len(ctxs), q, k, v, out)
-    _check(lib().vst_dec_step(h, len(ctxs), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream)),
+    pq, pk, pv, po = _io(_ctx_cfg.get(ctxs[0]) if ctxs else None, len(ctxs), q, k, v, out)
+    _check(lib().vst_dec_step(h, len(ctxs), pq, pk, pv, po, _stream(stream)),
            "vst_dec_step")
 
 
 def dec_step_noalloc(ctxs, q, k, v, out, stream=None):
     """vst_dec_step with its scratch in the library's static device array (no allocation)."""
     h, keep = _handles(ctxs)
-    _need_io(_ctx_cfg.get(ctxs[0]) if ctxs else None, len(ctxs), q, k, v, out)
-    _check(lib().vst_dec_step_noalloc(h, len(ctxs), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream)),
+    pq, pk, pv, po = _io(_ctx_cfg.get(ctxs[0]) if ctxs else None, len(ctxs), q, k, v, out)
+    _check(lib().vst_dec_step_noalloc(h, len(ctxs), pq, pk, pv, po, _stream(stream)),
            "vst_dec_step_noalloc")
 
 
 def dec_prefill(c: int, q, k, v, out, n: int | None = None, stream=None):
     """vst_dec_prefill: n tokens of one decoder ctx, q/out [n][H][D], k/v [n][Hk][D]."""
     n = q.shape[0] if n is None else n
-    _need_io(_ctx_cfg.get(c), n, q, k, v, out)
-    _check(lib().vst_dec_prefill(c, _ptr(q), _ptr(k), _ptr(v), n, _ptr(out), _stream(stream)), "vst_dec_prefill")
+    pq, pk, pv, po = _io(_ctx_cfg.get(c), n, q, k, v, out)
+    _check(lib().vst_dec_prefill(c, pq, pk, pv, n, po, _stream(stream)), "vst_dec_prefill")
 
 
 class Offline:
@@ -294,9 +315,8 @@ class Offline:
 
     def run(self, q, k, v, out, left: int, right: int = 0, stream=None):
         """vst_enc_offline: q, k, v, out [B][T][H][D]."""
-        _need_io(self.cfg, self.B * self.T, q, k, v, out)
-        _check(lib().vst_enc_offline(self.handle, _ptr(q), _ptr(k), _ptr(v), left, right, _ptr(out),
-                                     _stream(stream)), "vst_enc_offline")
+        pq, pk, pv, po = _io(self.cfg, self.B * self.T, q, k, v, out)
+        _check(lib().vst_enc_offline(self.handle, pq, pk, pv, left, right, po, _stream(stream)), "vst_enc_offline")
 
     def check(self, stream=None) -> int:
         return lib().vst_offline_check(self.handle, _stream(stream))
@@ -313,8 +333,8 @@ def offline_bytes(module_handle: int, B: int, T: int) -> int:
 
 def dec_append(c: int, k, v, n: int | None = None, stream=None):
     n = k.shape[0] if n is None else n
-    _need_io(_ctx_cfg.get(c), n, None, k, v, None)
-    _check(lib().vst_dec_append(c, _ptr(k), _ptr(v), n, _stream(stream)), "vst_dec_append")
+    _, pk, pv, _ = _io(_ctx_cfg.get(c), n, None, k, v, None)
+    _check(lib().vst_dec_append(c, pk, pv, n, _stream(stream)), "vst_dec_append")
 
 
 class Module:

@@ -112,21 +112,43 @@ def test_enc_plan_hand_cases():
     assert steps == [(50, 0)] and (n_kv, base) == (1536, 0)
 
 
+class _FakeCudaTensor:
+    """Stands in for a CUDA tensor in the binding's checks (no GPU here)."""
+
+    def __init__(self, n, dtype=None, cuda=True, contiguous=True):
+        import torch
+        self.n, self.dtype, self.is_cuda, self.contig = n, dtype or torch.bfloat16, cuda, contiguous
+
+    def numel(self):
+        return self.n
+
+    def is_contiguous(self):
+        return self.contig
+
+    def data_ptr(self):
+        return 0x1000
+
+
 def test_binding_refuses_short_tensors():
     """The binding checks every tensor against the rows the call reads or writes before it
-    reaches the library (whose pointers carry no size)."""
+    reaches the library (whose pointers carry no size), and refuses anything but contiguous
+    bf16 CUDA tensors."""
     import torch
     cfg = vst.config_default(vst.ENC)
     rows, hd = 10, cfg.n_heads * cfg.head_dim
-    full = torch.empty(rows * hd, dtype=torch.bfloat16)
-    vst._need_io(cfg, rows, full, full, full, full)
-    short = torch.empty(rows * hd - 1, dtype=torch.bfloat16)
-    for i in range(4):
-        args = [full] * 4
-        args[i] = short
-        with pytest.raises(ValueError):
-            vst._need_io(cfg, rows, *args)
-    vst._need_io(None, rows, short, short, short, short)  # unknown ctx: nothing to check against
+    hkd = cfg.n_kv_heads * cfg.head_dim
+    full, full_kv = _FakeCudaTensor(rows * hd), _FakeCudaTensor(rows * hkd)
+    assert vst._io(cfg, rows, full, full_kv, full_kv, full) == (0x1000,) * 4
+    assert vst._io(cfg, rows, None, 5, full_kv, None) == (0, 5, 0x1000, 0)  # None and raw pointers pass
+    for i, n in enumerate((rows * hd, rows * hkd, rows * hkd, rows * hd)):
+        for b in (_FakeCudaTensor(n - 1), _FakeCudaTensor(n, dtype=torch.float16), _FakeCudaTensor(n, cuda=False),
+                  _FakeCudaTensor(n, contiguous=False), torch.empty(n, dtype=torch.bfloat16)):
+            args = [full, full_kv, full_kv, full]
+            args[i] = b
+            with pytest.raises(ValueError):
+                vst._io(cfg, rows, *args)
+    short = _FakeCudaTensor(1)
+    assert vst._io(None, rows, short, short, short, short) == (0x1000,) * 4  # unknown ctx: no size to check
 
 
 def test_split_shape_grid_fits_the_resident_ctas():
