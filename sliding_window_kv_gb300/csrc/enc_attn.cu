@@ -317,17 +317,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             o[d] = 0.f;
         float m_run = -INFINITY, l_run = 0.f;
         float mt_prev = -INFINITY;  // tile-local max of the previous tile, folded one tile late
-        uint32_t ph = 0;
+        float l_prev = 0.f;         // this thread's half of the previous tile's sum
         int fail = qfail;
-        // o <- fold(o, O_t) for the tile in TMEM buffer b, with m_t = mt and l_t from red_l
-        // (both halves' sums, ordered before this read by a pair barrier)
-        auto fold_from = [&](int b, float mt) {
-            if (mbar_wait(bar(kBarO + b), (ph >> (kBarO + b)) & 1u))
-                ph ^= 1u << (kBarO + b);
-            else
+        const int n_t = (int)(t_hi - t_lo + 1);
+        // o <- fold(o, O_i) for tile i of the CTA, in TMEM buffer i & 1, with m_t = mt and
+        // l_t = l_prev + the partner's half (ordered before this read by a pair barrier; the
+        // sum is the same in either order)
+        auto fold_from = [&](int i, float mt) {
+            const int b = i & 1;
+            if (!mbar_wait(bar(kBarO + b), (uint32_t)((i >> 1) & 1)))
                 fail = 1;
             tc_fence_after();
-            const float lt = __fadd_rn(red_l[(b * 2 + 0) * 128 + r], red_l[(b * 2 + 1) * 128 + r]);
+            const float lt = __fadd_rn(l_prev, red_l[(b * 2 + (half ^ 1)) * 128 + r]);
             // in two groups of 16 dims (the same operations per dim as one group of 32)
             const enc::FoldCoef f = enc::fold_coef(m_run, mt);
 #pragma unroll
@@ -347,22 +348,27 @@ __global__ void __launch_bounds__(kThreads, 2)
                 enc::fold_finish(m_run, l_run, lt, f);
         };
 
-        for (long long t = t_lo; t <= t_hi; ++t, rel += 128) {
-            const int b = (int)((t - t_lo) & 1), nb = b ^ 1;
+        for (int i = 0; i < n_t; ++i, rel += 128) {
+            const int b = i & 1;
 
-            // ---- S_t: this thread's 64 columns of row r, as two quarters of 32
-            if (mbar_wait(bar(kBarS + b), (ph >> (kBarS + b)) & 1u))
-                ph ^= 1u << (kBarS + b);
-            else
+            // ---- S_i: this thread's 64 columns of row r, as two quarters of 32
+            if (!mbar_wait(bar(kBarS + b), (uint32_t)((i >> 1) & 1)))
                 fail = 1;
             tc_fence_after();
             const uint32_t tm_s = tmem + 128u * b + lane_base + 64 * half;  // this thread's columns
-            int lo = 1, hi = 0;  // visible columns of row r in this tile; empty unless r is real
-            if (row_real) {
-                lo = max(-1, min(128, r - c.W + 1 - rel));
-                hi = max(-1, min(128, min(r + c.right, kl) - rel));
+            // Every column visible to every row of the CTA (the same answer in all threads):
+            // no per-column masks.
+            const bool interior = nrows == 128 && rel >= 128 - c.W && min(c.right, kl) - rel >= 127;
+            uint32_t mask0 = 0xffffffffu, mask1 = 0xffffffffu;
+            if (!interior) {
+                int lo = 1, hi = 0;  // visible columns of row r in this tile; empty unless r is real
+                if (row_real) {
+                    lo = max(-1, min(128, r - c.W + 1 - rel));
+                    hi = max(-1, min(128, min(r + c.right, kl) - rel));
+                }
+                mask0 = enc::visible_mask(64 * half, lo, hi);
+                mask1 = enc::visible_mask(64 * half + 32, lo, hi);
             }
-            const uint32_t mask0 = enc::visible_mask(64 * half, lo, hi), mask1 = enc::visible_mask(64 * half + 32, lo, hi);
 
             // ---- tile-local row max of row r, one quarter at a time
             float mh;
@@ -370,49 +376,53 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint32_t sv[32];
                 tmem_ld_32x32b_x32(tm_s, sv);
                 tmem_ld_wait();
-                mh = enc::quarter_max(sv, mask0);
+                mh = interior ? enc::quarter_max_all(sv) : enc::quarter_max(sv, mask0);
                 tmem_ld_32x32b_x32(tm_s + 32, sv);
                 tmem_ld_wait();
-                mh = fmaxf(mh, enc::quarter_max(sv, mask1));
+                mh = fmaxf(mh, interior ? enc::quarter_max_all(sv) : enc::quarter_max(sv, mask1));
             }
             red_m[(b * 2 + half) * 128 + r] = mh;
             if (bar_sync_or(pair_bar, 64, fail)) {  // also orders the partner's l of the previous tile
                 aborted = 1;
                 break;
             }
-            const float mt = __fmul_rn(fmaxf(red_m[(b * 2) * 128 + r], red_m[(b * 2 + 1) * 128 + r]), c.scale_log2);
+            // the two halves' maxima (exact, so the same in either order)
+            const float mt = __fmul_rn(fmaxf(mh, red_m[(b * 2 + (half ^ 1)) * 128 + r]), c.scale_log2);
 
             // ---- fold of the previous tile (its PV ran while this tile's max was taken); frees its
-            // buffer for S_{t+1}
-            if (t > t_lo) {
-                fold_from(nb, mt_prev);
+            // buffer for S_{i+1}
+            if (i > 0) {
+                fold_from(i - 1, mt_prev);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(bar(kBarFree + nb));
+                    mbar_arrive(bar(kBarFree + (b ^ 1)));
             }
 
-            // ---- tile-local exps, quarter by quarter (S_t read again); P_t over this thread's
+            // ---- tile-local exps, quarter by quarter (S_i read again); P_i over this thread's
             // scores already read
             float l0, l1;
             {
+                auto st0 = [&](int qd, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+                    tmem_st_32x32b_x4(tm_s + 4 * qd, w0, w1, w2, w3);
+                };
+                auto st1 = [&](int qd, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+                    tmem_st_32x32b_x4(tm_s + 16 + 4 * qd, w0, w1, w2, w3);
+                };
                 uint32_t sv[32];
                 tmem_ld_32x32b_x32(tm_s, sv);
                 tmem_ld_wait();
-                l0 = enc::quarter_exp_to(sv, mask0, c.scale_log2, -mt,
-                                         [&](int qd, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
-                                             tmem_st_32x32b_x4(tm_s + 4 * qd, w0, w1, w2, w3);
-                                         });
+                l0 = interior ? enc::quarter_exp_core<false>(sv, mask0, c.scale_log2, -mt, st0)
+                              : enc::quarter_exp_to(sv, mask0, c.scale_log2, -mt, st0);
                 tmem_ld_32x32b_x32(tm_s + 32, sv);
                 tmem_ld_wait();
-                l1 = enc::quarter_exp_to(sv, mask1, c.scale_log2, -mt,
-                                         [&](int qd, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
-                                             tmem_st_32x32b_x4(tm_s + 16 + 4 * qd, w0, w1, w2, w3);
-                                         });
+                l1 = interior ? enc::quarter_exp_core<false>(sv, mask1, c.scale_log2, -mt, st1)
+                              : enc::quarter_exp_to(sv, mask1, c.scale_log2, -mt, st1);
             }
-            red_l[(b * 2 + half) * 128 + r] = __fadd_rn(l0, l1);
+            l_prev = __fadd_rn(l0, l1);
+            red_l[(b * 2 + half) * 128 + r] = l_prev;
             tmem_st_wait();
-            tc_fence_before();  // P_t written (and S_t read) before the MMAs use the columns
+            tc_fence_before();  // P_i written (and S_i read) before the MMAs use the columns
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar(kBarP + half));
@@ -422,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!aborted && bar_sync_or(pair_bar, 64, fail))  // orders the partner's l of the last tile
             aborted = 1;
         if (!aborted) {
-            fold_from((int)((t_hi - t_lo) & 1), mt_prev);
+            fold_from(n_t - 1, mt_prev);
             if (bar_sync_or(pair_bar, 64, fail))
                 aborted = 1;
         }

@@ -72,25 +72,27 @@ __device__ __forceinline__ float quarter_max(const uint32_t* sv, uint32_t mask)
     return max32(x);
 }
 
-// Probabilities of a quarter (32 columns, neg = -m_t), visible columns in `mask`, as bf16
-// pairs handed to `sink(qd, w0, w1, w2, w3)` eight columns at a time: w_i holds columns
-// 8 qd + 2i (low half) and 8 qd + 2i + 1; returns the quarter sum. Columns are taken in
-// ascending order; a hidden column is 0. Called by whole warps (the branches are taken warp
-// by warp).
-template <class Sink>
-__device__ __forceinline__ float quarter_exp_to(const uint32_t* sv, uint32_t mask, float scale_log2, float neg,
-                                                Sink&& sink)
+// Max over a quarter whose 32 columns are all visible for the whole warp.
+__device__ __forceinline__ float quarter_max_all(const uint32_t* sv)
 {
-    if (__all_sync(0xffffffffu, mask == 0u)) {  // nothing visible: P = 0 and the sum is 0, as below
+    float x[32];
 #pragma unroll
-        for (int qd = 0; qd < 4; ++qd)
-            sink(qd, 0u, 0u, 0u, 0u);
-        return 0.f;
-    }
+    for (int j = 0; j < 32; ++j)
+        x[j] = __uint_as_float(sv[j]);
+    return max32(x);
+}
+
+// Probabilities of a quarter (32 columns, neg = -m_t) as bf16 pairs handed to
+// `sink(qd, w0, w1, w2, w3)` eight columns at a time: w_i holds columns 8 qd + 2i (low half)
+// and 8 qd + 2i + 1; returns the quarter sum. Columns are taken in ascending order. With
+// kSel, a column whose bit in `mask` is clear is 0; without, every column is visible.
+template <bool kSel, class Sink>
+__device__ __forceinline__ float quarter_exp_core(const uint32_t* sv, uint32_t mask, float scale_log2, float neg,
+                                                  Sink&& sink)
+{
     // Paired fp32 operations (__ffma2_rn, __fadd2_rn) round each lane exactly as the scalar
     // operation does; l01 and l23 hold the partial sums (l0, l1) and (l2, l3).
     float2 l01 = make_float2(0.f, 0.f), l23 = make_float2(0.f, 0.f);
-    const bool full = __all_sync(0xffffffffu, mask == 0xffffffffu);  // no selects needed (whole warp)
     const float2 sc2 = make_float2(scale_log2, scale_log2), ng2 = make_float2(neg, neg);
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
@@ -101,7 +103,7 @@ __device__ __forceinline__ float quarter_exp_to(const uint32_t* sv, uint32_t mas
             const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])), sc2, ng2);
             pv[e] = ex2(x.x);
             pv[e + 1] = ex2(x.y);
-            if (!full) {
+            if (kSel) {
                 pv[e] = (mask >> j) & 1u ? pv[e] : 0.f;
                 pv[e + 1] = (mask >> (j + 1)) & 1u ? pv[e + 1] : 0.f;
             }
@@ -113,6 +115,25 @@ __device__ __forceinline__ float quarter_exp_to(const uint32_t* sv, uint32_t mas
         sink(qd, pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
     }
     return __fadd_rn(__fadd_rn(l01.x, l01.y), __fadd_rn(l23.x, l23.y));
+}
+
+// The same with the visible columns in `mask` (bit j for column j; a hidden column is 0).
+// Called by whole warps: the branches between nothing visible, everything visible and the
+// per-column selects are taken warp by warp (the selects give the same values when every
+// bit is set).
+template <class Sink>
+__device__ __forceinline__ float quarter_exp_to(const uint32_t* sv, uint32_t mask, float scale_log2, float neg,
+                                                Sink&& sink)
+{
+    if (__all_sync(0xffffffffu, mask == 0u)) {  // nothing visible: P = 0 and the sum is 0
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd)
+            sink(qd, 0u, 0u, 0u, 0u);
+        return 0.f;
+    }
+    if (__all_sync(0xffffffffu, mask == 0xffffffffu))
+        return quarter_exp_core<false>(sv, mask, scale_log2, neg, sink);
+    return quarter_exp_core<true>(sv, mask, scale_log2, neg, sink);
 }
 
 // The same for quarter q (columns [32 q, 32 q + 32)) of row `row`, written as bf16 into the
