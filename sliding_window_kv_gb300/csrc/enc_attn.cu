@@ -99,10 +99,24 @@ __global__ void __launch_bounds__(kThreads, 2)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint32_t s_tmem;
     const EncAttnCommon& c = p.c;
-    const EncAttnJob& job = p.jobs[blockIdx.z];
-    const int h = blockIdx.y;
+    // Launch order. Plain: query tile fastest, so the query tiles of a (context, head), which
+    // share most of their key tiles, run side by side and read them once into L2. With lpt
+    // (set when all the (context, head) pairs of the launch fit on the GPU at once, so that
+    // neighbouring query tiles still run together): the query tile slowest and the last one
+    // first, so that the first query tiles of a clip, which see fewer key tiles, come last and
+    // leave a shorter tail.
+    unsigned qi = blockIdx.x, hi = blockIdx.y, zi = blockIdx.z;
+    if (c.lpt) {
+        const unsigned n_hz = gridDim.y * gridDim.z;
+        const unsigned lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        qi = gridDim.x - 1 - lin / n_hz;
+        hi = (lin % n_hz) % gridDim.y;
+        zi = (lin % n_hz) / gridDim.y;
+    }
+    const EncAttnJob& job = p.jobs[zi];
+    const int h = (int)hi;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row0 = (int)blockIdx.x * 128;
+    const int row0 = (int)qi * 128;
     const int nrows = min(128, c.n_rows - row0);
     const long long p_first = job.pos0 + row0;
     const long long key_last = job.pos0 + c.n_rows - 1;  // last key of the batch

@@ -863,6 +863,7 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
             e2.appended = split ? 0 : 1;
             if (!split && !make_query_map(&e2.tmap_q, qb + ((long long)c0 * n_new + off) * H * D, D, H, b, nj, n_new))
                 return fail_all(ctxs, n_ctx);
+            e2.lpt = (long long)H * nj <= m->n_sms;
             e2.early = record_touch(s, ctxs + c0, nj);
             if (tracked(VST_K_ENC_ATTN, s, [&] {
                     return split ? launch_enc_attn_split(e2, ej, nj, grid_x, s) : launch_enc_attn(e2, ej, nj, grid_x, s);
@@ -1079,7 +1080,7 @@ vst_status vst_enc_offline(vst_offline* p, const void* q, const void* k, const v
             return VST_E_CUDA;
         // one loop-shape launch over every query tile of every clip; mask [i - left + 1, i + right - 1]
         EncAttnCommon ec{m->rope, T, H, left, T, 0, 0, 0, 1, (float)(1.4426950408889634 / std::sqrt((double)D)),
-                         right > 0 ? right - 1 : 0, m->rope_map};
+                         right > 0 ? right - 1 : 0, H * nj <= m->n_sms ? 1 : 0, m->rope_map};
         if (!make_query_map(&ec.tmap_q, qb + (long long)b0 * T * H * D, D, H, T, nj, T))
             return VST_E_UNSUPPORTED;
         const int grid_x = (T + kEncTileN - 1) / kEncTileN;

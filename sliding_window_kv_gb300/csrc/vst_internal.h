@@ -95,6 +95,7 @@ struct EncAttnCommon {
     int appended;            // 1: the batch's K'/V rows are already in the ring (loop shape)
     float scale_log2;        // log2(e) / sqrt(D)
     int right;               // keys after the query that the mask shows (loop shape; 0: causal)
+    int lpt;                 // loop shape: launch the last query tiles of every (context, head) first
     const CUtensorMap* tmap_rope;  // loop shape: over the (cos, sin) table, fp32 {D, positions}, box {D, 128}
     CUtensorMap tmap_q;      // loop shape: over this launch's queries {D, H, rows, jobs}, box {D, 1, 128, 1}, SW128
 };
