@@ -263,10 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the first key tile's new rows are rotated and stored to the ring now
     const bool staged = (t_begin + 1) * 128 > job.pos0 && stage_new_row(s, c, job, h, t_begin);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    s.tmem = s_tmem;
+    // (the loop's first CTA barrier publishes these shared-memory writes and the TMEM address)
     s.lane_base = (uint32_t)((s.warp & 3) * 32) << 16;
 
     uint32_t ph_k = 0, ph_v = 0, ph_m = 0;
@@ -296,7 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        if (__syncthreads_or(fail)) {
+        const int any_fail = __syncthreads_or(fail);
+        s.tmem = s_tmem;
+        if (any_fail) {
             aborted = 1;
             break;
         }
@@ -417,15 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(s.bar_v, ph_v);
     }
     if (!merger) {
-        // The CTA barrier orders every thread's partials before thread 0's releasing
-        // increment (cumulative), which the merger acquires.
-        __syncthreads();
+        // The CTA barrier that ended the last tile orders every thread's partials before
+        // thread 0's releasing increment (cumulative), which the merger acquires. (After a
+        // failure the partials do not matter; the count still does.)
         if (s.tid == 0)
             red_add_release_gpu(job.counters + h, 1u);
     } else {
-        if (t_end > t_begin)
+        if (t_end > t_begin) {
             __threadfence();  // this CTA's own earlier tile partials, read back from scratch below
-        __syncthreads();
+            __syncthreads();
+        }
         if (s.tid == 0) {
             // Wait until the other CTAs of (job, head) have counted themselves in, then re-arm
             // the counter for the next launch by taking their counts back out: a CTA that
