@@ -325,7 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         const uint32_t vmask = enc::visible_mask(c0, lo, hi);
         s.red_m[s.q * 128 + r] = quarter_max(sv, vmask);
-        __syncthreads();
+        // the four warps that hold rows [32 (warp & 3), +32) meet on their own barrier
+        __syncwarp();
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + (s.warp & 3)) : "memory");
         const float mraw = fmaxf(fmaxf(s.red_m[r], s.red_m[128 + r]), fmaxf(s.red_m[256 + r], s.red_m[384 + r]));
         const float mt = __fmul_rn(mraw, c.scale_log2);  // -inf when the row sees nothing here
         s.red_l[s.q * 128 + r] = quarter_exp(sv, vmask, s.q, c.scale_log2, -mt, s.sP, r);
