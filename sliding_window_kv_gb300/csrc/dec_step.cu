@@ -276,14 +276,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t ph_o = 0;
 
     for (int i = 0; i < n_tiles; ++i) {
-        // ---- S^T of tile i
+        // ---- S^T of tile i (issued by warp 0 alone: the other warps wait for its completion;
+        // if warp 0 gives up, they give up on that wait and the barrier below ends the loop)
         if (warp == 0 && !prepare_and_issue_s(i))
             fail = 1;
-        if (__syncthreads_or(fail)) {
-            aborted = 1;
-            break;
-        }
-        if (!mbar_wait(bar_s(i & 1), (uint32_t)((i >> 1) & 1)))
+        if (!fail && !mbar_wait(bar_s(i & 1), (uint32_t)((i >> 1) & 1)))
             fail = 1;
         tc_fence_after();
         if (tid == 0 && !fail && i + 1 < n_tiles)
