@@ -820,8 +820,9 @@ vst_status vst_enc_feed_batch(vst_ctx* const* ctxs, int32_t n_ctx, const void* q
                 }
             }
             if (ncj > 0) {
-                record_touch(s, cctx, ncj);
-                if (tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc, cj, ncj, s); }) != cudaSuccess)
+                CompactCommon cc2 = cc;
+                cc2.early = record_touch(s, cctx, ncj);
+                if (tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc2, cj, ncj, s); }) != cudaSuccess)
                     return fail_all(ctxs, n_ctx);
             }
             // Launch shape, same bits either way (enc_shape): the loop shape when it fills the
@@ -895,10 +896,10 @@ vst_status vst_ctx_compact(vst_ctx* c, void* stream)
     if (c->n_kv <= cfg.window)
         return VST_OK;
     DeviceGuard g(c->m->device);
-    const CompactCommon cc{cfg.n_kv_heads, cfg.ring_slots, cfg.head_dim, cfg.window};
+    CompactCommon cc{cfg.n_kv_heads, cfg.ring_slots, cfg.head_dim, cfg.window};
     const CompactJob cj{c->k_ring, c->v_ring, c->n_kv - cfg.window};
     cudaStream_t s = as_stream(stream);
-    record_touch(s, cs, 1);
+    cc.early = record_touch(s, cs, 1);
     if (tracked(VST_K_COMPACT, s, [&] { return launch_compact(cc, &cj, 1, s); }) != cudaSuccess)
         return fail_all(cs, 1);
     c->abs_base += c->n_kv - cfg.window;

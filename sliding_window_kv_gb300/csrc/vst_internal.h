@@ -64,6 +64,7 @@ struct CompactJob {
 struct CompactCommon {
     int Hk, R, D, keep;
     int split;  // CTAs per (K|V, head) plane; set by the launcher
+    int early;  // 1: the previous kernel in the stream touched none of these rings
 };
 constexpr int kCompactSplit = 2;  // CTAs per plane when no job's move overlaps itself
 
