@@ -155,13 +155,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto sV = [&](int i) { return smem + (2 + 2 * (i & 1)) * kBox; };  // V of tile i: two buffers
     auto parity = [&](int i) { return (uint32_t)(i & 1); };
     auto slot_of = [&](int i) { return (int)(((tau_lo + i) * kTile) % c.R); };
+    int k_issued = 0, v_issued = 0;  // tiles requested so far, in order (thread 0)
     auto issue_k = [&](int i) {
+        k_issued = i + 1;
         const uint32_t dst = smem_u32(sK);
         mbar_arrive_expect_tx(bar_k, 2 * kBox);
         tma_load_3d(dst, job.tmap_k, bar_k, 0, slot_of(i), g);
         tma_load_3d(dst + kBox, job.tmap_k, bar_k, 64, slot_of(i), g);
     };
     auto issue_v = [&](int i) {
+        v_issued = i + 1;
         const uint32_t dst = smem_u32(sV(i));
         mbar_arrive_expect_tx(bar_v(i), 2 * kBox);
         tma_load_3d(dst, job.tmap_v, bar_v(i), 0, slot_of(i), g);
@@ -347,9 +350,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ends this launch at zero like any other: the launch's output is undefined (the
         // error word says so), the next launch's is not.
         atomicExch(job.err, kErrTimeout);
-        mbar_wait(bar_k, 0);
-        mbar_wait(bar_v(0), 0);
-        mbar_wait(bar_v(1), 0);
+        if (k_issued > 0)  // tile i's K is the i-th completion of the K barrier
+            mbar_wait(bar_k, parity(k_issued - 1));
+        for (int i = v_issued - 2 < 0 ? 0 : v_issued - 2; i < v_issued; ++i)  // the last V of each buffer
+            mbar_wait(bar_v(i), (uint32_t)((i >> 1) & 1));
     }
     {
         // ---- this split's partial; the last CTA of (stream, g) folds all splits in order.

@@ -617,22 +617,26 @@ def test_dec_append_ring_contents(dev, dec_module):
 def test_interleaved_contexts_bit_exact(dev, enc_module, dec_module):
     """Layers of a stream are different contexts called one after another on one CUDA
     stream; a launch may then fetch its ring tiles while the previous kernel (another
-    context) is still running. Feeding three encoder contexts and three decoder contexts
-    round-robin must give the same bits as running each context alone."""
-    # encoder: 3 contexts, 900 frames each, alternating 50-frame feeds with one 300-frame feed
-    ins = [_enc_inputs(31, l, 900) for l in range(3)]
-    alone = [_feed(enc_module, *ins[l], [50] * 6 + [300] + [50] * 6)[0] for l in range(3)]
+    context) is still running, and a compaction may copy its ring beside that kernel's tail.
+    Feeding three encoder contexts and three decoder contexts round-robin must give the same
+    bits as running each context alone."""
+    # encoder: 3 contexts, 2024 frames each: 50-frame feeds, one 300-frame feed, then 512- and
+    # 50-frame feeds, so that every context compacts right after another context's attention
+    sched = [50] * 6 + [300] + [50] * 6 + [512, 50, 512, 50]
+    ins = [_enc_inputs(31, l, sum(sched)) for l in range(3)]
+    alone = [_feed(enc_module, *ins[l], sched)[0] for l in range(3)]
     ctxs = [vst.Ctx(enc_module) for _ in range(3)]
     outs = [torch.empty_like(ins[l][0], device=dev) for l in range(3)]
     dins = [[t.to(dev) for t in ins[l]] for l in range(3)]
     t = 0
-    for n in [50] * 6 + [300] + [50] * 6:
+    for n in sched:
         for l in range(3):
             q, k, v = dins[l]
             vst.enc_feed(ctxs[l].handle, q[t:t + n], k[t:t + n], v[t:t + n], outs[l][t:t + n])
         t += n
     torch.cuda.synchronize()
     for l in range(3):
+        assert vst.ctx_info_get(ctxs[l].handle).n_compactions >= 1
         assert torch.equal(outs[l], alone[l]), l
         ctxs[l].close()
     # decoder: 3 contexts with different fills, 6 steps round-robin
