@@ -44,8 +44,8 @@
 // Launch shape (loop): one CTA per (context, head, 128-query tile) folds its key tiles in
 // registers. The split shape for a single query tile (enc_attn_split.cu) gives the same
 // bits: tiles are fixed by absolute position and folded in ascending order, every row's
-// arithmetic comes from enc_common.cuh, and the P V product reads the same bf16 values
-// from tensor memory that the split shape reads from shared memory.
+// arithmetic comes from enc_common.cuh, and both shapes' P V products read the same bf16 P
+// values from tensor memory (as two N = 32 products here, one N = 64 product there).
 #include "common.cuh"
 #include "enc_common.cuh"
 #include "ptx.cuh"

@@ -17,8 +17,8 @@
 // slot n_kv_before + row. Per tile:
 //   S   = Q' K'^T      tcgen05.mma M=128 N=128 K=64, A/B K-major bf16 in smem, D in TMEM
 //   softmax            tile-local max m_t, p = 2^(s*log2e/sqrt(D) - m_t), l_t = sum p;
-//                      P -> smem as bf16
-//   O_t = P V          tcgen05.mma M=128 N=64 K=128, A = P (K-major), B = V (MN-major)
+//                      P -> TMEM as bf16 pairs, over the S columns already read
+//   O_t = P V          tcgen05.mma M=128 N=64 K=128, A = P from TMEM, B = V (MN-major smem)
 //   fold               (m, l, o) <- fold((m, l, o), (m_t, l_t, O_t)), ascending t
 // A tile where a row sees no key is skipped for that row (exact no-op).
 //
@@ -53,7 +53,7 @@ constexpr uint32_t kTileBytes = 128u * 128u;  // 128 rows x 128 B
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;
 constexpr uint32_t kOffV = kOffK + kTileBytes;
-constexpr uint32_t kOffP = kOffV + kTileBytes;       // two 64-key blocks
+constexpr uint32_t kOffP = kOffV + kTileBytes;       // the merger's own tile partial: O as [row][64] floats
 constexpr uint32_t kOffRed = kOffP + 2 * kTileBytes; // float [2][4][128]: row max / row sum quarters
 constexpr uint32_t kOffKn = kOffRed + 2 * 4 * 128 * 4; // split mode: new rows of the first key tile,
 constexpr uint32_t kOffVn = kOffKn + kTileBytes;       // K rotated and V, staged in the prologue
@@ -68,7 +68,6 @@ constexpr int kMergeGroup = 8;  // tile partials loaded together by the merger
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 64, false, true);
 
-using enc::quarter_exp;
 using enc::quarter_max;
 using enc::rotate_quarter;
 
@@ -158,13 +157,16 @@ __device__ __forceinline__ void issue_s_mma(const Cta& s, uint32_t e)
     mma_commit_if(s.bar_m, e);
 }
 
+// O = P V: A = P from tensor memory (keys [32 q, 32 q + 32) as bf16 pairs in columns
+// [32 q, 32 q + 16), written by the threads of quarter q over scores they have read; 16 keys
+// per eight columns), B = V (MN-major shared memory, 16 keys per K step).
 __device__ __forceinline__ void issue_o_mma(const Cta& s, uint32_t e)
 {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t ad = smem_desc_sw128(smem_u32(s.sP) + (kk >> 2) * kTileBytes + 32 * (kk & 3), 16, 1024);
+        const uint32_t a = s.tmem + kTmS + 32u * (kk >> 1) + 8u * (kk & 1);
         const uint64_t bd = smem_desc_sw128(smem_u32(s.sV) + 2048 * kk, kTileBytes, 1024);
-        mma_bf16_ss_if(s.tmem + kTmO, ad, bd, kIdescO, kk > 0 ? 1u : 0u, e);
+        mma_bf16_ts_if(s.tmem + kTmO, a, bd, kIdescO, kk > 0 ? 1u : 0u, e);
     }
     mma_commit_if(s.bar_m, e);
 }
@@ -330,7 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync %0, 128;" ::"r"(1 + (s.warp & 3)) : "memory");
         const float mraw = fmaxf(fmaxf(s.red_m[r], s.red_m[128 + r]), fmaxf(s.red_m[256 + r], s.red_m[384 + r]));
         const float mt = __fmul_rn(mraw, c.scale_log2);  // -inf when the row sees nothing here
-        s.red_l[s.q * 128 + r] = quarter_exp(sv, vmask, s.q, c.scale_log2, -mt, s.sP, r);
+        {
+            // P over this thread's scores already read, four columns at a time
+            const uint32_t tm_q = s.tmem + s.lane_base + kTmS + c0;
+            s.red_l[s.q * 128 + r] = enc::quarter_exp_to(
+                sv, vmask, c.scale_log2, -mt, [&](int qd, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+                    tmem_st_32x32b_x4(tm_q + 4 * qd, w0, w1, w2, w3);
+                });
+            tmem_st_wait();
+        }
 
         // ---- V of tile t in smem (new rows patched in), then O_t = P V
         if (!mbar_wait(s.bar_v, ph_v))

@@ -136,17 +136,6 @@ __device__ __forceinline__ float quarter_exp_to(const uint32_t* sv, uint32_t mas
     return quarter_exp_core<true>(sv, mask, scale_log2, neg, sink);
 }
 
-// The same for quarter q (columns [32 q, 32 q + 32)) of row `row`, written as bf16 into the
-// K-major P operand in shared memory (two 64-key blocks, 128-B swizzle).
-__device__ __forceinline__ float quarter_exp(const uint32_t* sv, uint32_t mask, int q, float scale_log2, float neg,
-                                             uint8_t* sP, int row)
-{
-    return quarter_exp_to(sv, mask, scale_log2, neg, [&](int qd, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
-        *reinterpret_cast<uint4*>(sP + (q >> 1) * kTileBytes + sw128_offset(row, (q & 1) * 4 + qd)) =
-            make_uint4(w0, w1, w2, w3);
-    });
-}
-
 // Merge of a tile-local softmax state (mt, lt, ot) into a running state (m, l, o):
 //   mn = max(m, mt), a = 2^(m - mn), b = 2^(mt - mn), l <- l a + lt b, o <- o a + ot b.
 struct FoldCoef {
